@@ -1,0 +1,464 @@
+"""Benchmark: PQ-KV decode attention on one GB300 (or N, one process each).
+
+One step = one decode step of the batch: append the current token of every
+request into the PQ code cache (encode against the request's codebooks), then
+PQ decode attention over the L cached tokens of every request, kv head and
+query head.  The cache (codebooks fitted on the first 64 tokens, all L tokens
+encoded) is built once before timing, as a serving system does at prefill.
+
+Printed: one JSON line (rank 0).  `value` = KV tokens x kv heads attended per
+second over the whole job (device-timed, inputs resident in HBM, L2 defeated
+by rotating through input copies larger than twice the L2); `e2e` = the same
+through the public API with pinned host buffers, copies in the timed region
+and the host waiting for every step's output; `roofline` = the decode kernel's
+algorithmic bytes per launch over its event-timed duration against the measured
+HBM copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded sample.
+
+  python bench.py [--steps K] [--warmup W] [--workload page1|ragged|long|qwen_gqa|tiny]
+  python bench.py --impl reference      # the CPU oracle arm
+  torchrun --nproc-per-node N bench.py --gpus N   # weak scaling, one process per GPU
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "PQ-KV decode attention: KV tokens·heads/s; code-stream GB/s as % of HBM peak"
+UNIT = "KV tokens*heads/s"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: B{w.batch} Hq{w.num_q_heads} Hkv{w.num_kv_heads} D{w.head_dim} "
+            f"M{w.num_subspaces} K{w.num_codewords} L{int(w.seq_lens.max())}"
+            + (f" ({w.total_tokens} tokens, ragged)" if w.name == "ragged" else "")
+            + (f" x{w.layers} layers" if w.layers > 1 else ""))
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and --impl reference)
+# --------------------------------------------------------------------------
+class OracleStep:
+    """The oracle's decode step (append one token per request, then decode
+    attention over all heads), request by request on the host cores.  The
+    per-request cache (oracle codebook fit + prefill encode) is built once,
+    untimed, for `n_req` requests; `run(budget_s)` cycles over them until the
+    timed work reaches the budget."""
+
+    def __init__(self, w, n_req: int = 4, layer: int = 0):
+        import oracle
+        oracle.build()
+        self.oracle, self.w = oracle, w
+        self.q = w.queries(layer)
+        M, Hkv = w.num_subspaces, w.num_kv_heads
+        self.reqs = []
+        for b in range(min(n_req, w.batch)):
+            L = int(w.seq_lens[b])
+            kv = w.kv(b, layer, 0, L)
+            samples = w.fit_samples(kv)
+            cb16, _, _, _ = oracle.kmeans_fit(samples.reshape(-1, *samples.shape[2:]), M, 256,
+                                              w.fit_iters)
+            cbs = cb16.reshape(1, Hkv, 2, M, 256, w.dsub)
+            npg = -(-L // 16)
+            pages = np.zeros((npg, Hkv, 16, 2, M), np.uint8)
+            slots = np.arange(L, dtype=np.int64)
+            oracle.encode_append(kv[:L - 1], np.zeros(L - 1, np.int32), slots[:L - 1], cbs, pages, 16)
+            self.reqs.append((b, L, kv[L - 1:L].copy(), cbs, pages,
+                              np.arange(npg, dtype=np.int32)[None]))
+
+    def run(self, budget_s: float):
+        o, w = self.oracle, self.w
+        units, elapsed, n = 0, 0.0, 0
+        while elapsed < budget_s:
+            b, L, kv_new, cbs, pages, bt = self.reqs[n % len(self.reqs)]
+            t0 = time.perf_counter()
+            o.encode_append(kv_new, np.zeros(1, np.int32), np.array([L - 1], np.int64), cbs, pages, 16)
+            o.decode_attention(self.q[b:b + 1], pages, cbs, np.zeros(1, np.int32), bt,
+                               np.array([L], np.int32), w.scale, 16)
+            elapsed += time.perf_counter() - t0
+            units += L * w.num_kv_heads
+            n += 1
+        return units, elapsed, n
+
+    def describe(self, n):
+        return (f"{n} request-steps of {self.w.name} cycling over its first {len(self.reqs)} "
+                f"requests (append 1 token + decode attention, all heads)")
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    ost = OracleStep(w)
+    # each step a bounded sample, the whole run within about two minutes
+    budget = min(4.0, 120.0 / (args.steps + args.warmup))
+    units = secs = n_tot = 0
+    for i in range(args.warmup + args.steps):
+        u, s_, n = ost.run(budget)
+        if i >= args.warmup:
+            units, secs, n_tot = units + u, secs + s_, n_tot + n
+    v = units / secs
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(w)},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": ost.oracle.num_threads(),
+                             "kind": "oracle", "sample": ost.describe(n_tot)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def build_cache(w, api, torch, layer=0):
+    """Fit codebooks (GPU) on each request's first 64 tokens and encode all L
+    tokens into pages (GPU).  Returns device tensors and the new-token K/V."""
+    Hkv, M = w.num_kv_heads, w.num_subspaces
+    kvs = w.kv_all(layer, threads=16)
+    samples = np.stack([w.fit_samples(k) for k in kvs])                 # [B][Hkv][2][N][D]
+    samples_d = torch.from_numpy(samples.reshape(-1, *samples.shape[3:])).cuda()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    cbs = api.fit_codebooks(samples_d, M, w.fit_iters)
+    t1.record()
+    torch.cuda.synchronize()
+    fit_ms = t0.elapsed_time(t1)
+    cbs = cbs.view(w.batch, Hkv, 2, M, 256, w.dsub)
+    bt, npages = w.block_table()
+    kv = np.concatenate(kvs)
+    tset = np.concatenate([np.full(len(k), b, np.int32) for b, k in enumerate(kvs)])
+    slots = np.concatenate([w.slot_mapping(bt, b, 0, len(k)) for b, k in enumerate(kvs)])
+    pages = torch.zeros((npages, Hkv, 16, 2, M), dtype=torch.uint8, device="cuda")
+    st = api.new_status()
+    kv_d = torch.from_numpy(kv).cuda()
+    t0.record()
+    api.encode_append(kv_d, torch.from_numpy(tset).cuda(), torch.from_numpy(slots).cuda(), cbs,
+                      pages, st)
+    t1.record()
+    torch.cuda.synchronize()
+    enc_ms = t0.elapsed_time(t1)
+    assert int(st.item()) == 0
+    # the decode step's "current token": the last cached token of each request
+    last = np.stack([k[-1] for k in kvs])                                # [B][Hkv][2][D]
+    last_slot = np.array([w.slot_mapping(bt, b, len(k) - 1, len(k))[0] for b, k in enumerate(kvs)],
+                         np.int64)
+    del kv_d, samples_d
+    return {"codebooks": cbs, "pages": pages, "bt": torch.from_numpy(bt).cuda(),
+            "seq_lens": torch.from_numpy(w.seq_lens).cuda(),
+            "req_set": torch.arange(w.batch, dtype=torch.int32, device="cuda"),
+            "q": torch.from_numpy(w.queries(layer)).cuda(),
+            "new_kv": torch.from_numpy(last).cuda(), "new_slot": torch.from_numpy(last_slot).cuda(),
+            "new_set": torch.arange(w.batch, dtype=torch.int32, device="cuda"),
+            "fit_ms": fit_ms, "encode_prefill_ms": enc_ms, "npages": npages, "bt_np": bt,
+            "kvs": kvs}
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    from decode_attention_product_gb300 import api, build as B, traffic as T
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+        B.build()
+    dist = world > 1
+    Lmax = int(w.seq_lens.max())
+    base = build_cache(w, api, torch)
+    M, Hq, Hkv = w.num_subspaces, w.num_q_heads, w.num_kv_heads
+    # rotation copies so that every timed step reads cold inputs (> 2 x L2)
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    per_copy = (base["codebooks"].numel() * 2 + base["pages"].numel() + base["q"].numel() * 4
+                + base["new_kv"].numel() * 2)
+    R = max(2, min(64, math.ceil(2.2 * l2 / per_copy))) if not args.no_rotate else 1
+    copies = [base] + [{k: (v.clone() if torch.is_tensor(v) and k in
+                            ("codebooks", "pages", "q", "new_kv") else v)
+                        for k, v in base.items()} for _ in range(R - 1)]
+    splits, cluster, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda") for _ in range(R)]
+    status = api.new_status()
+
+    def step(i, ev=None):
+        c = copies[i % R]
+        api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)
+        if ev is not None:
+            ev.record()
+        api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                             c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws,
+                             status=status)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    # timed region: K steps; decode-kernel events inside each step
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record()
+    for i in range(args.steps):
+        starts[i].record()
+        step(args.warmup + i, mids[i])
+    starts[args.steps].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    dec_ms = [mids[i].elapsed_time(starts[i + 1]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    units = T.kv_tokens_heads(w.seq_lens, Hkv)
+    value = world * units * args.steps / (total_ms / 1e3)
+    # roofline of the decode kernel (algorithmic bytes per launch / event time)
+    byt = T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M)
+    dec_avg_ms = float(np.mean(dec_ms))
+    peak, peak_kind = measured_peaks()
+    achieved = byt["total"] / (dec_avg_ms / 1e3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get(w.name)
+    # e2e through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist)
+    # fp16 comparison kernel on the same shape (cache of the same raw vectors)
+    fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "batch": w.batch, "seq_len": Lmax,
+                   "num_q_heads": Hq, "num_kv_heads": Hkv, "num_subspaces": M,
+                   "num_codewords": w.num_codewords, "plan": {"splits": splits, "cluster": cluster},
+                   "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB "
+                         f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)" if R > 1 else "none",
+                   "step": "append 1 token/request (encode) + PQ decode attention"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "pq_decode_kernel",
+                     "bytes_per_launch": byt["total"], "launch_ms": dec_avg_ms,
+                     "peak_kind": peak_kind},
+        "code_stream": {"gbs": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9,
+                        "codes_only_gbs": byt["codes"] / (dec_avg_ms / 1e3) / 1e9,
+                        "frac_of_peak": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9 / peak},
+        "gpu_launches": args.steps * (2 + (1 if splits > 1 else 0)),
+        "clocks": clk,
+        "prefill": {"fit_ms": base["fit_ms"], "encode_ms": base["encode_prefill_ms"]},
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if fp16:
+        line["fp16_comparison"] = fp16
+    if rank == 0 and not args.no_cpu:
+        ost = OracleStep(w)
+        units_c, secs_c, n_c = ost.run(args.cpu_budget)
+        line["cpu_baseline"] = {"value": units_c / secs_c, "unit": UNIT,
+                                "cores": ost.oracle.num_threads(), "kind": "oracle",
+                                "sample": ost.describe(n_c) + f", {secs_c:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
+    """Per step: pinned q and new K/V copied in, append + decode through the API,
+    output copied out, host waits for it."""
+    Hq = w.num_q_heads
+    q_h = torch.from_numpy(w.queries()).pin_memory()
+    kv_h = base["new_kv"].cpu().pin_memory()
+    out_h = torch.empty((w.batch, Hq, 128), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(base["q"])
+    kv_d = torch.empty_like(base["new_kv"])
+    out_d = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
+    st = api.new_status()
+
+    def one():
+        q_d.copy_(q_h, non_blocking=True)
+        kv_d.copy_(kv_h, non_blocking=True)
+        api.encode_append(kv_d, base["new_set"], base["new_slot"], base["codebooks"], base["pages"], st)
+        api.decode_attention(q_d, base["pages"], base["codebooks"], base["req_set"], base["bt"],
+                             base["seq_lens"], Lmax, w.scale, out=out_d, workspace=ws, status=st)
+        out_h.copy_(out_d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    if dist:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    secs = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([secs], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = float(t.item())
+    return {"value": world * units * args.steps / secs, "unit": UNIT,
+            "h2d_bytes_per_step": q_h.numel() * 4 + kv_h.numel() * 2,
+            "d2h_bytes_per_step": out_h.numel() * 4, "ms_per_step": 1e3 * secs / args.steps}
+
+
+def measure_fp16(args, w, api, torch, base, Lmax, units, T):
+    """The uncompressed comparison: fp16 pages of the same raw vectors."""
+    Hq, Hkv = w.num_q_heads, w.num_kv_heads
+    kvs = base["kvs"]
+    bt = base["bt_np"]
+    npages = base["npages"]
+    pages = torch.zeros((npages, Hkv, 2, 16, 128), dtype=torch.float16, device="cuda")
+    for b, k in enumerate(kvs):
+        L = len(k)
+        pad = (-L) % 16
+        kk = np.concatenate([k, np.zeros((pad, Hkv, 2, 128), np.float16)]) if pad else k
+        blk = kk.reshape(-1, 16, Hkv, 2, 128).transpose(0, 2, 3, 1, 4)   # [pg][Hkv][2][16][D]
+        idx = torch.from_numpy(bt[b, :blk.shape[0]].astype(np.int64)).cuda()
+        pages[idx] = torch.from_numpy(np.ascontiguousarray(blk)).cuda()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    per = pages.numel() * 2
+    R = max(1, min(8, math.ceil(2.2 * l2 / per)))
+    pcs = [pages] + [pages.clone() for _ in range(R - 1)]
+    splits, _, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, fp16=True)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
+    for i in range(3):
+        api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax, w.scale,
+                                  out=out, workspace=ws)
+    torch.cuda.synchronize()
+    n = max(10, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax, w.scale,
+                                  out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    byt = T.fp16_decode_bytes(w.seq_lens, Hq, Hkv)
+    peak, _ = measured_peaks()
+    del pcs, pages
+    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_call": ms,
+            "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
+            "splits": splits}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="page1", choices=list(W.NAMES))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fp16", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.make(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

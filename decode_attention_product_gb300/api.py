@@ -1,0 +1,170 @@
+"""Torch-facing wrappers of the C ABI (device memory and streams from PyTorch).
+
+Each function checks dtypes, devices and contiguity, passes raw pointers and
+the current CUDA stream to libaqpq, and raises AQError on a non-OK status.  No
+arithmetic of the method happens here.  Names follow include/aqpq.h.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+HEAD_DIM = 128
+CODEWORDS = 256
+PAGE = 16
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed int32 device_status word."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def fit_codebooks(samples: torch.Tensor, num_subspaces: int, iters: int = 10,
+                  with_assign: bool = False):
+    """Lloyd k-means codebooks from samples [U][N][D] fp16 -> fp16 [U][M][K][Dsub]."""
+    _need(samples, torch.float16, "samples", 3)
+    U, N, D = samples.shape
+    M = num_subspaces
+    cb = torch.empty((U, M, CODEWORDS, D // M), dtype=torch.float16, device=samples.device)
+    asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
+    cfg = _lib.config(M, head_dim=D)
+    st = _lib.load().aq_fit_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(cb),
+                                      _ptr(asg), _stream())
+    _lib.check(st, "aq_fit_codebooks")
+    return (cb, asg) if with_assign else cb
+
+
+def kmeans_step(samples: torch.Tensor, centroids: torch.Tensor):
+    """One Lloyd step from fp32 centroids [U][M][K][Dsub]: (centroids_out, assign)."""
+    _need(samples, torch.float16, "samples", 3)
+    _need(centroids, torch.float32, "centroids", 4)
+    U, N, D = samples.shape
+    M = centroids.shape[1]
+    out = torch.empty_like(centroids)
+    asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device)
+    cfg = _lib.config(M, head_dim=D)
+    st = _lib.load().aq_kmeans_step(ctypes.byref(cfg), U, N, _ptr(samples), _ptr(centroids),
+                                    _ptr(out), _ptr(asg), _stream())
+    _lib.check(st, "aq_kmeans_step")
+    return out, asg
+
+
+def encode_append(kv: torch.Tensor, token_set: torch.Tensor, slot_mapping: torch.Tensor,
+                  codebooks: torch.Tensor, code_pages: torch.Tensor,
+                  status: torch.Tensor | None = None) -> None:
+    """Encode kv [T][Hkv][2][D] fp16 into code_pages [NP][Hkv][P][2][M] uint8 (in place)."""
+    _need(kv, torch.float16, "kv", 4)
+    _need(token_set, torch.int32, "token_set", 1)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(codebooks, torch.float16, "codebooks", 6)
+    _need(code_pages, torch.uint8, "code_pages", 5)
+    T, Hkv, _, D = kv.shape
+    M = codebooks.shape[3]
+    cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
+    st = _lib.load().aq_encode_append(
+        ctypes.byref(cfg), T, Hkv, _ptr(kv), _ptr(token_set), _ptr(slot_mapping), _ptr(codebooks),
+        codebooks.shape[0], _ptr(code_pages), code_pages.shape[0], _ptr(status), _stream())
+    _lib.check(st, "aq_encode_append")
+
+
+def decode_plan(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int,
+                num_subspaces: int = 4, num_splits: int = 0, fp16: bool = False):
+    """(num_splits, cluster_size, workspace_bytes) a decode call will use."""
+    cfg = _lib.config(num_subspaces)
+    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    st = _lib.load().aq_decode_plan(ctypes.byref(cfg), batch, num_q_heads, num_kv_heads,
+                                    max_seq_len, num_splits, int(fp16), ctypes.byref(s),
+                                    ctypes.byref(c), ctypes.byref(w))
+    _lib.check(st, "aq_decode_plan")
+    return s.value, c.value, w.value
+
+
+def workspace_for(batch, num_q_heads, num_kv_heads, max_seq_len, num_subspaces=4, num_splits=0,
+                  fp16=False, device="cuda"):
+    """A device workspace of the size the planned call needs (None when 0)."""
+    _, _, w = decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_subspaces,
+                          num_splits, fp16)
+    return torch.empty(w, dtype=torch.uint8, device=device) if w else None
+
+
+def decode_attention(q: torch.Tensor, code_pages: torch.Tensor, codebooks: torch.Tensor,
+                     req_set: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                     max_seq_len: int, scale: float | None = None, num_splits: int = 0,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None) -> torch.Tensor:
+    """PQ decode attention; returns out [B][Hq][D] fp32."""
+    _need(q, torch.float32, "q", 3)
+    _need(code_pages, torch.uint8, "code_pages", 5)
+    _need(codebooks, torch.float16, "codebooks", 6)
+    _need(req_set, torch.int32, "req_set", 1)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    Hkv, M = codebooks.shape[1], codebooks.shape[3]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
+    cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
+    st = _lib.load().aq_decode_attention(
+        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(code_pages), code_pages.shape[0],
+        _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), max_seq_len, float(scale), num_splits, _ptr(out), _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _ptr(status), _stream())
+    _lib.check(st, "aq_decode_attention")
+    return out
+
+
+def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                          seq_lens: torch.Tensor, max_seq_len: int, scale: float | None = None,
+                          num_splits: int = 0, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None) -> torch.Tensor:
+    """fp16-cache decode attention (the comparison point); kv_pages [NP][Hkv][2][P][D]."""
+    _need(q, torch.float32, "q", 3)
+    _need(kv_pages, torch.float16, "kv_pages", 5)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    Hkv = kv_pages.shape[1]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(B, Hq, Hkv, max_seq_len, 4, num_splits, fp16=True, device=q.device)
+    cfg = _lib.config(4, head_dim=D, page_size=kv_pages.shape[3])
+    st = _lib.load().aq_decode_attention_fp16(
+        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_pages), kv_pages.shape[0],
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
+        num_splits, _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+        _ptr(status), _stream())
+    _lib.check(st, "aq_decode_attention_fp16")
+    return out

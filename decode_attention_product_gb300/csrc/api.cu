@@ -1,0 +1,295 @@
+// api.cu -- the extern "C" boundary of libaqpq (declared in include/aqpq.h):
+// host-side argument checks (before any CUDA call), work planning, dispatch to
+// the kernel launchers and mapping of CUDA errors to AQ_ERR_CUDA.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "aqpq.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace aq {
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+aq_status cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return AQ_ERR_CUDA;
+}
+
+aq_status check_cfg(const aq_pq_config *cfg, bool need_pq) {
+    if (!cfg) return AQ_ERR_INVALID_ARGUMENT;
+    if (cfg->head_dim <= 0 || cfg->page_size <= 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (cfg->head_dim != kHeadDim || cfg->page_size != kPage) return AQ_ERR_UNSUPPORTED;
+    if (!need_pq) return AQ_OK;
+    if (cfg->num_subspaces <= 0 || cfg->num_codewords <= 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (cfg->head_dim % cfg->num_subspaces != 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (cfg->num_codewords > 256) return AQ_ERR_INVALID_ARGUMENT;      // uint8 codes
+    if (cfg->num_codewords != kCodewords) return AQ_ERR_UNSUPPORTED;
+    if (cfg->num_subspaces != 4 && cfg->num_subspaces != 8) return AQ_ERR_UNSUPPORTED;
+    return AQ_OK;
+}
+
+bool group_ok(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+
+}  // namespace
+
+// The plan is a pure function of the arguments (no device query), so that
+// aq_decode_plan and the decode call always agree: it is sized for GB300
+// (152 SMs, 227 KiB of opt-in shared memory per CTA).
+constexpr int kPlanSMs = 152;
+constexpr size_t kPlanSmemCap = 232448;
+
+// Work plan of a decode call.  Host-only arithmetic; `sms` is the SM count.
+//   PQ:   cluster C = 4 CTAs per split when M >= 4 (each owns M/C subspaces of
+//         both codebooks, so every codebook byte is read once and a split's
+//         tokens spread over 4 SMs), smaller if shared memory does not fit.
+//         Splits are added only when (request, kv head) clusters cannot fill
+//         the GPU and each split keeps >= 1024 tokens, since every split
+//         re-reads the codebooks.
+//   fp16: splits so that (request, kv head, split) CTAs reach 2 per SM, each
+//         keeping >= 256 tokens.
+static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
+                           int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
+    const int P = cfg->page_size;
+    const int G = Hq / Hkv;
+    const int64_t units = static_cast<int64_t>(batch) * Hkv;
+    const int max_pages_needed = (max_seq_len + P - 1) / P;
+    int C = 1;
+    if (!fp16) {
+        const int M = cfg->num_subspaces;
+        C = 0;
+        for (int c = 4; c >= 1; c /= 2)
+            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
+        if (C == 0) return AQ_ERR_UNSUPPORTED;
+    }
+    int S = req;
+    if (S <= 0) {
+        const int64_t target = 2ll * sms;
+        const int min_tok = fp16 ? 256 : 1024;
+        const int64_t per_split_ctas = units * C;
+        S = 1;
+        if (per_split_ctas > 0 && per_split_ctas < target) {
+            const int64_t want = (target + per_split_ctas - 1) / per_split_ctas;
+            const int64_t cap = max_seq_len / min_tok;
+            S = static_cast<int>(want < cap ? want : cap);
+            if (S < 1) S = 1;
+        }
+    }
+    if (S > 1024) S = 1024;
+    if (max_pages_needed == 0) S = 1;
+    // split length: page multiple; recompute S so no trailing split is empty
+    int split_pages = (max_pages_needed + S - 1) / S;
+    if (split_pages < 1) split_pages = 1;
+    S = (max_pages_needed + split_pages - 1) / split_pages;
+    if (S < 1) S = 1;
+    pl->num_splits = S;
+    pl->cluster = C;
+    pl->split_len = split_pages * P;
+    pl->workspace = S > 1 ? static_cast<size_t>(batch) * Hq * S * (kHeadDim + 2) * sizeof(float) : 0;
+    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C);
+    return AQ_OK;
+}
+
+}  // namespace aq
+
+using namespace aq;
+
+extern "C" {
+
+const char *aq_status_string(aq_status s) {
+    switch (s) {
+        case AQ_OK: return "AQ_OK";
+        case AQ_ERR_INVALID_ARGUMENT: return "AQ_ERR_INVALID_ARGUMENT";
+        case AQ_ERR_UNSUPPORTED: return "AQ_ERR_UNSUPPORTED";
+        case AQ_ERR_WORKSPACE_TOO_SMALL: return "AQ_ERR_WORKSPACE_TOO_SMALL";
+        case AQ_ERR_CUDA: return "AQ_ERR_CUDA";
+        default: return "AQ_ERR_UNKNOWN";
+    }
+}
+
+const char *aq_last_error_message(void) { return aq::g_last_error; }
+
+const char *aq_version(void) { return "aqpq 0.1 sm_103a"; }
+
+aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
+                           int32_t iters, const void *samples_f16, void *codebooks_f16,
+                           int32_t *assign_out, aq_stream_t stream) {
+    aq_status st = check_cfg(cfg, true);
+    if (st != AQ_OK) return st;
+    if (num_units < 0 || n_samples < 1 || iters < 1 || iters > 1000) return AQ_ERR_INVALID_ARGUMENT;
+    if (n_samples > 1024) return AQ_ERR_UNSUPPORTED;
+    if (num_units > 0 && (!samples_f16 || !codebooks_f16)) return AQ_ERR_INVALID_ARGUMENT;
+    if (num_units > 2147483647ll) return AQ_ERR_UNSUPPORTED;
+    if (num_units == 0) return AQ_OK;
+    FitParams p{};
+    p.samples = samples_f16;
+    p.codebooks = codebooks_f16;
+    p.assign = assign_out;
+    p.num_units = num_units;
+    p.n_samples = n_samples;
+    p.iters = iters;
+    cudaError_t e = launch_fit(p, cfg->num_subspaces, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
+aq_status aq_kmeans_step(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
+                         const void *samples_f16, const float *centroids_in, float *centroids_out,
+                         int32_t *assign_out, aq_stream_t stream) {
+    aq_status st = check_cfg(cfg, true);
+    if (st != AQ_OK) return st;
+    if (num_units < 0 || n_samples < 1) return AQ_ERR_INVALID_ARGUMENT;
+    if (n_samples > 1024) return AQ_ERR_UNSUPPORTED;
+    if (num_units > 0 && (!samples_f16 || !centroids_in || !centroids_out || !assign_out))
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (num_units > 2147483647ll) return AQ_ERR_UNSUPPORTED;
+    if (num_units == 0) return AQ_OK;
+    FitParams p{};
+    p.samples = samples_f16;
+    p.cent_in = centroids_in;
+    p.cent_out = centroids_out;
+    p.assign = assign_out;
+    p.num_units = num_units;
+    p.n_samples = n_samples;
+    p.iters = 1;
+    cudaError_t e = launch_fit(p, cfg->num_subspaces, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
+aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens, int32_t num_kv_heads,
+                           const void *kv_f16, const int32_t *token_set, const int64_t *slot_mapping,
+                           const void *codebooks_f16, int64_t num_sets, uint8_t *code_pages,
+                           int64_t num_pages, int32_t *device_status, aq_stream_t stream) {
+    aq_status st = check_cfg(cfg, true);
+    if (st != AQ_OK) return st;
+    if (num_tokens < 0 || num_kv_heads < 1 || num_kv_heads > 65535 || num_sets < 0 || num_pages < 0)
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return AQ_OK;
+    if (!kv_f16 || !token_set || !slot_mapping || !codebooks_f16 || !code_pages)
+        return AQ_ERR_INVALID_ARGUMENT;
+    EncodeParams p{};
+    p.kv = kv_f16;
+    p.token_set = token_set;
+    p.slot_mapping = slot_mapping;
+    p.codebooks = codebooks_f16;
+    p.code_pages = code_pages;
+    p.status = device_status;
+    p.num_tokens = num_tokens;
+    p.num_kv_heads = num_kv_heads;
+    p.num_sets = num_sets;
+    p.num_pages = num_pages;
+    cudaError_t e = launch_encode(p, cfg->num_subspaces, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
+static aq_status check_decode_common(const aq_pq_config *cfg, bool need_pq, int32_t batch, int32_t Hq,
+                                     int32_t Hkv, int32_t max_pages, int32_t max_seq_len,
+                                     int32_t num_splits) {
+    aq_status st = check_cfg(cfg, need_pq);
+    if (st != AQ_OK) return st;
+    if (batch < 0 || Hq < 1 || Hkv < 1 || max_pages < 0 || max_seq_len < 0 || num_splits < 0)
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (Hq % Hkv != 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (!group_ok(Hq / Hkv)) return AQ_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * cfg->page_size)
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (batch > 65535 || Hkv > 65535) return AQ_ERR_UNSUPPORTED;
+    return AQ_OK;
+}
+
+aq_status aq_decode_plan(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t max_seq_len, int32_t num_splits_req,
+                         int32_t fp16, int32_t *num_splits, int32_t *cluster_size,
+                         size_t *workspace_bytes) {
+    const int P = cfg ? cfg->page_size : 1;
+    aq_status st = check_decode_common(cfg, !fp16, batch, num_q_heads, num_kv_heads,
+                                       P > 0 ? (max_seq_len + P - 1) / P : 0, max_seq_len,
+                                       num_splits_req);
+    if (st != AQ_OK) return st;
+    Plan pl{};
+    st = make_plan(cfg, batch, num_q_heads, num_kv_heads, max_seq_len, num_splits_req, fp16 != 0,
+                   kPlanSMs, kPlanSmemCap, &pl);
+    if (st != AQ_OK) return st;
+    if (num_splits) *num_splits = pl.num_splits;
+    if (cluster_size) *cluster_size = pl.cluster;
+    if (workspace_bytes) *workspace_bytes = pl.workspace;
+    return AQ_OK;
+}
+
+static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, int32_t Hq, int32_t Hkv,
+                             const float *q, const uint8_t *code_pages, const void *kv_pages,
+                             int64_t num_pages, const void *codebooks, int64_t num_sets,
+                             const int32_t *req_set, const int32_t *block_table, int32_t max_pages,
+                             const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                             int32_t num_splits, float *out, void *ws, size_t ws_bytes,
+                             int32_t *device_status, aq_stream_t stream) {
+    aq_status st = check_decode_common(cfg, !fp16, batch, Hq, Hkv, max_pages, max_seq_len, num_splits);
+    if (st != AQ_OK) return st;
+    if (!std::isfinite(scale)) return AQ_ERR_INVALID_ARGUMENT;
+    if (num_pages < 0 || num_sets < 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (batch == 0) return AQ_OK;
+    if (!q || !out || !block_table || !seq_lens) return AQ_ERR_INVALID_ARGUMENT;
+    if (fp16 ? !kv_pages : (!code_pages || !codebooks || !req_set)) return AQ_ERR_INVALID_ARGUMENT;
+    if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
+    Plan pl{};
+    st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl);
+    if (st != AQ_OK) return st;
+    if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return AQ_ERR_WORKSPACE_TOO_SMALL;
+    DecodeParams p{};
+    p.q = q;
+    p.code_pages = code_pages;
+    p.codebooks = codebooks;
+    p.kv_pages = kv_pages;
+    p.req_set = req_set;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    if (pl.num_splits > 1) {
+        p.part_o = static_cast<float *>(ws);
+        p.part_ml = p.part_o + static_cast<size_t>(batch) * Hq * pl.num_splits * kHeadDim;
+    }
+    p.status = device_status;
+    p.batch = batch;
+    p.num_q_heads = Hq;
+    p.num_kv_heads = Hkv;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.num_sets = num_sets;
+    p.max_seq_len = max_seq_len;
+    p.num_splits = pl.num_splits;
+    p.split_len = pl.split_len;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = fp16 ? launch_fp16_decode(p, Hq / Hkv, pl, s)
+                         : launch_pq_decode(p, cfg->num_subspaces, Hq / Hkv, pl, s);
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
+aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, const float *q, const uint8_t *code_pages,
+                              int64_t num_pages, const void *codebooks_f16, int64_t num_sets,
+                              const int32_t *req_set, const int32_t *block_table, int32_t max_pages,
+                              const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                              int32_t num_splits, float *out, void *workspace, size_t workspace_bytes,
+                              int32_t *device_status, aq_stream_t stream) {
+    return decode_impl(cfg, false, batch, num_q_heads, num_kv_heads, q, code_pages, nullptr, num_pages,
+                       codebooks_f16, num_sets, req_set, block_table, max_pages, seq_lens, max_seq_len,
+                       scale, num_splits, out, workspace, workspace_bytes, device_status, stream);
+}
+
+aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                                   int32_t num_kv_heads, const float *q, const void *kv_pages_f16,
+                                   int64_t num_pages, const int32_t *block_table, int32_t max_pages,
+                                   const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                                   int32_t num_splits, float *out, void *workspace,
+                                   size_t workspace_bytes, int32_t *device_status, aq_stream_t stream) {
+    return decode_impl(cfg, true, batch, num_q_heads, num_kv_heads, q, nullptr, kv_pages_f16, num_pages,
+                       nullptr, 0, nullptr, block_table, max_pages, seq_lens, max_seq_len, scale,
+                       num_splits, out, workspace, workspace_bytes, device_status, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// fit.cu -- codebook fit by Lloyd k-means (AQPIM blog §3.2 item 2 and §5.2
+// item 1: per-sequence codebooks initialised from its first tokens by a quick
+// k-means on a small sample set).
+//
+// One CTA per (unit, subspace).  The unit's N samples (sub-vectors, fp16) and
+// the 256 centroids (fp32, plus their fp16 rounding) live in shared memory.
+// One step:
+//   assign  each sample to its nearest centroid: fp32 squared distance with
+//           separately rounded subtract / multiply / add in increasing j, ties
+//           to the lowest index (the same decision rule as encode);
+//   update  each centroid with members to their mean.  Member sums are formed
+//           exactly: an fp16 value is an integer multiple of 2^-24 below 2^16,
+//           so x * 2^24 is an int64 and sums of up to 1024 of them are exact in
+//           int64 and in double.  The mean is that exact sum divided by the
+//           count in double (correctly rounded), then rounded to fp32 for the
+//           next assignment and to fp16 (nearest even) for the codebook.  A
+//           centroid without members keeps both values.
+// Initial centroid k is sample (k mod N).
+#include "common.cuh"
+#include "internal.h"
+
+namespace aq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxSamples = 1024;
+
+template <int M>
+struct FitCfg {
+    static constexpr int D = kHeadDim, K = kCodewords, DSUB = D / M;
+    static constexpr int CSTR = DSUB + 4;                   // padded fp32 centroid row
+    static size_t smem(int n) {
+        size_t b = 0;
+        b += static_cast<size_t>(K) * DSUB * 8;             // isum  int64 [K][DSUB]
+        b += static_cast<size_t>(K) * CSTR * 4;             // cent  fp32  [K][CSTR]
+        b += static_cast<size_t>(K) * DSUB * 2;             // c16   fp16  [K][DSUB]
+        b += static_cast<size_t>(n) * DSUB * 2;             // xs    fp16  [N][DSUB]
+        b += static_cast<size_t>(n) * 4;                    // assign int  [N]
+        b += static_cast<size_t>(K) * 4;                    // cnt   int   [K]
+        return b + 64;
+    }
+};
+
+__device__ __forceinline__ float sqdist_step(float acc, float x, float c) {
+    const float e = __fsub_rn(x, c);
+    return __fadd_rn(acc, __fmul_rn(e, e));
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ FitParams p) {
+    using F = FitCfg<M>;
+    constexpr int D = F::D, K = F::K, DSUB = F::DSUB, CSTR = F::CSTR;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int N = p.n_samples;
+    long long *isum = reinterpret_cast<long long *>(smem);
+    float *cent = reinterpret_cast<float *>(isum + K * DSUB);
+    __half *c16 = reinterpret_cast<__half *>(cent + K * CSTR);
+    __half *xs = c16 + K * DSUB;
+    int *asg = reinterpret_cast<int *>(xs + static_cast<size_t>(N) * DSUB);
+    int *cnt = asg + N;
+
+    const int64_t u = blockIdx.x;
+    const int m = blockIdx.y, tid = threadIdx.x;
+    const __half *src = reinterpret_cast<const __half *>(p.samples) + static_cast<size_t>(u) * N * D + m * DSUB;
+    for (int i = tid; i < N * DSUB; i += kThreads) xs[i] = src[(i / DSUB) * D + (i % DSUB)];
+    __syncthreads();
+    const size_t cbase = (static_cast<size_t>(u) * M + m) * K * DSUB;
+    for (int i = tid; i < K * DSUB; i += kThreads) {
+        const int k = i / DSUB, j = i % DSUB;
+        if (p.cent_in) {
+            cent[k * CSTR + j] = p.cent_in[cbase + i];
+        } else {
+            const __half h = xs[(k % N) * DSUB + j];
+            cent[k * CSTR + j] = __half2float(h);
+            c16[i] = h;
+        }
+    }
+    __syncthreads();
+
+    // assignment mapping: NCH threads per sample, each over K / NCH centroids
+    int nch = 1;
+    while (nch < 8 && nch * 2 * N <= kThreads) nch *= 2;
+    const int spass = kThreads / nch;                        // samples per pass
+    const int ch = tid % nch, kspan = K / nch;
+    const int iters = p.cent_in ? 1 : p.iters;
+    for (int it = 0; it < iters; ++it) {
+        for (int n0 = 0; n0 < N; n0 += spass) {
+            const int n = n0 + tid / nch;
+            unsigned long long key = ~0ull;
+            if (n < N) {
+                float x[DSUB];
+#pragma unroll
+                for (int j = 0; j < DSUB; ++j) x[j] = __half2float(xs[n * DSUB + j]);
+                float best = INFINITY;
+                int bk = 0;
+                for (int i = 0; i < kspan; ++i) {
+                    const int k = ch * kspan + ((i + ch) % kspan);   // staggered: no bank conflicts
+                    const float4 *c4 = reinterpret_cast<const float4 *>(cent + k * CSTR);
+                    float d = 0.f;
+#pragma unroll
+                    for (int j = 0; j < DSUB; j += 4) {
+                        const float4 c = c4[j / 4];
+                        d = sqdist_step(d, x[j], c.x);
+                        d = sqdist_step(d, x[j + 1], c.y);
+                        d = sqdist_step(d, x[j + 2], c.z);
+                        d = sqdist_step(d, x[j + 3], c.w);
+                    }
+                    if (d < best || (d == best && k < bk)) { best = d; bk = k; }
+                }
+                key = (static_cast<unsigned long long>(__float_as_uint(best)) << 32) | static_cast<unsigned>(bk);
+            }
+            for (int off = 1; off < nch; off <<= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+                key = o < key ? o : key;
+            }
+            if (n < N && ch == 0) asg[n] = static_cast<int>(key & 0xffffffffu);
+        }
+        for (int i = tid; i < K * DSUB; i += kThreads) isum[i] = 0;
+        for (int i = tid; i < K; i += kThreads) cnt[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < N * DSUB; i += kThreads) {
+            const int n = i / DSUB, j = i % DSUB;
+            const int k = asg[n];
+            // fp16 -> exact int64 multiple of 2^-24
+            const long long v = static_cast<long long>(ldexpf(__half2float(xs[i]), 24));
+            atomicAdd(reinterpret_cast<unsigned long long *>(&isum[k * DSUB + j]),
+                      static_cast<unsigned long long>(v));
+            if (j == 0) atomicAdd(&cnt[k], 1);
+        }
+        __syncthreads();
+        for (int i = tid; i < K * DSUB; i += kThreads) {
+            const int k = i / DSUB, j = i % DSUB;
+            const int c = cnt[k];
+            if (c > 0) {
+                const double mean = __ddiv_rn(ldexp(static_cast<double>(isum[i]), -24), static_cast<double>(c));
+                cent[k * CSTR + j] = __double2float_rn(mean);
+                c16[i] = __double2half(mean);
+            }
+        }
+        __syncthreads();
+    }
+    if (p.assign) {
+        for (int n = tid; n < N; n += kThreads)
+            p.assign[(static_cast<size_t>(u) * N + n) * M + m] = asg[n];
+    }
+    if (p.cent_out) {
+        for (int i = tid; i < K * DSUB; i += kThreads)
+            p.cent_out[cbase + i] = cent[(i / DSUB) * CSTR + (i % DSUB)];
+    }
+    if (p.codebooks) {
+        __half *dst = reinterpret_cast<__half *>(p.codebooks) + cbase;
+        for (int i = tid; i < K * DSUB; i += kThreads) dst[i] = c16[i];
+    }
+}
+
+template <int M>
+cudaError_t launch_m(const FitParams &p, cudaStream_t s) {
+    const size_t smem = FitCfg<M>::smem(p.n_samples);
+    static size_t attr_bytes = 0;
+    if (smem > attr_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(fit_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(FitCfg<M>::smem(kMaxSamples)));
+        if (e != cudaSuccess) return e;
+        attr_bytes = FitCfg<M>::smem(kMaxSamples);
+    }
+    dim3 grid(static_cast<unsigned>(p.num_units), static_cast<unsigned>(M));
+    fit_kernel<M><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fit_smem_bytes(int M, int n_samples) {
+    return M == 4 ? FitCfg<4>::smem(n_samples) : FitCfg<8>::smem(n_samples);
+}
+
+cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s) {
+    if (p.num_units == 0) return cudaSuccess;
+    return M == 4 ? launch_m<4>(p, s) : launch_m<8>(p, s);
+}
+
+}  // namespace aq

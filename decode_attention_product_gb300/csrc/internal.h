@@ -1,0 +1,70 @@
+// internal.h -- launch parameters and launcher entry points shared between the
+// C-ABI layer (api.cu) and the kernel translation units.  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace aq {
+
+struct DecodeParams {
+    const float *q;             // [B][Hq][D]
+    const uint8_t *code_pages;  // [NP][Hkv][P][2][M]
+    const void *codebooks;      // fp16 [S][Hkv][2][M][K][Dsub]
+    const void *kv_pages;       // fp16 [NP][Hkv][2][P][D] (fp16 path)
+    const int32_t *req_set;     // [B]
+    const int32_t *block_table; // [B][max_pages]
+    const int32_t *seq_lens;    // [B]
+    float *out;                 // [B][Hq][D]
+    float *part_o;              // [B][Hq][S][D]   (num_splits > 1)
+    float *part_ml;             // [B][Hq][S][2]   (num_splits > 1)
+    int32_t *status;
+    int32_t batch, num_q_heads, num_kv_heads, max_pages;
+    int64_t num_pages, num_sets;
+    int32_t max_seq_len, num_splits, split_len;  // split_len: tokens, multiple of P
+    float scale_log2;                            // scale * log2(e)
+};
+
+struct EncodeParams {
+    const void *kv;            // fp16 [T][Hkv][2][D]
+    const int32_t *token_set;  // [T]
+    const int64_t *slot_mapping;
+    const void *codebooks;     // fp16 [S][Hkv][2][M][K][Dsub]
+    uint8_t *code_pages;       // [NP][Hkv][P][2][M]
+    int32_t *status;
+    int32_t num_tokens, num_kv_heads;
+    int64_t num_sets, num_pages;
+};
+
+struct FitParams {
+    const void *samples;       // fp16 [U][N][D]
+    const float *cent_in;      // fp32 [U][M][K][Dsub] (step) or nullptr (fit)
+    float *cent_out;           // fp32 [U][M][K][Dsub] (step) or nullptr
+    void *codebooks;           // fp16 [U][M][K][Dsub] (fit) or nullptr
+    int32_t *assign;           // [U][N][M] or nullptr
+    int64_t num_units;
+    int32_t n_samples, iters;
+};
+
+struct Plan {
+    int32_t num_splits;
+    int32_t cluster;      // CTAs per split
+    int32_t split_len;    // tokens per split (multiple of the page size)
+    size_t workspace;     // bytes
+    size_t smem;          // dynamic shared memory per CTA
+};
+
+// Returns cudaSuccess or the launch error.
+cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &plan,
+                             cudaStream_t s);
+cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s);
+cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
+cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
+cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s);
+
+// Shared-memory bytes a PQ decode CTA needs for (M, G, cluster).
+size_t pq_decode_smem_bytes(int M, int G, int cluster);
+size_t fit_smem_bytes(int M, int n_samples);
+
+}  // namespace aq

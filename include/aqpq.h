@@ -1,0 +1,232 @@
+/*
+ * aqpq.h -- C ABI of libaqpq: product-quantised (PQ) KV-cache decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The method (AQPIM blog, devpress.csdn.net, "当大模型推理撞上内存墙"):
+ *   - each head_dim-D key and value vector is split into M contiguous
+ *     sub-vectors of Dsub = D / M dims (§3.1 step 1);
+ *   - each sub-vector is stored as the 8-bit index of its nearest codeword in a
+ *     K = 256-entry codebook kept per request, layer, kv head and K-or-V
+ *     (§3.1 steps 2-3, §3.2 item 1);
+ *   - codebooks are fitted online from the first tokens of the sequence by a
+ *     quick k-means (§3.2 item 2, §5.2 item 1);
+ *   - attention scores are computed by the fused "index -> codebook lookup ->
+ *     sub-vector dot product -> accumulate" flow without writing decoded
+ *     vectors to memory (§4.1, §5.1 item 3);
+ * with the online, split-KV softmax whose per-block (max, sum) statistics are
+ * merged by a reduction (PAM article, maplevalley.com.cn,
+ * "大语言模型KV缓存优化与PAM架构实践", §2.2.3) and a paged cache addressed by a
+ * block table (PAM article §2.2.2; AQPIM blog §5.1 item 4).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; arrays are
+ *     contiguous and row-major with the shapes given below.  libaqpq never
+ *     allocates device memory and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *     legacy default stream).  A status other than AQ_OK from argument checks
+ *     means nothing was launched.
+ *   - Argument checks (host side, before any CUDA call) return
+ *     AQ_ERR_INVALID_ARGUMENT or AQ_ERR_UNSUPPORTED; a launch failure returns
+ *     AQ_ERR_CUDA (aq_last_error_message() names the CUDA error).
+ *   - Data errors that only the device can see (a page id outside the pool, a
+ *     sequence length beyond the block table, a codebook-set index outside the
+ *     codebook array) never fault or trap: the kernels OR AQ_DEV_* bits into
+ *     the caller-zeroed int32 `device_status` word and skip the offending
+ *     element; attention outputs of an affected request are set to NaN.
+ *   - Kernels never wait on another launch.  Their only waits are on their own
+ *     asynchronous copies, bounded in time; a wait that runs out sets
+ *     AQ_DEV_TIMEOUT, and the affected outputs become NaN.
+ *
+ * Layouts (D = head_dim, M = num_subspaces, Dsub = D / M, K = num_codewords,
+ * P = page_size, S = number of codebook sets, NP = number of pages):
+ *   codebooks_f16  fp16 [S][Hkv][2][M][K][Dsub]; [2] is K then V; a "set" is
+ *                  one request (and layer): its codebooks for every kv head.
+ *   code_pages     uint8 [NP][Hkv][P][2][M]; for each token slot the M key
+ *                  codes then the M value codes.
+ *   kv_pages_f16   fp16 [NP][Hkv][2][P][D] (uncompressed comparison cache).
+ *   block_table    int32 [B][max_pages]; token t of request b is in page
+ *                  block_table[b][t / P], slot t % P.
+ *   GQA: query head h reads kv head h / (Hq / Hkv) (Near-memory computing
+ *   ch.1, zsc.github.io, §1.4.3).
+ */
+#ifndef AQPQ_H
+#define AQPQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t aq_status;
+#define AQ_OK                      0
+#define AQ_ERR_INVALID_ARGUMENT    1
+#define AQ_ERR_UNSUPPORTED         2
+#define AQ_ERR_WORKSPACE_TOO_SMALL 3
+#define AQ_ERR_CUDA                4
+
+/* Bits ORed into *device_status by the kernels. */
+#define AQ_DEV_BAD_PAGE    1  /* block-table entry or slot outside [0, num_pages)  */
+#define AQ_DEV_BAD_LENGTH  2  /* seq_len < 0, > max_pages * P or > max_seq_len     */
+#define AQ_DEV_BAD_SET     4  /* req_set / token_set outside [0, num_sets)         */
+#define AQ_DEV_TIMEOUT     8  /* an asynchronous copy did not land in time         */
+
+typedef struct CUstream_st *aq_stream_t;   /* == cudaStream_t */
+
+typedef struct {
+    int32_t head_dim;        /* D: 128                                  */
+    int32_t num_subspaces;   /* M: 4 or 8 (Dsub = 32 or 16)             */
+    int32_t num_codewords;   /* K: 256 (codes are uint8)                */
+    int32_t page_size;       /* P: 16 tokens per page                   */
+} aq_pq_config;
+
+/* Human-readable name of a status code (static string). */
+const char *aq_status_string(aq_status s);
+
+/* Text of the last CUDA error seen by this thread's libaqpq call ("" if none). */
+const char *aq_last_error_message(void);
+
+/* Library version, e.g. "aqpq 0.1 sm_103a". */
+const char *aq_version(void);
+
+/* ---------------------------------------------------------------------------
+ * aq_fit_codebooks -- codebook fit by Lloyd k-means (AQPIM blog §3.2 item 2,
+ * §5.2 item 1: codebooks initialised from the first tokens of each sequence
+ * with a quick k-means on a small sample set).
+ *
+ * For each unit u in [0, num_units) (one set, kv head and K-or-V; the unit
+ * order matches codebooks_f16 with u = (set * Hkv + kvh) * 2 + kv) and each
+ * subspace m: centroid k starts as sample (k mod n_samples); then `iters`
+ * steps of {assign every sample to its nearest centroid (squared Euclidean
+ * distance summed in fp32 over j = 0..Dsub-1 without fused multiply-add, ties
+ * to the lowest index); move every centroid with members to their mean
+ * (exact sum, double-precision division); a centroid without members keeps its
+ * value}.  The codebook is the final centroids rounded to fp16 (nearest even).
+ *
+ *   samples_f16   in   fp16 [U][N][D]
+ *   codebooks_f16 out  fp16 [U][M][K][Dsub]
+ *   assign_out    out  int32 [U][N][M], the assignment of the last step, or NULL
+ * Requires 1 <= n_samples <= 1024, 1 <= iters <= 1000.
+ * ------------------------------------------------------------------------- */
+aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units,
+                           int32_t n_samples, int32_t iters,
+                           const void *samples_f16, void *codebooks_f16,
+                           int32_t *assign_out, aq_stream_t stream);
+
+/* One Lloyd step from given fp32 centroids (the step of aq_fit_codebooks,
+ * exposed for step-by-step checking).
+ *   centroids_in   in  fp32 [U][M][K][Dsub]
+ *   centroids_out  out fp32 [U][M][K][Dsub] (member mean rounded to fp32, or
+ *                      the input value for a centroid without members)
+ *   assign_out     out int32 [U][N][M]                                     */
+aq_status aq_kmeans_step(const aq_pq_config *cfg, int64_t num_units,
+                         int32_t n_samples, const void *samples_f16,
+                         const float *centroids_in, float *centroids_out,
+                         int32_t *assign_out, aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * aq_encode_append -- encode new K/V vectors and write their codes into the
+ * paged code cache (AQPIM blog §3.1 step 3 and §5.2 item 2: the index of the
+ * nearest codeword per subspace; §5.1 item 2: the cache stores indices).
+ *
+ * Token i uses codebook set token_set[i] and is written to page
+ * slot_mapping[i] / P, slot slot_mapping[i] % P, for every kv head.  The
+ * nearest codeword is decided exactly as in aq_fit_codebooks (fp32 squared
+ * distance, plain order, lowest index on ties).  A negative slot_mapping entry
+ * skips the token.  Out-of-range slots or sets set AQ_DEV_BAD_PAGE /
+ * AQ_DEV_BAD_SET and skip the token.
+ *
+ *   kv_f16        in   fp16 [T][Hkv][2][D] (key then value of each token)
+ *   token_set     in   int32 [T]
+ *   slot_mapping  in   int64 [T]
+ *   codebooks_f16 in   fp16 [num_sets][Hkv][2][M][K][Dsub]
+ *   code_pages    out  uint8 [num_pages][Hkv][P][2][M] (only the named slots)
+ *   device_status out  int32, ORed
+ * ------------------------------------------------------------------------- */
+aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens,
+                           int32_t num_kv_heads, const void *kv_f16,
+                           const int32_t *token_set, const int64_t *slot_mapping,
+                           const void *codebooks_f16, int64_t num_sets,
+                           uint8_t *code_pages, int64_t num_pages,
+                           int32_t *device_status, aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * aq_decode_plan -- host-only: the split count and workspace a decode call
+ * with these arguments will use (no CUDA call).
+ *   num_splits_req  0 = choose automatically, else the requested count
+ *   *num_splits     out: splits per (request, kv head)  (may be NULL)
+ *   *cluster_size   out: CTAs cooperating on one split (may be NULL)
+ *   *workspace_bytes out: bytes the call needs in `workspace` (may be NULL)
+ * `fp16` selects the plan of aq_decode_attention_fp16.
+ * ------------------------------------------------------------------------- */
+aq_status aq_decode_plan(const aq_pq_config *cfg, int32_t batch,
+                         int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t max_seq_len, int32_t num_splits_req, int32_t fp16,
+                         int32_t *num_splits, int32_t *cluster_size,
+                         size_t *workspace_bytes);
+
+/* ---------------------------------------------------------------------------
+ * aq_decode_attention -- single-token PQ decode attention over the paged code
+ * cache.
+ *
+ * For request b (codebook set req_set[b], seq_lens[b] cached tokens) and query
+ * head h (kv head h / G, G = Hq / Hkv):
+ *   LUT[m][k] = q[b][h][m*Dsub .. +Dsub) . C^K_m[k]          (per-query table)
+ *   s_t       = scale * sum_m LUT[m][kcode(t, m)]
+ *   p         = softmax(s) over t < seq_lens[b]
+ *   out[b][h][m*Dsub + j] = sum_k ( sum_{t: vcode(t,m) = k} p_t ) * C^V_m[k][j]
+ * i.e. exactly softmax attention over the reconstructed keys and values
+ * (AQPIM blog §4 / §4.1 decomposition; PAM article §2.2.3 for the blockwise
+ * softmax merged over splits).  seq_lens[b] == 0 gives the zero vector.
+ * The current token must already be appended (aq_encode_append).
+ *
+ *   q             in   fp32 [B][Hq][D]
+ *   code_pages    in   uint8 [num_pages][Hkv][P][2][M]
+ *   codebooks_f16 in   fp16 [num_sets][Hkv][2][M][K][Dsub]
+ *   req_set       in   int32 [B]
+ *   block_table   in   int32 [B][max_pages]
+ *   seq_lens      in   int32 [B]   (device)
+ *   max_seq_len   host upper bound of seq_lens, <= max_pages * P; work is
+ *                 planned for it, longer device lengths set AQ_DEV_BAD_LENGTH
+ *   scale         softmax scale (1/sqrt(D) for standard attention)
+ *   num_splits    0 = automatic, else splits per (request, kv head)
+ *   out           out  fp32 [B][Hq][D]
+ *   workspace     device scratch of >= the planned workspace_bytes (may be
+ *                 NULL when that is 0); contents need no initialisation
+ *   device_status out  int32, ORed
+ * ------------------------------------------------------------------------- */
+aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch,
+                              int32_t num_q_heads, int32_t num_kv_heads,
+                              const float *q, const uint8_t *code_pages,
+                              int64_t num_pages, const void *codebooks_f16,
+                              int64_t num_sets, const int32_t *req_set,
+                              const int32_t *block_table, int32_t max_pages,
+                              const int32_t *seq_lens, int32_t max_seq_len,
+                              float scale, int32_t num_splits, float *out,
+                              void *workspace, size_t workspace_bytes,
+                              int32_t *device_status, aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * aq_decode_attention_fp16 -- the uncompressed comparison point: the same
+ * paged decode attention over an fp16 K/V cache (AQPIM blog §2.1 cache).
+ * Only cfg->head_dim and cfg->page_size are used.
+ *
+ *   kv_pages_f16  in   fp16 [num_pages][Hkv][2][P][D]
+ *   other arguments as aq_decode_attention.
+ * ------------------------------------------------------------------------- */
+aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch,
+                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                   const float *q, const void *kv_pages_f16,
+                                   int64_t num_pages, const int32_t *block_table,
+                                   int32_t max_pages, const int32_t *seq_lens,
+                                   int32_t max_seq_len, float scale,
+                                   int32_t num_splits, float *out,
+                                   void *workspace, size_t workspace_bytes,
+                                   int32_t *device_status, aq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AQPQ_H */

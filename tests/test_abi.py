@@ -1,0 +1,129 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/aqpq.h declares, and rejects invalid arguments on the host before any
+CUDA call (so these run on a CPU-only machine)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from decode_attention_product_gb300 import _lib, build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "aqpq.h")
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: checks fail first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(aq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (aq_[a-z0-9_]+)$", out, flags=re.M))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    assert lib.aq_status_string(0) == b"AQ_OK"
+    assert lib.aq_status_string(3) == b"AQ_ERR_WORKSPACE_TOO_SMALL"
+    assert lib.aq_status_string(99) == b"AQ_ERR_UNKNOWN"
+    assert lib.aq_version().startswith(b"aqpq")
+
+
+def _cfg(M=4, D=128, K=256, P=16):
+    return _lib.PQConfig(D, M, K, P)
+
+
+def _decode(lib, cfg, B=2, Hq=4, Hkv=4, max_pages=8, max_seq_len=100, scale=0.1, splits=0,
+            ws=None, wsb=0, q=FAKE):
+    return lib.aq_decode_attention(
+        ctypes.byref(cfg) if cfg is not None else None, B, Hq, Hkv, q, FAKE, 64, FAKE, 4, FAKE,
+        FAKE, max_pages, FAKE, max_seq_len, scale, splits, FAKE, ws, wsb, None, None)
+
+
+def test_decode_argument_checks(lib):
+    INV, UNS, WS = 1, 2, 3
+    assert _decode(lib, None) == INV
+    assert _decode(lib, _cfg(D=64)) == UNS              # head_dim other than 128
+    assert _decode(lib, _cfg(M=3)) == INV               # D % M != 0
+    assert _decode(lib, _cfg(M=16)) == UNS              # Dsub 8 not built
+    assert _decode(lib, _cfg(K=512)) == INV             # codes are 8-bit
+    assert _decode(lib, _cfg(K=128)) == UNS
+    assert _decode(lib, _cfg(P=32)) == UNS
+    assert _decode(lib, _cfg(), Hq=6, Hkv=4) == INV     # Hq % Hkv != 0
+    assert _decode(lib, _cfg(), Hq=48, Hkv=2) == UNS    # group of 24
+    assert _decode(lib, _cfg(), max_pages=4, max_seq_len=65) == INV   # beyond the table
+    assert _decode(lib, _cfg(), scale=float("nan")) == INV
+    assert _decode(lib, _cfg(), B=-1) == INV
+    assert _decode(lib, _cfg(), q=None) == INV
+    assert _decode(lib, _cfg(), B=0) == 0               # empty batch: nothing to do
+    # forced splits need a workspace
+    assert _decode(lib, _cfg(), max_seq_len=100, splits=3) == WS
+
+
+def test_fp16_decode_argument_checks(lib):
+    cfg = _cfg()
+    r = lib.aq_decode_attention_fp16(ctypes.byref(cfg), 2, 4, 4, FAKE, None, 8, FAKE, 8, FAKE, 100,
+                                     0.1, 0, FAKE, None, 0, None, None)
+    assert r == 1                                       # kv_pages NULL
+    r = lib.aq_decode_attention_fp16(ctypes.byref(cfg), 2, 4, 4, FAKE, FAKE, 8, FAKE, 8, FAKE, 100,
+                                     0.1, 4, FAKE, None, 0, None, None)
+    assert r == 3
+
+
+def test_encode_and_fit_argument_checks(lib):
+    cfg = _cfg()
+    assert lib.aq_encode_append(ctypes.byref(cfg), 4, 0, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1, None,
+                                None) == 1          # no kv heads
+    assert lib.aq_encode_append(ctypes.byref(cfg), 4, 2, None, FAKE, FAKE, FAKE, 1, FAKE, 1, None,
+                                None) == 1
+    assert lib.aq_encode_append(ctypes.byref(cfg), 0, 2, None, None, None, None, 1, None, 1, None,
+                                None) == 0          # nothing to encode
+    assert lib.aq_fit_codebooks(ctypes.byref(cfg), 4, 0, 10, FAKE, FAKE, None, None) == 1
+    assert lib.aq_fit_codebooks(ctypes.byref(cfg), 4, 2048, 10, FAKE, FAKE, None, None) == 2
+    assert lib.aq_fit_codebooks(ctypes.byref(cfg), 4, 64, 0, FAKE, FAKE, None, None) == 1
+    assert lib.aq_fit_codebooks(ctypes.byref(cfg), 0, 64, 10, None, None, None, None) == 0
+    assert lib.aq_kmeans_step(ctypes.byref(cfg), 4, 64, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def _plan(lib, B, Hq, Hkv, L, M=4, splits=0, fp16=0):
+    cfg = _cfg(M=M)
+    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    r = lib.aq_decode_plan(ctypes.byref(cfg), B, Hq, Hkv, L, splits, fp16, ctypes.byref(s),
+                           ctypes.byref(c), ctypes.byref(w))
+    assert r == 0
+    return s.value, c.value, w.value
+
+
+def test_plans_for_the_workloads(lib):
+    # B4 H32 L2048 M4: 128 clusters of 4 CTAs fill the GPU, no split, no workspace
+    assert _plan(lib, 4, 32, 32, 2048) == (1, 4, 0)
+    # 80-layer GQA shape (8 kv heads serve 64 query heads)
+    s, c, w = _plan(lib, 8, 64, 8, 1000)
+    assert c == 4 and s == 1 and w == 0
+    # B1 H32 L131072 M8: splits, and a workspace of B*Hq*S*(D+2) floats
+    s, c, w = _plan(lib, 1, 32, 32, 131072, M=8)
+    assert s > 1 and w == 1 * 32 * s * 130 * 4
+    # ragged 256 requests: enough clusters already
+    assert _plan(lib, 256, 32, 32, 4096)[0] == 1
+    # forced split counts are honoured (rounded so no split is empty)
+    assert _plan(lib, 2, 4, 4, 100, splits=3)[0] == 3
+    assert _plan(lib, 2, 4, 4, 100, splits=50)[0] == 7     # 7 pages
+    assert _plan(lib, 2, 4, 4, 0, splits=5)[0] == 1

@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: codes and k-means assignments bit-exact wherever the oracle's relative
+runner-up gap exceeds 1e-4 (and, since both sides decide with the same fp32
+arithmetic, everywhere in practice -- asserted separately); codebooks bit-exact;
+attention outputs within |o - o*| <= 2e-3 + 2e-3 |o*|.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 2e-3
+GAP = 1e-4
+
+
+@pytest.fixture(scope="module")
+def A():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_attention_product_gb300 import build
+    build.build()
+    from decode_attention_product_gb300 import api
+    return api
+
+
+def dev(x, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def close(got, want):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - want)
+    bound = ATOL + RTOL * np.abs(want)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    bad = err > bound
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tol; max err {err.max():.3e}"
+    return float(err.max())
+
+
+def run_pq(A, p, num_splits=0, max_seq_len=None):
+    st = A.new_status()
+    L = int(max(p["seq_lens"].max(), 0)) if max_seq_len is None else max_seq_len
+    out = A.decode_attention(dev(p["q"]), dev(p["code_pages"]), dev(p["codebooks"]),
+                             dev(p["req_set"]), dev(p["block_table"]), dev(p["seq_lens"]),
+                             L, 1.0 / np.sqrt(128), num_splits=num_splits, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(st.item())
+
+
+def oracle_pq(orc, p):
+    return orc.decode_attention(p["q"], p["code_pages"], p["codebooks"], p["req_set"],
+                                p["block_table"], p["seq_lens"], 1.0 / np.sqrt(128), 16)
+
+
+# --------------------------------------------------------------------------
+# decode attention (random codes and codebooks; stage parity)
+# --------------------------------------------------------------------------
+CASES = [
+    # (B, Hq, Hkv, M, lens)
+    (1, 2, 2, 4, [512]),                       # the tiny shape
+    (3, 4, 4, 4, [1, 17, 333]),                # ragged tails, 1-token request
+    (2, 8, 2, 4, [700, 45]),                   # GQA group 4
+    (2, 16, 2, 4, [1000, 257]),                # GQA group 8: several chunks per CTA
+    (2, 4, 2, 4, [64, 31]),                    # group 2
+    (2, 4, 4, 8, [400, 1500]),                 # M = 8 (Dsub 16)
+    (1, 16, 2, 8, [3001]),                     # M = 8 with group 8
+    (1, 2, 2, 4, [9001]),                      # group 1, several chunks per CTA
+    (4, 4, 4, 4, [0, 16, 15, 48]),             # empty request, page-exact lengths
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}M{c[3]}" for c in CASES])
+@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+def test_decode_matches_oracle(A, orc, case, splits):
+    B, Hq, Hkv, M, lens = case
+    p = W.paged_codes_problem(hash((B, Hq, Hkv, M, tuple(lens))) % 10000, B, Hq, Hkv, M, lens,
+                              num_sets=B + 1)
+    got, st = run_pq(A, p, num_splits=splits)
+    assert st == 0
+    close(got, oracle_pq(orc, p))
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[b] == 0.0)
+
+
+def test_decode_plan_variants_agree(A, orc):
+    """Cluster sizes 4 and the split counts the planner picks for the long shape
+    give the same answer as the oracle."""
+    p = W.paged_codes_problem(5, 1, 4, 4, 8, [20000], num_sets=1)
+    want = oracle_pq(orc, p)
+    for s in (0, 3, 16):
+        got, st = run_pq(A, p, num_splits=s)
+        assert st == 0
+        close(got, want)
+
+
+def test_decode_repeated_calls_are_identical(A):
+    p = W.paged_codes_problem(6, 2, 8, 8, 4, [900, 1200])
+    a, _ = run_pq(A, p)
+    b, _ = run_pq(A, p)
+    assert np.array_equal(a, b)
+
+
+def test_decode_data_errors_flag_and_nan(A):
+    p = W.paged_codes_problem(7, 3, 4, 4, 4, [40, 40, 40], num_sets=3)
+    # request 0: block-table entry outside the pool; request 1: set outside the array
+    p["block_table"][0, 1] = p["num_pages"] + 5
+    p["req_set"][1] = 99
+    got, st = run_pq(A, p)
+    assert st & 1 and st & 4
+    assert np.all(np.isnan(got[0])) and np.all(np.isnan(got[1]))
+    assert np.all(np.isfinite(got[2]))
+    # a device length beyond the planned maximum
+    p = W.paged_codes_problem(8, 2, 4, 4, 4, [40, 64], num_sets=2)
+    got, st = run_pq(A, p, max_seq_len=48)
+    assert st & 2
+    assert np.all(np.isnan(got[1])) and np.all(np.isfinite(got[0]))
+
+
+# --------------------------------------------------------------------------
+# fp16 comparison kernel
+# --------------------------------------------------------------------------
+FP16_CASES = [(1, 2, 2, [512]), (3, 4, 4, [1, 17, 333]), (2, 16, 2, [1000, 37]),
+              (2, 8, 2, [64, 0]), (1, 4, 4, [5000])]
+
+
+@pytest.mark.parametrize("case", FP16_CASES)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_fp16_decode_matches_oracle(A, orc, case, splits):
+    B, Hq, Hkv, lens = case
+    p = W.paged_fp16_problem(sum(lens) + B, B, Hq, Hkv, lens)
+    st = A.new_status()
+    out = A.decode_attention_fp16(dev(p["q"]), dev(p["kv_pages"]), dev(p["block_table"]),
+                                  dev(p["seq_lens"]), int(max(lens)), 1.0 / np.sqrt(128),
+                                  num_splits=splits, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = orc.decode_attention_fp16(p["q"], p["kv_pages"], p["block_table"], p["seq_lens"],
+                                     1.0 / np.sqrt(128))
+    close(out.cpu().numpy(), want)
+
+
+# --------------------------------------------------------------------------
+# encode
+# --------------------------------------------------------------------------
+def _encode_case(A, orc, w, t0, t1):
+    """Encode tokens [t0, t1) of every request of workload w on both sides, with
+    codebooks fitted (by the oracle) on each request's first 64 tokens."""
+    B, Hkv, M = w.batch, w.num_kv_heads, w.num_subspaces
+    if w.mixture:
+        samples = np.stack([w.fit_samples(w.kv(b, t1=w.n_fit)) for b in range(B)])
+        cb16, _, _, _ = orc.kmeans_fit(samples.reshape(-1, *samples.shape[3:]), M, 256, 3)
+        cbs = cb16.reshape(B, Hkv, 2, M, 256, w.dsub)
+    else:
+        cbs = np.stack([w.given_codebooks()] * B)
+    kvs = [w.kv(b, t0, t1) for b in range(B)]
+    bt, npages = w.block_table()
+    kv = np.concatenate(kvs)
+    tset = np.concatenate([np.full(len(k), b, np.int32) for b, k in enumerate(kvs)])
+    slots = np.concatenate([w.slot_mapping(bt, b, t0, t0 + len(k)) for b, k in enumerate(kvs)])
+    want = np.zeros((npages, Hkv, 16, 2, M), np.uint8)
+    gap = orc.encode_append(kv, tset, slots, cbs, want, 16)
+    pages = torch.zeros((npages, Hkv, 16, 2, M), dtype=torch.uint8, device="cuda")
+    st = A.new_status()
+    A.encode_append(dev(kv), dev(tset), dev(slots), dev(cbs), pages, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = pages.cpu().numpy()
+    # compare every written slot: bit-exact where the gap clears the band ...
+    pg, sl = slots // 16, slots % 16
+    g_codes = got[pg, :, sl]                     # [T][Hkv][2][M]
+    w_codes = want[pg, :, sl]
+    clear = gap > GAP
+    assert np.array_equal(g_codes[clear], w_codes[clear])
+    # ... and, the decision arithmetic being the same, everywhere
+    assert np.array_equal(g_codes, w_codes)
+    return clear.mean()
+
+
+def test_encode_tiny_workload(A, orc):
+    assert _encode_case(A, orc, W.make("tiny"), 0, 512) > 0.99
+
+
+def test_encode_small_batch_append(A, orc):
+    # a decode step: one token per request (codeword-parallel kernel)
+    _encode_case(A, orc, W.make("page1"), 2047, 2048)
+    _encode_case(A, orc, W.make("long", seq_lens=[200]), 100, 101)
+
+
+def test_encode_prefill_tiles(A, orc):
+    # many tokens (token-parallel kernel), ragged requests sharing tiles
+    w = W.make("ragged", seq_lens=[300, 70, 333, 64], num_q_heads=8, num_kv_heads=8)
+    _encode_case(A, orc, w, 0, 10**9)
+    w = W.make("long", seq_lens=[700, 129], num_q_heads=4, num_kv_heads=4)
+    _encode_case(A, orc, w, 0, 10**9)
+
+
+def test_encode_bad_slots_flagged(A):
+    kv = torch.zeros((2, 1, 2, 128), dtype=torch.float16, device="cuda")
+    cbs = torch.zeros((1, 1, 2, 4, 256, 32), dtype=torch.float16, device="cuda")
+    pages = torch.full((2, 1, 16, 2, 4), 7, dtype=torch.uint8, device="cuda")
+    st = A.new_status()
+    A.encode_append(kv, dev(np.array([0, 5], np.int32)), dev(np.array([40, -1], np.int64)), cbs,
+                    pages, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 1                   # page 2 outside a 2-page pool; -1 skipped
+    assert torch.all(pages == 7)
+
+
+# --------------------------------------------------------------------------
+# codebook fit
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name,N", [("page1", 64), ("long", 64), ("page1", 1024), ("tiny", 300)])
+def test_fit_matches_oracle(A, orc, name, N):
+    w = W.make(name)
+    units = []
+    for b in range(min(w.batch, 2)):
+        kv = w.kv(b, t1=N)
+        units.append(np.ascontiguousarray(kv[:N].transpose(1, 2, 0, 3)).reshape(-1, N, 128))
+    samples = np.concatenate(units)[:24]                            # [U][N][D]
+    M = w.num_subspaces
+    cb16, _, assign, mg = orc.kmeans_fit(samples, M, 256, 10)
+    cb_gpu, asg_gpu = A.fit_codebooks(dev(samples), M, 10, with_assign=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(asg_gpu.cpu().numpy(), assign)
+    assert np.array_equal(cb_gpu.cpu().numpy().view(np.uint16), cb16.view(np.uint16))
+
+
+def test_kmeans_step_matches_oracle(A, orc):
+    w = W.make("page1")
+    kv = w.kv(0, t1=1024)
+    samples = np.ascontiguousarray(kv.transpose(1, 2, 0, 3)).reshape(-1, 1024, 128)[:8]
+    _, cent, _, _ = orc.kmeans_fit(samples, 4, 256, 2)
+    c32 = cent.astype(np.float32)
+    a_o, c_o, gap = orc.kmeans_step(samples, c32)
+    c_g, a_g = A.kmeans_step(dev(samples), dev(c32))
+    torch.cuda.synchronize()
+    assert np.array_equal(a_g.cpu().numpy(), a_o)
+    assert np.array_equal(c_g.cpu().numpy(), c_o.astype(np.float32))

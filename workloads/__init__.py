@@ -243,3 +243,57 @@ def make(name: str, seed: int | None = None, **overrides) -> Workload:
 
 
 NAMES = ("tiny", "page1", "qwen_gqa", "long", "ragged")
+
+
+def paged_codes_problem(seed: int, batch: int, num_q_heads: int, num_kv_heads: int,
+                        num_subspaces: int, seq_lens, num_sets: int | None = None,
+                        shuffle: bool = True, extra_pages: int = 3, page_size: int = PAGE,
+                        head_dim: int = HEAD_DIM, num_codewords: int = CODEWORDS) -> dict:
+    """Random inputs for the decode step alone: fp16 N(0,1) codebooks, uniform
+    uint8 codes in every page slot, fp32 N(0,1) queries, a (shuffled) block
+    table with `extra_pages` unused pages in the pool, and a random request ->
+    codebook-set map.  Returns numpy arrays keyed by argument name."""
+    g = _rng(seed, 0x9a9ed)
+    lens = np.asarray(seq_lens, np.int32)
+    assert len(lens) == batch
+    S = num_sets or batch
+    M, Dsub = num_subspaces, head_dim // num_subspaces
+    codebooks = g.standard_normal((S, num_kv_heads, 2, M, num_codewords, Dsub),
+                                  dtype=np.float32).astype(np.float16)
+    pages_per = [-(-int(L) // page_size) for L in lens]
+    num_pages = int(sum(pages_per)) + extra_pages
+    perm = g.permutation(num_pages) if shuffle else np.arange(num_pages)
+    max_pages = max(1, max(pages_per) if pages_per else 1)
+    bt = np.zeros((batch, max_pages), np.int32)
+    nxt = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[nxt:nxt + n]
+        nxt += n
+    code_pages = g.integers(0, num_codewords, size=(num_pages, num_kv_heads, page_size, 2, M),
+                            dtype=np.uint8)
+    req_set = g.integers(0, S, size=batch).astype(np.int32)
+    q = g.standard_normal((batch, num_q_heads, head_dim), dtype=np.float32)
+    return {"q": q, "code_pages": code_pages, "codebooks": codebooks, "req_set": req_set,
+            "block_table": bt, "seq_lens": lens, "num_pages": num_pages}
+
+
+def paged_fp16_problem(seed: int, batch: int, num_q_heads: int, num_kv_heads: int, seq_lens,
+                       shuffle: bool = True, extra_pages: int = 3, page_size: int = PAGE,
+                       head_dim: int = HEAD_DIM) -> dict:
+    """Random fp16 K/V pages [NP][Hkv][2][P][D] (N(0,1)), queries and a block table."""
+    g = _rng(seed, 0xf16)
+    lens = np.asarray(seq_lens, np.int32)
+    pages_per = [-(-int(L) // page_size) for L in lens]
+    num_pages = int(sum(pages_per)) + extra_pages
+    perm = g.permutation(num_pages) if shuffle else np.arange(num_pages)
+    max_pages = max(1, max(pages_per) if pages_per else 1)
+    bt = np.zeros((batch, max_pages), np.int32)
+    nxt = 0
+    for b, n in enumerate(pages_per):
+        bt[b, :n] = perm[nxt:nxt + n]
+        nxt += n
+    kv_pages = g.standard_normal((num_pages, num_kv_heads, 2, page_size, head_dim),
+                                 dtype=np.float32).astype(np.float16)
+    q = g.standard_normal((batch, num_q_heads, head_dim), dtype=np.float32)
+    return {"q": q, "kv_pages": kv_pages, "block_table": bt, "seq_lens": lens,
+            "num_pages": num_pages}
