@@ -251,42 +251,93 @@ def run_ours(args, w, rank, world, local_rank):
     outs = [torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda") for _ in range(R)]
     status = api.new_status()
 
-    def step(i, ev=None):
+    def step(i, ev0=None, ev1=None):
         c = copies[i % R]
         api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)
-        if ev is not None:
-            ev.record()
+        if ev0 is not None:
+            ev0.record()
         api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
                              c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws,
                              status=status)
+        if ev1 is not None:
+            ev1.record()
 
     for i in range(args.warmup):
         step(i)
+    torch.cuda.synchronize()
+    # The timed steps are replayed from CUDA graphs (launch overhead of the
+    # Python binding off the critical path): one graph of R steps (one per input
+    # copy) and one of the K mod R remaining steps, so exactly K steps run.
+    evpairs = []
+
+    def capture(n, with_events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                e0 = e1 = None
+                if with_events:
+                    e0 = torch.cuda.Event(enable_timing=True, external=True)
+                    e1 = torch.cuda.Event(enable_timing=True, external=True)
+                    evpairs.append((e0, e1))
+                step(i, e0, e1)
+        return g
+
+    try:
+        g_full = capture(R, True)
+        events_in_graph = True
+    except Exception:                                   # torch without external events
+        torch.cuda.synchronize()
+        evpairs.clear()
+        g_full = capture(R, False)
+        events_in_graph = False
+    n_full, n_tail = divmod(args.steps, R)
+    g_tail = capture(n_tail, False) if n_tail else None
+    for _ in range(2):
+        g_full.replay()
     torch.cuda.synchronize()
     if dist:
         torch.distributed.barrier()
     clocks = ClockSampler(local_rank)
     clocks.start()
-    # timed region: K steps; decode-kernel events inside each step
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()
     if dist:
         torch.distributed.barrier()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_begin.record()
-    for i in range(args.steps):
-        starts[i].record()
-        step(args.warmup + i, mids[i])
-    starts[args.steps].record()
+    for _ in range(n_full):
+        g_full.replay()
+    if g_tail is not None:
+        g_tail.replay()
     t_end.record()
     torch.cuda.synchronize()
     if dist:
         torch.distributed.barrier()
     clk = clocks.stop()
     total_ms = t_begin.elapsed_time(t_end)
-    dec_ms = [mids[i].elapsed_time(starts[i + 1]) for i in range(args.steps)]
+    if events_in_graph and n_full > 0:
+        dec_ms = [e0.elapsed_time(e1) for e0, e1 in evpairs]
+        dec_how = "events around each decode launch inside the replayed step graph (last replay)"
+    else:
+        # decode-only graph of R back-to-back launches, timed with events
+        g_dec = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_dec):
+            for i in range(R):
+                c = copies[i % R]
+                api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                                     c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws,
+                                     status=status)
+        g_dec.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = max(1, args.steps // R)
+        e0.record()
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        dec_ms = [e0.elapsed_time(e1) / (reps * R)]
+        dec_how = "decode-only graph of back-to-back launches (events around the replays)"
     if dist:
         t = torch.tensor([total_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -323,7 +374,7 @@ def run_ours(args, w, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "kernel": "pq_decode_kernel",
                      "bytes_per_launch": byt["total"], "launch_ms": dec_avg_ms,
-                     "peak_kind": peak_kind},
+                     "peak_kind": peak_kind, "timing": dec_how},
         "code_stream": {"gbs": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9,
                         "codes_only_gbs": byt["codes"] / (dec_avg_ms / 1e3) / 1e9,
                         "frac_of_peak": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9 / peak},
@@ -346,41 +397,33 @@ def run_ours(args, w, rank, world, local_rank):
 
 
 def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
-    """Per step: pinned q and new K/V copied in, append + decode through the API,
-    output copied out, host waits for it."""
+    """Through the public API (api.DecodeStep) with pinned host buffers: per
+    step the q and new-K/V copies in, the append and decode calls and the output
+    copy out run as one captured graph, and the host waits for the output."""
     Hq = w.num_q_heads
     q_h = torch.from_numpy(w.queries()).pin_memory()
     kv_h = base["new_kv"].cpu().pin_memory()
     out_h = torch.empty((w.batch, Hq, 128), dtype=torch.float32).pin_memory()
-    q_d = torch.empty_like(base["q"])
-    kv_d = torch.empty_like(base["new_kv"])
-    out_d = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
-    st = api.new_status()
-
-    def one():
-        q_d.copy_(q_h, non_blocking=True)
-        kv_d.copy_(kv_h, non_blocking=True)
-        api.encode_append(kv_d, base["new_set"], base["new_slot"], base["codebooks"], base["pages"], st)
-        api.decode_attention(q_d, base["pages"], base["codebooks"], base["req_set"], base["bt"],
-                             base["seq_lens"], Lmax, w.scale, out=out_d, workspace=ws, status=st)
-        out_h.copy_(out_d, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-
+    ds = api.DecodeStep(base["pages"], base["codebooks"], base["req_set"], base["bt"],
+                        base["seq_lens"], Lmax, base["new_slot"], base["new_set"], Hq, w.scale)
+    ds.capture_host(q_h, kv_h, out_h)
     for _ in range(max(3, args.warmup)):
-        one()
+        ds.replay()
     if dist:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one()
+        ds.replay(wait=True)
     secs = time.perf_counter() - t0
+    ds.check_status()
     if dist:
         t = torch.tensor([secs], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         secs = float(t.item())
     return {"value": world * units * args.steps / secs, "unit": UNIT,
             "h2d_bytes_per_step": q_h.numel() * 4 + kv_h.numel() * 2,
-            "d2h_bytes_per_step": out_h.numel() * 4, "ms_per_step": 1e3 * secs / args.steps}
+            "d2h_bytes_per_step": out_h.numel() * 4, "ms_per_step": 1e3 * secs / args.steps,
+            "how": "api.DecodeStep graph replay per step, host waits for the output"}
 
 
 def measure_fp16(args, w, api, torch, base, Lmax, units, T):
@@ -408,16 +451,22 @@ def measure_fp16(args, w, api, torch, base, Lmax, units, T):
         api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax, w.scale,
                                   out=out, workspace=ws)
     torch.cuda.synchronize()
-    n = max(10, args.steps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(R):
+            api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax,
+                                      w.scale, out=out, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(2, -(-max(10, args.steps) // R))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(n):
-        api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax, w.scale,
-                                  out=out, workspace=ws)
+    for _ in range(reps):
+        g.replay()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
+    ms = e0.elapsed_time(e1) / (reps * R)
     byt = T.fp16_decode_bytes(w.seq_lens, Hq, Hkv)
     peak, _ = measured_peaks()
     del pcs, pages

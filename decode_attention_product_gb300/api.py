@@ -168,3 +168,75 @@ def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: 
         _ptr(status), _stream())
     _lib.check(st, "aq_decode_attention_fp16")
     return out
+
+
+class DecodeStep:
+    """One decode step of a fixed batch: append each request's current K/V
+    token into the PQ code cache, then PQ decode attention over the cache.
+
+    Holds the cache tensors, the workspace, the output and a device status
+    word.  `run(q, new_kv)` launches the two C-ABI calls on the current stream.
+    `capture_host(q_host, kv_host, out_host)` records the whole step -- copies
+    of the pinned host inputs to the device, the two calls, the copy of the
+    output back to pinned host memory -- into a CUDA graph; `replay()` launches
+    it and, with wait=True, blocks until the output is on the host.
+    """
+
+    def __init__(self, code_pages, codebooks, req_set, block_table, seq_lens, max_seq_len,
+                 new_slot, new_set, num_q_heads, scale=None, num_splits=0):
+        self.code_pages, self.codebooks = code_pages, codebooks
+        self.req_set, self.block_table, self.seq_lens = req_set, block_table, seq_lens
+        self.max_seq_len = int(max_seq_len)
+        self.new_slot, self.new_set = new_slot, new_set
+        self.B, self.Hq = int(seq_lens.shape[0]), int(num_q_heads)
+        self.Hkv, self.M = int(codebooks.shape[1]), int(codebooks.shape[3])
+        self.scale = scale
+        self.num_splits = num_splits
+        dev = code_pages.device
+        self.workspace = workspace_for(self.B, self.Hq, self.Hkv, self.max_seq_len, self.M,
+                                       num_splits, device=dev)
+        self.status = new_status(dev)
+        self.out = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32, device=dev)
+        self.graph = None
+        self._host = None
+
+    def run(self, q, new_kv, out=None):
+        encode_append(new_kv, self.new_set, self.new_slot, self.codebooks, self.code_pages,
+                      self.status)
+        return decode_attention(q, self.code_pages, self.codebooks, self.req_set, self.block_table,
+                                self.seq_lens, self.max_seq_len, self.scale, self.num_splits,
+                                out=self.out if out is None else out, workspace=self.workspace,
+                                status=self.status)
+
+    def capture_host(self, q_host, kv_host, out_host):
+        """Capture copy-in, step, copy-out into a CUDA graph (pinned host tensors)."""
+        for t, n in ((q_host, "q_host"), (kv_host, "kv_host"), (out_host, "out_host")):
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError(f"{n} must be a pinned host tensor")
+        q_d = torch.empty(q_host.shape, dtype=q_host.dtype, device=self.out.device)
+        kv_d = torch.empty(kv_host.shape, dtype=kv_host.dtype, device=self.out.device)
+        self._host = (q_host, kv_host, out_host, q_d, kv_d)
+        # one eager run sets kernel attributes outside the capture
+        q_d.copy_(q_host)
+        kv_d.copy_(kv_host)
+        self.run(q_d, kv_d)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            q_d.copy_(q_host, non_blocking=True)
+            kv_d.copy_(kv_host, non_blocking=True)
+            self.run(q_d, kv_d)
+            out_host.copy_(self.out, non_blocking=True)
+        self.graph = g
+        return g
+
+    def replay(self, wait=True):
+        self.graph.replay()
+        if wait:
+            torch.cuda.current_stream().synchronize()
+
+    def check_status(self):
+        """Raise if a kernel flagged a data error (reads the status word)."""
+        st = int(self.status.item())
+        if st:
+            raise RuntimeError(f"device status {st:#x}")

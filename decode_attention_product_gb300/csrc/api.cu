@@ -16,6 +16,7 @@ namespace {
 thread_local char g_last_error[256] = "";
 
 aq_status cuda_fail(cudaError_t e) {
+    cudaGetLastError();            // reported here: do not leave it for the next caller
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
                   cudaGetErrorString(e));
     return AQ_ERR_CUDA;
@@ -60,12 +61,17 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
     const int max_pages_needed = (max_seq_len + P - 1) / P;
     int C = 1;
+    int share_max = kMaxShare;
     if (!fp16) {
         const int M = cfg->num_subspaces;
         C = 0;
         for (int c = 4; c >= 1; c /= 2)
-            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
+            if (c <= M && pq_decode_smem_bytes(M, G, c, P) <= smem_cap) { C = c; break; }
         if (C == 0) return AQ_ERR_UNSUPPORTED;
+        // the largest token share whose codes still fit next to the rest
+        const size_t room = smem_cap - pq_decode_smem_bytes(M, G, C, 0);
+        const int fit = static_cast<int>(room / (2 * M)) / P * P;
+        share_max = fit < kMaxShare ? fit : kMaxShare;
     }
     int S = req;
     if (S <= 0) {
@@ -80,18 +86,27 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
             if (S < 1) S = 1;
         }
     }
-    if (S > 1024) S = 1024;
+    if (!fp16) {
+        // each CTA of a cluster stages at most kMaxShare tokens of codes
+        const int64_t need = (static_cast<int64_t>(max_seq_len) + static_cast<int64_t>(C) * share_max - 1) /
+                             (static_cast<int64_t>(C) * share_max);
+        if (S < need) S = static_cast<int>(need);
+    }
+    if (S > 4096) S = 4096;
     if (max_pages_needed == 0) S = 1;
     // split length: page multiple; recompute S so no trailing split is empty
     int split_pages = (max_pages_needed + S - 1) / S;
     if (split_pages < 1) split_pages = 1;
     S = (max_pages_needed + split_pages - 1) / split_pages;
     if (S < 1) S = 1;
+    const int split_len = split_pages * P;
+    const int share = ((split_len + C - 1) / C + P - 1) / P * P;
     pl->num_splits = S;
     pl->cluster = C;
-    pl->split_len = split_pages * P;
+    pl->split_len = split_len;
+    pl->share = share;
     pl->workspace = S > 1 ? static_cast<size_t>(batch) * Hq * S * (kHeadDim + 2) * sizeof(float) : 0;
-    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C);
+    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C, share);
     return AQ_OK;
 }
 
@@ -262,6 +277,7 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.max_seq_len = max_seq_len;
     p.num_splits = pl.num_splits;
     p.split_len = pl.split_len;
+    p.share = pl.share;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = fp16 ? launch_fp16_decode(p, Hq / Hkv, pl, s)

@@ -44,29 +44,39 @@ struct PqCfg {
     static constexpr int CB_HALVES = MC * K * DSUB;         // owned part of one codebook
     static constexpr int CB_BYTES = CB_HALVES * 2;
     static constexpr int LUT_FLOATS = M * K * G;
+    static constexpr int ROW_FLOATS = MC * K * G;           // one rank's rows of LUT / bins
     static constexpr int TPT = 8;                           // tokens per thread per chunk
     static constexpr int TOK_PER_PASS = kThreads / G;
     static constexpr int CHUNK = TOK_PER_PASS * TPT;
+    // statistics pushed with the bins: m[G], l[G], bad flag
+    static constexpr int STAT_FLOATS = 2 * G + 1;
+    static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
     // V-product thread mapping
     static constexpr int NJP = MC * DSUB / 2;               // owned j-pairs
     static constexpr int KS = kThreads / NJP;               // k slices
     static constexpr int KSL = K / KS;                      // k per slice
     // shared-memory layout (bytes)
-    static constexpr int OFF_BAR = 0;                       // 2 mbarriers
-    static constexpr int OFF_MISC = 16;                     // int flags
+    static constexpr int OFF_BAR = 0;                       // 5 mbarriers
+    static constexpr int OFF_MISC = 64;                     // int flags
     static constexpr int OFF_CBK = 128;
     static constexpr int OFF_CBV = OFF_CBK + CB_BYTES;
     static constexpr int OFF_LUT = OFF_CBV + CB_BYTES;
     static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
-    static constexpr int OFF_Q = OFF_BINS + LUT_FLOATS * 4;
+    // [C-1][INC_STRIDE] from the peers; sender src lands in slot (src - dst - 1) mod C
+    static constexpr int OFF_INC = OFF_BINS + LUT_FLOATS * 4;
+    static constexpr int OFF_Q = OFF_INC + (C > 1 ? (C - 1) * INC_STRIDE * 4 : 0);
     static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_max, red_sum [kWarps][G]
-    static constexpr int OFF_XCH = OFF_RED + 2 * kWarps * G * 4;  // m, l [G] (read by peers)
-    static constexpr int OFF_FAC = OFF_XCH + 2 * G * 4;     // fac[C][G], mst[G], lst[G], cfac[G]
-    static constexpr int SMEM = OFF_FAC + (C + 3) * G * 4 + 16;
+    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mst, lst, cfac [G], fac [C][G]
+    static constexpr int OFF_CODES = (OFF_STAT + (3 + C) * G * 4 + 15) / 16 * 16;  // [share][2M] uint8
+    static constexpr int PAGE_BYTES = P * 2 * M;            // one page's codes for one kv head
+    static constexpr int PPL = kMaxShare / P / 32;          // page ids per lane of warp 0
+    static size_t smem(int share) { return OFF_CODES + static_cast<size_t>(share) * 2 * M; }
     static_assert(K == kThreads, "one thread per codeword in the table build");
     static_assert(KS * NJP == kThreads && KS * KSL == K, "V-product mapping");
     static_assert(KS * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
-    static_assert(CB_BYTES % 16 == 0 && OFF_CBV % 16 == 0 && OFF_LUT % 16 == 0, "alignment");
+    static_assert(CB_BYTES % 16 == 0 && OFF_LUT % 16 == 0 && OFF_INC % 16 == 0 && OFF_Q % 16 == 0,
+                  "alignment");
+    static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "vector pushes");
 };
 
 template <int N>
@@ -100,22 +110,35 @@ __device__ __forceinline__ void load_vec(float (&v)[N], const float *src) {
     }
 }
 
+// Push N floats from registers to the same offset in a peer's shared memory.
+template <int N>
+__device__ __forceinline__ void push_vec(uint32_t raddr, const float (&v)[N], uint32_t rbar) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4)
+            st_async_v4(raddr + 4 * i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]), rbar);
+    } else if constexpr (N == 2) {
+        st_async_v2(raddr, v[0], v[1], rbar);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) st_async_f32(raddr + 4 * i, v[i], rbar);
+    }
+}
+
 // Code bytes of one token: M key codes then M value codes.
 template <int M>
 struct Codes;
 template <>
 struct Codes<4> {
     uint2 v;
-    __device__ __forceinline__ void load(const uint8_t *p) { v = ldg_stream_v2(p); }
-    __device__ __forceinline__ void zero() { v = make_uint2(0, 0); }
+    __device__ __forceinline__ void load(const uint8_t *p) { v = *reinterpret_cast<const uint2 *>(p); }
     __device__ __forceinline__ int k(int m) const { return (v.x >> (8 * m)) & 0xff; }
     __device__ __forceinline__ int vv(int m) const { return (v.y >> (8 * m)) & 0xff; }
 };
 template <>
 struct Codes<8> {
     uint4 v;
-    __device__ __forceinline__ void load(const uint8_t *p) { v = ldg_stream_v4(p); }
-    __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void load(const uint8_t *p) { v = *reinterpret_cast<const uint4 *>(p); }
     __device__ __forceinline__ int k(int m) const {
         return ((m < 4 ? v.x : v.y) >> (8 * (m & 3))) & 0xff;
     }
@@ -124,46 +147,65 @@ struct Codes<8> {
     }
 };
 
-template <int C>
-__device__ __forceinline__ void cluster_sync_if() {
-    if constexpr (C > 1) cg::this_cluster().sync();
-}
-
 template <int M, int G, int C>
 __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
-    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC;
+    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
-    int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);   // [0] bad bits of this CTA
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in
+    int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);           // [0] local bad, [1] all
     __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
     __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
     float *lut = reinterpret_cast<float *>(smem + S::OFF_LUT);
     float *bins = reinterpret_cast<float *>(smem + S::OFF_BINS);
+    float *inc = reinterpret_cast<float *>(smem + S::OFF_INC);
     float *qs = reinterpret_cast<float *>(smem + S::OFF_Q);
     float *red_max = reinterpret_cast<float *>(smem + S::OFF_RED);
     float *red_sum = red_max + kWarps * G;
-    float *xch = reinterpret_cast<float *>(smem + S::OFF_XCH);  // [0,G): m  [G,2G): l
-    float *fac = reinterpret_cast<float *>(smem + S::OFF_FAC);  // [C][G]
-    float *mst = fac + C * G;
+    float *mst = reinterpret_cast<float *>(smem + S::OFF_STAT);
     float *lst = mst + G;
     float *cfac = lst + G;
+    float *fac = cfac + G;                                              // [C][G]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int rank = 0;
-    if constexpr (C > 1) rank = static_cast<int>(cg::this_cluster().block_rank());
+    if constexpr (C > 1) rank = static_cast<int>(cluster_ctarank());
     const int split = blockIdx.x / C;
     const int kvh = blockIdx.y, b = blockIdx.z;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
+    uint8_t *codes_s = smem + S::OFF_CODES;
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+        sflag[0] = 0;
+    }
+    // ---- independent loads first: length, codebook set, page ids ------------
+    // A CTA's token share does not depend on the request length, so warp 0
+    // fetches its page ids in parallel with the length.
+    const int share = p.share;
+    const int ts = split * p.split_len;
+    const int a0 = ts + rank * share;
+    const int g = tid % G, jslot = tid / G;
+    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    const int L_raw = __ldg(p.seq_lens + b);
+    const int set = __ldg(p.req_set + b);
+    int pgw[S::PPL];
+    if (warp == 0) {
+        const int np_lim = min(share / P, p.max_pages - a0 / P);
+#pragma unroll
+        for (int j = 0; j < S::PPL; ++j) {
+            const int idx = lane + 32 * j;
+            pgw[j] = idx < np_lim ? __ldg(bt + a0 / P + idx) : -1;
+        }
+    }
+
     // ---- request-level checks: uniform over the cluster ------------------
-    const int L_raw = p.seq_lens[b];
-    const int set = p.req_set[b];
     int bad0 = 0;
     if (L_raw < 0 || L_raw > p.max_pages * P || L_raw > p.max_seq_len) bad0 |= AQ_DEV_BAD_LENGTH;
     if (set < 0 || static_cast<int64_t>(set) >= p.num_sets) bad0 |= AQ_DEV_BAD_SET;
-    const int ts = split * p.split_len;
     const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
     if (bad0 || ts >= te) {
         // nothing to stream: NaN for a bad request, zeros / empty partials otherwise
@@ -171,8 +213,8 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             if (bad0 && tid == 0) flag_status(p.status, bad0);
             const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
             for (int i = tid; i < G * D; i += kThreads) {
-                const int g = i / D, d = i % D;
-                const size_t bh = static_cast<size_t>(b) * Hq + kvh * G + g;
+                const int gg = i / D, d = i % D;
+                const size_t bh = static_cast<size_t>(b) * Hq + kvh * G + gg;
                 if (S_ == 1) p.out[bh * D + d] = v;
                 else if (d == 0) {
                     p.part_ml[(bh * S_ + split) * 2 + 0] = bad0 ? v : -INFINITY;
@@ -182,38 +224,67 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         }
         return;
     }
+    const int e0 = min(te, a0 + share);
+    const int npg = e0 > a0 ? (e0 - a0 + P - 1) / P : 0;
 
-    // ---- 1. async codebook copies, queries, zeroed bins -------------------
-    if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        sflag[0] = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
+    // ---- warp 0 issues every copy: K slice, code pages + query, V slice ----
     const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
     const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
                        ((static_cast<size_t>(set) * Hkv + kvh) * 2) * cb_unit +
                        static_cast<size_t>(rank) * S::CB_HALVES;
     const __half *gV = gK + cb_unit;
-    if (tid == 0) {
-        const uint64_t pol = policy_evict_first();
-        mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
-        bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
-        mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
-        bulk_g2s_hint(cbv, gV, S::CB_BYTES, &bar[1], pol);
+    if (warp == 0) {
+        __syncwarp();
+        uint64_t pol = 0;
+        if (lane == 0) {
+            pol = policy_evict_first();
+            mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
+            bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
+        }
+        bool ok[S::PPL];
+        int nvalid = 0, bad = 0;
+#pragma unroll
+        for (int j = 0; j < S::PPL; ++j) {
+            const int idx = lane + 32 * j;
+            ok[j] = idx < npg && pgw[j] >= 0 && static_cast<int64_t>(pgw[j]) < p.num_pages;
+            bad |= (idx < npg && !ok[j]);
+            nvalid += __popc(__ballot_sync(0xffffffffu, ok[j]));
+        }
+        if (bad) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+        if (lane == 0) mbar_arrive_expect_tx(&bar[4], nvalid * S::PAGE_BYTES + G * D * 4);
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < S::PPL; ++j) {
+            if (ok[j]) {
+                const int idx = lane + 32 * j;
+                bulk_g2s(codes_s + idx * S::PAGE_BYTES,
+                         p.code_pages + (static_cast<size_t>(pgw[j]) * Hkv + kvh) * S::PAGE_BYTES,
+                         S::PAGE_BYTES, &bar[4]);
+            }
+        }
+        if (lane == 0) {
+            bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
+                     &bar[4]);
+            mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
+            bulk_g2s_hint(cbv, gV, S::CB_BYTES, &bar[1], pol);
+            if constexpr (C > 1) {
+                mbar_arrive_expect_tx(&bar[2], (C - 1) * S::ROW_FLOATS * 4);
+                mbar_arrive_expect_tx(&bar[3], (C - 1) * (S::ROW_FLOATS + S::STAT_FLOATS) * 4);
+            }
+        }
     }
-    {
-        const float4 *qg = reinterpret_cast<const float4 *>(
-            p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D);
-        for (int i = tid; i < G * D / 4; i += kThreads) reinterpret_cast<float4 *>(qs)[i] = qg[i];
-        for (int i = tid; i < S::LUT_FLOATS / 4; i += kThreads)
-            reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = tid; i < S::LUT_FLOATS / 4; i += kThreads)
+        reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (C > 1) {
+        cluster_arrive_relaxed();          // peers' mbarriers exist before anyone pushes
+        cluster_wait_acquire();
+    } else {
+        __syncthreads();
     }
-    __syncthreads();
 
-    // ---- 2. lookup table for the owned subspaces --------------------------
+    // ---- lookup-table rows of the owned subspaces, pushed to the peers ------
     if (!mbar_wait_bounded(&bar[0], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    if (!mbar_wait_bounded(&bar[4], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     {
         constexpr int NCH = DSUB / 8;                   // 16-byte chunks per codeword row
         constexpr int ROWS128 = 128 / (DSUB * 2);       // rows per 128 bytes
@@ -224,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             const __half *row = cbk + (static_cast<size_t>(mi) * K + tid) * DSUB;
             float acc[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] = 0.f;
+            for (int gg = 0; gg < G; ++gg) acc[gg] = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < NCH; ++c0) {
                 const int c = (c0 + rot) % NCH;
@@ -232,134 +303,151 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                 const float2 f0 = h2_to_f2(u.x), f1 = h2_to_f2(u.y), f2 = h2_to_f2(u.z),
                              f3 = h2_to_f2(u.w);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float4 *qv = reinterpret_cast<const float4 *>(qs + g * D + m * DSUB + c * 8);
+                for (int gg = 0; gg < G; ++gg) {
+                    const float4 *qv = reinterpret_cast<const float4 *>(qs + gg * D + m * DSUB + c * 8);
                     const float4 qa = qv[0], qb = qv[1];
-                    float a = acc[g];
+                    float a = acc[gg];
                     a = fmaf(qa.x, f0.x, a); a = fmaf(qa.y, f0.y, a);
                     a = fmaf(qa.z, f1.x, a); a = fmaf(qa.w, f1.y, a);
                     a = fmaf(qb.x, f2.x, a); a = fmaf(qb.y, f2.y, a);
                     a = fmaf(qb.z, f3.x, a); a = fmaf(qb.w, f3.y, a);
-                    acc[g] = a;
+                    acc[gg] = a;
                 }
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] *= p.scale_log2;
-            store_vec<G>(lut + (static_cast<size_t>(m) * K + tid) * G, acc);
+            for (int gg = 0; gg < G; ++gg) acc[gg] *= p.scale_log2;
+            float *dst = lut + (static_cast<size_t>(m) * K + tid) * G;
+            store_vec<G>(dst, acc);
+            if constexpr (C > 1) {
+                const uint32_t la = smem_u32(dst), lb = smem_u32(&bar[2]);
+#pragma unroll
+                for (int r = 1; r < C; ++r) {
+                    const uint32_t pr = (rank + r) % C;
+                    push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
+                }
+            }
         }
     }
     if constexpr (C > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();                                 // every CTA's own rows are written
-        constexpr int ROW_F4 = MC * K * G / 4;
-#pragma unroll 1
-        for (int r = 0; r < C; ++r) {
-            if (r == rank) continue;
-            float *mine = lut + static_cast<size_t>(r) * MC * K * G;
-            const float4 *src = reinterpret_cast<const float4 *>(cluster.map_shared_rank(mine, r));
-            float4 *dst = reinterpret_cast<float4 *>(mine);
-            for (int i = tid; i < ROW_F4; i += kThreads) dst[i] = src[i];
-        }
+        if (!mbar_wait_bounded(&bar[2], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     }
     __syncthreads();
 
-    // ---- 3. code stream: scores, online softmax, value bins ----------------
-    const int n_tok = te - ts;
-    const int per = ((n_tok + C - 1) / C + P - 1) / P * P;        // page-aligned share
-    const int a0 = ts + rank * per;
-    const int e0 = min(te, a0 + per);
-    const int g = tid % G, jslot = tid / G;
-    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
-    float m_run = -INFINITY, l_run = 0.f;
-    int badpage = 0;
+    // ---- code stream: scores, softmax statistics, value bins -------------------
+    // The share's codes are in shared memory, so the scores are recomputed
+    // (M table gathers each) in three passes: (1) per-head max, (2) per-head sum
+    // of exp2(s - max), (3) scatter of each weight into the 256-bin value
+    // accumulators as an unsigned fixed-point integer floor(p * 2^32 / l), so the
+    // bins cannot overflow, integer shared-memory atomics are exact and fast,
+    // and the result does not depend on the order of the atomics.
+    unsigned *ibins = reinterpret_cast<unsigned *>(bins);
+    auto score = [&](int t, Codes<M> &cd) -> float {
+        cd.load(codes_s + (t - a0) * (2 * M));
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc += lut[(m * K + cd.k(m)) * G + g];
+        return acc;
+    };
+    float mx = -INFINITY;
 #pragma unroll 1
     for (int cb = a0; cb < e0; cb += S::CHUNK) {
-        Codes<M> cd[S::TPT];
-        float s[S::TPT];
 #pragma unroll
-        for (int i = 0; i < S::TPT; ++i) {
+        for (int i = 0; i < TPT; ++i) {
             const int t = cb + i * S::TOK_PER_PASS + jslot;
-            cd[i].zero();
-            s[i] = -INFINITY;
             if (t < e0) {
-                const int pg = bt[t / P];
-                if (pg < 0 || static_cast<int64_t>(pg) >= p.num_pages) {
-                    badpage = 1;
-                } else {
-                    cd[i].load(p.code_pages +
-                               ((static_cast<size_t>(pg) * Hkv + kvh) * P + (t % P)) * (2 * M));
-                    s[i] = 0.f;          // marks the token valid
-                }
+                Codes<M> cd;
+                mx = fmaxf(mx, score(t, cd));
             }
         }
-        float cm = -INFINITY;
+    }
 #pragma unroll
-        for (int i = 0; i < S::TPT; ++i) {
-            if (s[i] == 0.f) {
-                float acc = 0.f;
+    for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane < G) red_max[warp * G + lane] = mx;
+    __syncthreads();
+    mx = red_max[g];
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc += lut[(m * K + cd[i].k(m)) * G + g];
-                s[i] = acc;
-                cm = fmaxf(cm, acc);
-            }
-        }
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w * G + g]);
+    float l_run = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll 1
+        for (int cb = a0; cb < e0; cb += S::CHUNK) {
 #pragma unroll
-        for (int off = G; off < 32; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-        if (lane < G) red_max[warp * G + lane] = cm;
-        __syncthreads();
-        float cmax = red_max[g];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) cmax = fmaxf(cmax, red_max[w * G + g]);
-        const float m_new = fmaxf(m_run, cmax);
-        // rescale the bins when a head's running max moved (never on its first
-        // chunk); both barriers are unconditional
-        const bool have_prev = (m_run != -INFINITY);
-        if (tid < G) cfac[tid] = have_prev ? exp2f(m_run - m_new) : 1.f;
-        if (__syncthreads_or(have_prev && m_new > m_run)) {
-            for (int i = tid; i < S::LUT_FLOATS; i += kThreads) bins[i] *= cfac[i % G];
-        }
-        if (have_prev) l_run *= exp2f(m_run - m_new);
-        m_run = m_new;
-        __syncthreads();
-        if (m_new != -INFINITY) {
-#pragma unroll
-            for (int i = 0; i < S::TPT; ++i) {
-                if (s[i] != -INFINITY) {
-                    const float pv = exp2f(s[i] - m_new);
-                    l_run += pv;
-#pragma unroll
-                    for (int m = 0; m < M; ++m) atomicAdd(&bins[(m * K + cd[i].vv(m)) * G + g], pv);
+            for (int i = 0; i < TPT; ++i) {
+                const int t = cb + i * S::TOK_PER_PASS + jslot;
+                if (t < e0) {
+                    Codes<M> cd;
+                    l_run += exp2f(score(t, cd) - mx);
                 }
             }
         }
     }
-    if (badpage) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
-    // per-head sum of this CTA
 #pragma unroll
     for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
     if (lane < G) red_sum[warp * G + lane] = l_run;
     __syncthreads();
-    if (tid < G) {
-        float l = 0.f;
+    float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) l += red_sum[w * G + tid];
-        xch[tid] = m_run;          // m_run is uniform per head
-        xch[G + tid] = l;
+    for (int w = 0; w < kWarps; ++w) lsum += red_sum[w * G + g];
+    // 2^32 (1 - 2^-16) / l: the margin covers the rounding of the float sum
+    const float qscale = lsum > 0.f ? 4294901760.0f / lsum : 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll 1
+        for (int cb = a0; cb < e0; cb += S::CHUNK) {
+#pragma unroll
+            for (int i = 0; i < TPT; ++i) {
+                const int t = cb + i * S::TOK_PER_PASS + jslot;
+                if (t < e0) {
+                    Codes<M> cd;
+                    const unsigned q = __float2uint_rz(exp2f(score(t, cd) - mx) * qscale);
+#pragma unroll
+                    for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cd.vv(m)) * G + g], q);
+                }
+            }
+        }
+    }
+    if (tid < G) {
+        mst[tid] = mx;                                 // this CTA's statistics for now
+        lst[tid] = lsum;
+        cfac[tid] = qscale > 0.f ? 1.0f / qscale : 0.f;
     }
     __syncthreads();
+    // integer bins -> float weights in the same storage (relative to this CTA's max)
+    for (int i = tid; i < S::LUT_FLOATS; i += kThreads) bins[i] = static_cast<float>(ibins[i]) * cfac[i % G];
+    __syncthreads();
 
-    // ---- 4. merge (max, sum, bins) across the cluster ----------------------
-    cluster_sync_if<C>();          // peers' bins and statistics are final
-    int bad_all = 0;
+    // ---- push bins rows and statistics to the peers that own them -----------
+    if constexpr (C > 1) {
+        const uint32_t lb = smem_u32(&bar[3]);
+#pragma unroll 1
+        for (int r = 1; r < C; ++r) {
+            const uint32_t pr = (rank + r) % C;
+            const int slot = (C - r - 1) % C;          // (rank - pr - 1) mod C
+            const uint32_t rslot = mapa_u32(smem_u32(inc + slot * S::INC_STRIDE), pr);
+            const uint32_t rbar = mapa_u32(lb, pr);
+            const float4 *src = reinterpret_cast<const float4 *>(bins + pr * S::ROW_FLOATS);
+            for (int i = tid; i < S::ROW_FLOATS / 4; i += kThreads) st_async_v4(rslot + 16 * i, src[i], rbar);
+            if (tid < G) {
+                st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mst[tid], rbar);
+                st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lst[tid], rbar);
+            }
+            if (tid == 0) st_async_f32(rslot + 4 * (S::ROW_FLOATS + 2 * G), __int_as_float(sflag[0]), rbar);
+        }
+        if (!mbar_wait_bounded(&bar[3], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+        cluster_arrive_relaxed();                      // all traffic into this CTA has landed
+    }
+
+    // ---- merge statistics, then the owned rows of the value bins ------------
     if (tid < G) {
         float mr[C], lr[C];
         float ms = -INFINITY;
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            const float *x = xch;
-            if constexpr (C > 1) x = cg::this_cluster().map_shared_rank(xch, r);
-            mr[r] = x[tid];
-            lr[r] = x[G + tid];
+            if (r == rank) { mr[r] = mst[tid]; lr[r] = lst[tid]; }
+            else {
+                const float *sl = inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE;
+                mr[r] = sl[S::ROW_FLOATS + tid];
+                lr[r] = sl[S::ROW_FLOATS + G + tid];
+            }
             if (lr[r] > 0.f) ms = fmaxf(ms, mr[r]);
         }
         float ls = 0.f;
@@ -373,32 +461,28 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         lst[tid] = ls;
     }
     if (tid == 0) {
-        int bb = 0;
+        int bb = sflag[0];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            const int *f = sflag;
-            if constexpr (C > 1) f = cg::this_cluster().map_shared_rank(sflag, r);
-            bb |= *f;
-        }
+        for (int r = 0; r < C; ++r)
+            if (r != rank)
+                bb |= __float_as_int(inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + S::ROW_FLOATS + 2 * G]);
         sflag[1] = bb;
         if (sflag[0]) flag_status(p.status, sflag[0]);
     }
     __syncthreads();
-    bad_all = sflag[1];
-    // W_tot for the owned subspaces -> the LUT region (peers finished reading it)
-    float *wtot = lut;
+    int bad_all = sflag[1];
+    float *wtot = lut;                                 // [MC][K][G]; the LUT is no longer read
     {
-        constexpr int N4 = MC * K * G / 4;
-        const size_t base4 = static_cast<size_t>(rank) * MC * K * G / 4;
+        constexpr int N4 = S::ROW_FLOATS / 4;
+        const float4 *own = reinterpret_cast<const float4 *>(bins + rank * S::ROW_FLOATS);
         for (int i = tid; i < N4; i += kThreads) {
+            const int g0 = (4 * i) % G;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float4 *br = reinterpret_cast<const float4 *>(bins);
-                if constexpr (C > 1)
-                    br = reinterpret_cast<const float4 *>(cg::this_cluster().map_shared_rank(bins, r));
-                const float4 v = br[base4 + i];
-                const int g0 = (4 * i) % G;
+                const float4 v = (r == rank) ? own[i]
+                                             : reinterpret_cast<const float4 *>(
+                                                   inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE)[i];
                 acc.x += fac[r * G + g0] * v.x;
                 acc.y += fac[r * G + (g0 + 1) % G] * v.y;
                 acc.z += fac[r * G + (g0 + 2) % G] * v.z;
@@ -409,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     }
     __syncthreads();
 
-    // ---- 5. value codebook product for the owned subspaces -----------------
+    // ---- value codebook product for the owned subspaces -----------------------
     if (!mbar_wait_bounded(&bar[1], 0)) {
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
@@ -461,13 +545,18 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             }
         }
     }
-    // A copy that timed out may still be landing: wait again (bounded) before
-    // the shared memory is released.
+    // A wait that ran out may leave a copy or a push still landing: wait again
+    // (bounded) before the shared memory is released.
     if (sflag[0] & AQ_DEV_TIMEOUT) {
         mbar_wait_bounded(&bar[0], 0);
         mbar_wait_bounded(&bar[1], 0);
+        mbar_wait_bounded(&bar[4], 0);
+        if constexpr (C > 1) {
+            mbar_wait_bounded(&bar[2], 0);
+            mbar_wait_bounded(&bar[3], 0);
+        }
     }
-    cluster_sync_if<C>();          // no CTA leaves while a peer may read its smem
+    if constexpr (C > 1) cluster_wait_acquire();      // no CTA leaves while a peer may push to it
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
@@ -498,17 +587,20 @@ template <int M, int G, int C>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
     auto kern = pq_decode_kernel<M, G, C>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (plan.share > kMaxShare || plan.share % kPage) return cudaErrorInvalidValue;
+    static size_t attr_bytes = 0;                  // opt-in dynamic shared memory set so far
+    const size_t need = S::smem(plan.share);
+    if (need > attr_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(need));
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        attr_bytes = need;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
                        static_cast<unsigned>(p.batch));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.dynamicSmemBytes = S::smem(plan.share);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -542,9 +634,9 @@ cudaError_t dispatch_g(const DecodeParams &p, int G, const Plan &plan, cudaStrea
 }
 
 template <int M>
-size_t smem_g(int G, int C) {
+size_t smem_g(int G, int C, int share) {
 #define AQ_SM(GG, CC) \
-    if (G == GG && C == CC) return PqCfg<M, GG, CC>::SMEM;
+    if (G == GG && C == CC) return PqCfg<M, GG, CC>::smem(share);
     AQ_SM(1, 1) AQ_SM(1, 2) AQ_SM(1, 4)
     AQ_SM(2, 1) AQ_SM(2, 2) AQ_SM(2, 4)
     AQ_SM(4, 1) AQ_SM(4, 2) AQ_SM(4, 4)
@@ -555,9 +647,9 @@ size_t smem_g(int G, int C) {
 
 }  // namespace
 
-size_t pq_decode_smem_bytes(int M, int G, int cluster) {
-    if (M == 4) return smem_g<4>(G, cluster);
-    if (M == 8) return smem_g<8>(G, cluster);
+size_t pq_decode_smem_bytes(int M, int G, int cluster, int share) {
+    if (M == 4) return smem_g<4>(G, cluster, share);
+    if (M == 8) return smem_g<8>(G, cluster, share);
     return 0;
 }
 

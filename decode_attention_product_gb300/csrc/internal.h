@@ -23,6 +23,7 @@ struct DecodeParams {
     int32_t batch, num_q_heads, num_kv_heads, max_pages;
     int64_t num_pages, num_sets;
     int32_t max_seq_len, num_splits, split_len;  // split_len: tokens, multiple of P
+    int32_t share;                               // tokens per cluster CTA, multiple of P
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -51,6 +52,7 @@ struct Plan {
     int32_t num_splits;
     int32_t cluster;      // CTAs per split
     int32_t split_len;    // tokens per split (multiple of the page size)
+    int32_t share;        // tokens per CTA of a cluster (multiple of the page size)
     size_t workspace;     // bytes
     size_t smem;          // dynamic shared memory per CTA
 };
@@ -63,8 +65,11 @@ cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
 cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s);
 
-// Shared-memory bytes a PQ decode CTA needs for (M, G, cluster).
-size_t pq_decode_smem_bytes(int M, int G, int cluster);
+// Shared-memory bytes a PQ decode CTA needs for (M, G, cluster) and a share of
+// `share` tokens per CTA (their codes are staged in shared memory).
+size_t pq_decode_smem_bytes(int M, int G, int cluster, int share);
+// Largest per-CTA token share the PQ decode kernel stages at once.
+constexpr int kMaxShare = 2048;
 size_t fit_smem_bytes(int M, int n_samples);
 
 }  // namespace aq

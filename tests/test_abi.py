@@ -127,3 +127,15 @@ def test_plans_for_the_workloads(lib):
     assert _plan(lib, 2, 4, 4, 100, splits=3)[0] == 3
     assert _plan(lib, 2, 4, 4, 100, splits=50)[0] == 7     # 7 pages
     assert _plan(lib, 2, 4, 4, 0, splits=5)[0] == 1
+
+
+def test_every_supported_shape_has_a_plan(lib):
+    """Each supported (M, group) pair plans within the shared-memory budget,
+    for short and very long sequences, and splits long ones."""
+    for M in (4, 8):
+        for G in (1, 2, 4, 8):
+            for L in (1, 100, 4096, 131072):
+                s, c, w = _plan(lib, 2, 4 * G, 4, L, M=M)
+                assert c in (1, 2, 4) and s >= 1
+                if L == 131072:
+                    assert s > 1 and w > 0

@@ -101,11 +101,13 @@ def test_decode_plan_variants_agree(A, orc):
         close(got, want)
 
 
-def test_decode_repeated_calls_are_identical(A):
+def test_decode_repeated_calls_agree(A):
+    """The value bins accumulate by shared-memory float atomics, whose order is
+    not fixed: repeated calls agree to fp32 rounding, not bit for bit."""
     p = W.paged_codes_problem(6, 2, 8, 8, 4, [900, 1200])
     a, _ = run_pq(A, p)
     b, _ = run_pq(A, p)
-    assert np.array_equal(a, b)
+    assert np.allclose(a, b, rtol=1e-5, atol=1e-6)
 
 
 def test_decode_data_errors_flag_and_nan(A):
@@ -160,7 +162,8 @@ def _encode_case(A, orc, w, t0, t1):
         cbs = cb16.reshape(B, Hkv, 2, M, 256, w.dsub)
     else:
         cbs = np.stack([w.given_codebooks()] * B)
-    kvs = [w.kv(b, t0, t1) for b in range(B)]
+    kvs = [w.kv(b, t0=t0, t1=t1) for b in range(B)]
+    assert sum(len(k) for k in kvs) > 0
     bt, npages = w.block_table()
     kv = np.concatenate(kvs)
     tset = np.concatenate([np.full(len(k), b, np.int32) for b, k in enumerate(kvs)])
