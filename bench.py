@@ -41,6 +41,26 @@ METRIC = "PQ-KV decode attention: KV tokens·heads/s; code-stream GB/s as % of H
 UNIT = "KV tokens*heads/s"
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (the job finishes with its slowest
+    rank); x itself when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    if device is None:
+        device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: int, steps: int, seconds: float, world: int) -> float:
+    """Whole-job throughput under weak scaling: every rank processes the same
+    per-GPU workload, the job takes the slowest rank's time."""
+    return world * units_per_rank * steps / seconds
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -338,13 +358,10 @@ def run_ours(args, w, rank, world, local_rank):
         torch.cuda.synchronize()
         dec_ms = [e0.elapsed_time(e1) / (reps * R)]
         dec_how = "decode-only graph of back-to-back launches (events around the replays)"
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     units = T.kv_tokens_heads(w.seq_lens, Hkv)
-    value = world * units * args.steps / (total_ms / 1e3)
+    value = job_value(units, args.steps, total_ms / 1e3, world)
     # roofline of the decode kernel (algorithmic bytes per launch / event time)
     byt = T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M)
     dec_avg_ms = float(np.mean(dec_ms))
@@ -416,11 +433,8 @@ def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
         ds.replay(wait=True)
     secs = time.perf_counter() - t0
     ds.check_status()
-    if dist:
-        t = torch.tensor([secs], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
-    return {"value": world * units * args.steps / secs, "unit": UNIT,
+    secs = max_over_ranks(secs)
+    return {"value": job_value(units, args.steps, secs, world), "unit": UNIT,
             "h2d_bytes_per_step": q_h.numel() * 4 + kv_h.numel() * 2,
             "d2h_bytes_per_step": out_h.numel() * 4, "ms_per_step": 1e3 * secs / args.steps,
             "how": "api.DecodeStep graph replay per step, host waits for the output"}
