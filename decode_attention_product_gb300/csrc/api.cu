@@ -39,6 +39,12 @@ bool group_ok(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) {
+    cudaGetLastError();
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+}
+
 // The plan is a pure function of the arguments (no device query), so that
 // aq_decode_plan and the decode call always agree: it is sized for GB300
 // (152 SMs, 227 KiB of opt-in shared memory per CTA).

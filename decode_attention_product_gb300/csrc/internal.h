@@ -71,5 +71,8 @@ size_t pq_decode_smem_bytes(int M, int G, int cluster, int share);
 // Largest per-CTA token share the PQ decode kernel stages at once.
 constexpr int kMaxShare = 2048;
 size_t fit_smem_bytes(int M, int n_samples);
+// Record a CUDA error for aq_last_error_message() and clear the runtime's
+// last-error state.
+void record_cuda_error(cudaError_t e);
 
 }  // namespace aq

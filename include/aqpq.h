@@ -225,6 +225,39 @@ aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch,
                                    void *workspace, size_t workspace_bytes,
                                    int32_t *device_status, aq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * aq_decode_attention_noalloc -- aq_decode_attention for callers that cannot
+ * allocate device memory.  (The pages describe no such variant: it is an
+ * interface convenience of this library.)
+ *
+ * Splitting long sequences needs device scratch for the per-split (max, sum,
+ * output) partials, which aq_decode_attention takes from the caller.  A
+ * caller that is handed only the call's tensors (a plugin or operator that
+ * must not draw on the host framework's memory pool), whose device memory is
+ * fully reserved elsewhere, or that runs where allocation is not allowed (it
+ * can synchronise the device and can fail) uses this entry point instead: the
+ * partials live in one fixed 4 MiB array owned by the library, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Arguments, layouts and results are those of aq_decode_attention without the
+ * workspace.  A call whose planned scratch exceeds 4 MiB (batch * Hq * splits *
+ * (D + 2) * 4 bytes) returns AQ_ERR_WORKSPACE_TOO_SMALL before any launch; no
+ * call allocates or frees memory.  The array's device address is looked up
+ * once per device by the first call made with that device current, so make
+ * that first call before any stream capture.  All calls share the array: two
+ * calls whose kernels overlap on the GPU (other streams, other host threads)
+ * race on it.  Nothing in it needs clearing between calls.
+ * ------------------------------------------------------------------------- */
+aq_status aq_decode_attention_noalloc(const aq_pq_config *cfg, int32_t batch,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      const float *q, const uint8_t *code_pages,
+                                      int64_t num_pages, const void *codebooks_f16,
+                                      int64_t num_sets, const int32_t *req_set,
+                                      const int32_t *block_table, int32_t max_pages,
+                                      const int32_t *seq_lens, int32_t max_seq_len,
+                                      float scale, int32_t num_splits, float *out,
+                                      int32_t *device_status, aq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
