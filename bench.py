@@ -273,6 +273,13 @@ def run_ours(args, w, rank, world, local_rank):
 
     def step(i, ev0=None, ev1=None):
         c = copies[i % R]
+        if not args.two_call:
+            # one fused launch: append the new token + attention; overlapping the
+            # previous step's tail (codebooks and req_set are not written by it)
+            api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                            c["seq_lens"], Lmax, w.scale, overlap=True, out=outs[i % R], workspace=ws,
+                            status=status)
+            return
         api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)
         if ev0 is not None:
             ev0.record()
@@ -302,14 +309,17 @@ def run_ours(args, w, rank, world, local_rank):
                 step(i, e0, e1)
         return g
 
-    try:
-        g_full = capture(R, True)
-        events_in_graph = True
-    except Exception:                                   # torch without external events
-        torch.cuda.synchronize()
-        evpairs.clear()
+    events_in_graph = False
+    if args.two_call:
+        try:
+            g_full = capture(R, True)
+            events_in_graph = True
+        except Exception:                               # torch without external events
+            torch.cuda.synchronize()
+            evpairs.clear()
+            g_full = capture(R, False)
+    else:
         g_full = capture(R, False)
-        events_in_graph = False
     n_full, n_tail = divmod(args.steps, R)
     g_tail = capture(n_tail, False) if n_tail else None
     for _ in range(2):
@@ -335,7 +345,11 @@ def run_ours(args, w, rank, world, local_rank):
         torch.distributed.barrier()
     clk = clocks.stop()
     total_ms = t_begin.elapsed_time(t_end)
-    if events_in_graph and n_full > 0:
+    if not args.two_call:
+        dec_ms = [total_ms / args.steps]
+        dec_how = ("one fused kernel per step: timed region / K launches (CUDA events around "
+                   "the graph replays)")
+    elif events_in_graph and n_full > 0:
         dec_ms = [e0.elapsed_time(e1) for e0, e1 in evpairs]
         dec_how = "events around each decode launch inside the replayed step graph (last replay)"
     else:
@@ -363,7 +377,8 @@ def run_ours(args, w, rank, world, local_rank):
     units = T.kv_tokens_heads(w.seq_lens, Hkv)
     value = job_value(units, args.steps, total_ms / 1e3, world)
     # roofline of the decode kernel (algorithmic bytes per launch / event time)
-    byt = T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M)
+    byt = (T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M) if args.two_call
+           else T.pq_step_bytes(w.seq_lens, Hq, Hkv, M))
     dec_avg_ms = float(np.mean(dec_ms))
     peak, peak_kind = measured_peaks()
     achieved = byt["total"] / (dec_avg_ms / 1e3) / 1e9
@@ -387,15 +402,18 @@ def run_ours(args, w, rank, world, local_rank):
                    "num_codewords": w.num_codewords, "plan": {"splits": splits, "cluster": cluster},
                    "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB "
                          f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)" if R > 1 else "none",
-                   "step": "append 1 token/request (encode) + PQ decode attention"},
+                   "step": ("append 1 token/request (encode) + PQ decode attention, two launches"
+                            if args.two_call else
+                            "fused launch: append 1 token/request + PQ decode attention "
+                            "(aq_decode_step, programmatic dependent launch)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "pq_decode_kernel",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": "pq_decode_kernel" + ("" if args.two_call else " (fused step)"),
                      "bytes_per_launch": byt["total"], "launch_ms": dec_avg_ms,
                      "peak_kind": peak_kind, "timing": dec_how},
         "code_stream": {"gbs": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9,
                         "codes_only_gbs": byt["codes"] / (dec_avg_ms / 1e3) / 1e9,
                         "frac_of_peak": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9 / peak},
-        "gpu_launches": args.steps * (2 + (1 if splits > 1 else 0)),
+        "gpu_launches": args.steps * ((2 if args.two_call else 1) + (1 if splits > 1 else 0)),
         "clocks": clk,
         "prefill": {"fit_ms": base["fit_ms"], "encode_ms": base["encode_prefill_ms"]},
     }
@@ -500,6 +518,8 @@ def main():
     ap.add_argument("--no-fp16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--two-call", action="store_true",
+                    help="time aq_encode_append + aq_decode_attention instead of the fused step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

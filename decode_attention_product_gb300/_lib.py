@@ -17,6 +17,7 @@ AQ_OK = 0
 STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARGUMENT", 2: "AQ_ERR_UNSUPPORTED",
                 3: "AQ_ERR_WORKSPACE_TOO_SMALL", 4: "AQ_ERR_CUDA"}
 DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_SET, DEV_TIMEOUT = 1, 2, 4, 8
+STEP_OVERLAP = 1
 
 # every symbol include/aqpq.h declares, with its ctypes signature
 P = ctypes.c_void_p
@@ -33,6 +34,8 @@ SIGNATURES = {
                              P, P, sz, P, P], i32),
     "aq_decode_attention_fp16": ([P, i32, i32, i32, P, P, i64, P, i32, P, i32, f32, i32, P, P, sz,
                                   P, P], i32),
+    "aq_decode_step": ([P, i32, i32, i32, P, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32, i32,
+                        P, P, sz, P, P], i32),
     "aq_decode_attention_noalloc": ([P, i32, i32, i32, P, P, i64, P, i64, P, P, i32, P, i32, f32,
                                      i32, P, P, P], i32),
 }

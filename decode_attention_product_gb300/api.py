@@ -142,6 +142,41 @@ def decode_attention(q: torch.Tensor, code_pages: torch.Tensor, codebooks: torch
     return out
 
 
+def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
+                codebooks: torch.Tensor, req_set: torch.Tensor, block_table: torch.Tensor,
+                seq_lens: torch.Tensor, max_seq_len: int, scale: float | None = None,
+                num_splits: int = 0, overlap: bool = False, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None,
+                status: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused decode step: append kv_new [B][Hkv][2][D] fp16 (the token at
+    position seq_lens[b]-1) to code_pages, then PQ decode attention over all
+    seq_lens[b] tokens; returns out [B][Hq][D] fp32."""
+    _need(q, torch.float32, "q", 3)
+    _need(kv_new, torch.float16, "kv_new", 4)
+    _need(code_pages, torch.uint8, "code_pages", 5)
+    _need(codebooks, torch.float16, "codebooks", 6)
+    _need(req_set, torch.int32, "req_set", 1)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    Hkv, M = codebooks.shape[1], codebooks.shape[3]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
+    cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
+    st = _lib.load().aq_decode_step(
+        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_new), _ptr(code_pages), code_pages.shape[0],
+        _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), max_seq_len, float(scale), num_splits, _lib.STEP_OVERLAP if overlap else 0,
+        _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status),
+        _stream())
+    _lib.check(st, "aq_decode_step")
+    return out
+
+
 def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
                           seq_lens: torch.Tensor, max_seq_len: int, scale: float | None = None,
                           num_splits: int = 0, out: torch.Tensor | None = None,
@@ -172,10 +207,11 @@ def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: 
 
 class DecodeStep:
     """One decode step of a fixed batch: append each request's current K/V
-    token into the PQ code cache, then PQ decode attention over the cache.
+    token (the one at position seq_len-1) into the PQ code cache, then PQ
+    decode attention over the cache, as one aq_decode_step launch.
 
     Holds the cache tensors, the workspace, the output and a device status
-    word.  `run(q, new_kv)` launches the two C-ABI calls on the current stream.
+    word.  `run(q, new_kv)` launches the step on the current stream.
     `capture_host(q_host, kv_host, out_host)` records the whole step -- copies
     of the pinned host inputs to the device, the two calls, the copy of the
     output back to pinned host memory -- into a CUDA graph; `replay()` launches
@@ -201,12 +237,10 @@ class DecodeStep:
         self._host = None
 
     def run(self, q, new_kv, out=None):
-        encode_append(new_kv, self.new_set, self.new_slot, self.codebooks, self.code_pages,
-                      self.status)
-        return decode_attention(q, self.code_pages, self.codebooks, self.req_set, self.block_table,
-                                self.seq_lens, self.max_seq_len, self.scale, self.num_splits,
-                                out=self.out if out is None else out, workspace=self.workspace,
-                                status=self.status)
+        return decode_step(q, new_kv, self.code_pages, self.codebooks, self.req_set,
+                           self.block_table, self.seq_lens, self.max_seq_len, self.scale,
+                           self.num_splits, out=self.out if out is None else out,
+                           workspace=self.workspace, status=self.status)
 
     def capture_host(self, q_host, kv_host, out_host):
         """Capture copy-in, step, copy-out into a CUDA graph (pinned host tensors)."""

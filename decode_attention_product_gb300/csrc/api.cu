@@ -243,6 +243,7 @@ aq_status aq_decode_plan(const aq_pq_config *cfg, int32_t batch, int32_t num_q_h
 
 static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, int32_t Hq, int32_t Hkv,
                              const float *q, const uint8_t *code_pages, const void *kv_pages,
+                             const void *kv_new, uint8_t *code_pages_w, int32_t flags,
                              int64_t num_pages, const void *codebooks, int64_t num_sets,
                              const int32_t *req_set, const int32_t *block_table, int32_t max_pages,
                              const int32_t *seq_lens, int32_t max_seq_len, float scale,
@@ -255,6 +256,8 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     if (batch == 0) return AQ_OK;
     if (!q || !out || !block_table || !seq_lens) return AQ_ERR_INVALID_ARGUMENT;
     if (fp16 ? !kv_pages : (!code_pages || !codebooks || !req_set)) return AQ_ERR_INVALID_ARGUMENT;
+    if (kv_new && !code_pages_w) return AQ_ERR_INVALID_ARGUMENT;
+    if (flags & ~AQ_STEP_OVERLAP) return AQ_ERR_INVALID_ARGUMENT;
     if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
     Plan pl{};
     st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl);
@@ -285,9 +288,13 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.split_len = pl.split_len;
     p.share = pl.share;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_new = kv_new;
+    p.code_pages_w = code_pages_w;
+    p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = fp16 ? launch_fp16_decode(p, Hq / Hkv, pl, s)
-                         : launch_pq_decode(p, cfg->num_subspaces, Hq / Hkv, pl, s);
+    cudaError_t e = fp16     ? launch_fp16_decode(p, Hq / Hkv, pl, s)
+                    : kv_new ? launch_pq_decode_step(p, cfg->num_subspaces, Hq / Hkv, pl, s)
+                             : launch_pq_decode(p, cfg->num_subspaces, Hq / Hkv, pl, s);
     return e == cudaSuccess ? AQ_OK : cuda_fail(e);
 }
 
@@ -298,9 +305,22 @@ aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch, int32_t nu
                               const int32_t *seq_lens, int32_t max_seq_len, float scale,
                               int32_t num_splits, float *out, void *workspace, size_t workspace_bytes,
                               int32_t *device_status, aq_stream_t stream) {
-    return decode_impl(cfg, false, batch, num_q_heads, num_kv_heads, q, code_pages, nullptr, num_pages,
-                       codebooks_f16, num_sets, req_set, block_table, max_pages, seq_lens, max_seq_len,
-                       scale, num_splits, out, workspace, workspace_bytes, device_status, stream);
+    return decode_impl(cfg, false, batch, num_q_heads, num_kv_heads, q, code_pages, nullptr, nullptr, nullptr, 0,
+                       num_pages, codebooks_f16, num_sets, req_set, block_table, max_pages, seq_lens,
+                       max_seq_len, scale, num_splits, out, workspace, workspace_bytes, device_status, stream);
+}
+
+aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                         const float *q, const void *kv_new_f16, uint8_t *code_pages, int64_t num_pages,
+                         const void *codebooks_f16, int64_t num_sets, const int32_t *req_set,
+                         const int32_t *block_table, int32_t max_pages, const int32_t *seq_lens,
+                         int32_t max_seq_len, float scale, int32_t num_splits, int32_t flags, float *out,
+                         void *workspace, size_t workspace_bytes, int32_t *device_status, aq_stream_t stream) {
+    if (batch > 0 && !kv_new_f16) return AQ_ERR_INVALID_ARGUMENT;
+    return decode_impl(cfg, false, batch, num_q_heads, num_kv_heads, q, code_pages, nullptr, kv_new_f16,
+                       code_pages, flags, num_pages, codebooks_f16, num_sets, req_set, block_table, max_pages,
+                       seq_lens, max_seq_len, scale, num_splits, out, workspace, workspace_bytes,
+                       device_status, stream);
 }
 
 aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
@@ -309,8 +329,8 @@ aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch, int32
                                    const int32_t *seq_lens, int32_t max_seq_len, float scale,
                                    int32_t num_splits, float *out, void *workspace,
                                    size_t workspace_bytes, int32_t *device_status, aq_stream_t stream) {
-    return decode_impl(cfg, true, batch, num_q_heads, num_kv_heads, q, nullptr, kv_pages_f16, num_pages,
-                       nullptr, 0, nullptr, block_table, max_pages, seq_lens, max_seq_len, scale,
+    return decode_impl(cfg, true, batch, num_q_heads, num_kv_heads, q, nullptr, kv_pages_f16, nullptr, nullptr, 0,
+                       num_pages, nullptr, 0, nullptr, block_table, max_pages, seq_lens, max_seq_len, scale,
                        num_splits, out, workspace, workspace_bytes, device_status, stream);
 }
 

@@ -48,8 +48,8 @@ struct PqCfg {
     static constexpr int TPT = 8;                           // tokens per thread per chunk
     static constexpr int TOK_PER_PASS = kThreads / G;
     static constexpr int CHUNK = TOK_PER_PASS * TPT;
-    // statistics pushed with the bins: m[G], l[G], bad flag
-    static constexpr int STAT_FLOATS = 2 * G + 1;
+    // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag
+    static constexpr int STAT_FLOATS = 3 * G + 1;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
     // V-product thread mapping
     static constexpr int NJP = MC * DSUB / 2;               // owned j-pairs
@@ -67,7 +67,11 @@ struct PqCfg {
     static constexpr int OFF_Q = OFF_INC + (C > 1 ? (C - 1) * INC_STRIDE * 4 : 0);
     static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_max, red_sum [kWarps][G]
     static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mst, lst, cfac [G], fac [C][G]
-    static constexpr int OFF_CODES = (OFF_STAT + (3 + C) * G * 4 + 15) / 16 * 16;  // [share][2M] uint8
+    // fused step: the new token's owned sub-vectors [2][MC][DSUB] f32, its codes
+    // [2][M] int, its score [G], argmin keys [kWarps] u64
+    static constexpr int OFF_NEW = (OFF_STAT + (3 + C) * G * 4 + 15) / 16 * 16;
+    static constexpr int NEW_BYTES = 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 8 * kWarps + 8;
+    static constexpr int OFF_CODES = (OFF_NEW + NEW_BYTES + 15) / 16 * 16;  // [share][2M] uint8
     static constexpr int PAGE_BYTES = P * 2 * M;            // one page's codes for one kv head
     static constexpr int PPL = kMaxShare / P / 32;          // page ids per lane of warp 0
     static size_t smem(int share) { return OFF_CODES + static_cast<size_t>(share) * 2 * M; }
@@ -147,12 +151,45 @@ struct Codes<8> {
     }
 };
 
-template <int M, int G, int C>
+// Nearest codeword of x (DSUB floats in shared memory) among the 256 rows of a
+// codebook slice in shared memory: one thread per codeword, fp32 squared
+// distance with separately rounded subtract / multiply / add in increasing j,
+// lowest index on ties (the encode decision rule).  CTA-wide; returns the code
+// to every thread.
+template <int DSUB>
+__device__ __forceinline__ int block_nearest(const float *x, const __half *rows, unsigned long long *keys) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const __half *r = rows + static_cast<size_t>(tid) * DSUB;
+    float d = 0.f;
+#pragma unroll
+    for (int j = 0; j < DSUB; ++j) {
+        const float e = __fsub_rn(x[j], __half2float(r[j]));
+        d = __fadd_rn(d, __fmul_rn(e, e));
+    }
+    unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d)) << 32) | static_cast<unsigned>(tid);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+        key = o < key ? o : key;
+    }
+    __syncthreads();                                   // keys[] free from a previous use
+    if (lane == 0) keys[warp] = key;
+    __syncthreads();
+    unsigned long long best = keys[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) best = keys[w] < best ? keys[w] : best;
+    return static_cast<int>(best & 0xffu);
+}
+
+// APPEND = the fused decode step: the token at position seq_len-1 of every
+// request is encoded here (each cluster CTA encodes the subspaces it owns) and
+// written to its page slot, and the attention includes it.
+template <int M, int G, int C, bool APPEND>
 __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
     constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in, codes+q
     int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);           // [0] local bad, [1] all
     __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
     __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
@@ -166,6 +203,12 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     float *lst = mst + G;
     float *cfac = lst + G;
     float *fac = cfac + G;                                              // [C][G]
+    float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);        // [2][MC][DSUB]
+    int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);          // [2][M]
+    float *snew = reinterpret_cast<float *>(newc + 2 * M);              // [G]
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(
+        smem + ((S::OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8));
+    uint8_t *codes_s = smem + S::OFF_CODES;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int rank = 0;
@@ -175,23 +218,40 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
-    uint8_t *codes_s = smem + S::OFF_CODES;
     if (tid == 0) {
 #pragma unroll
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         sflag[0] = 0;
     }
-    // ---- independent loads first: length, codebook set, page ids ------------
-    // A CTA's token share does not depend on the request length, so warp 0
-    // fetches its page ids in parallel with the length.
+    // ---- codebook set and the K slice first: the only reads allowed before
+    // the preceding kernel on the stream completes (programmatic dependent
+    // launch): codebooks and req_set are not written by it ------------------
     const int share = p.share;
     const int ts = split * p.split_len;
     const int a0 = ts + rank * share;
     const int g = tid % G, jslot = tid / G;
     const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
-    const int L_raw = __ldg(p.seq_lens + b);
     const int set = __ldg(p.req_set + b);
+    const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
+    const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
+    const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
+                       ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
+                       static_cast<size_t>(rank) * S::CB_HALVES;
+    const __half *gV = gK + cb_unit;
+    uint64_t pol = 0;
+    if (warp == 0) {
+        __syncwarp();
+        if (lane == 0 && set_ok) {
+            pol = policy_evict_first();
+            mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
+            bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
+        }
+    }
+    grid_dependency_wait();
+
+    // ---- length and page ids ----------------------------------------------
+    const int L_raw = __ldg(p.seq_lens + b);
     int pgw[S::PPL];
     if (warp == 0) {
         const int np_lim = min(share / P, p.max_pages - a0 / P);
@@ -205,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
     if (L_raw < 0 || L_raw > p.max_pages * P || L_raw > p.max_seq_len) bad0 |= AQ_DEV_BAD_LENGTH;
-    if (set < 0 || static_cast<int64_t>(set) >= p.num_sets) bad0 |= AQ_DEV_BAD_SET;
+    if (!set_ok) bad0 |= AQ_DEV_BAD_SET;
     const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
     if (bad0 || ts >= te) {
         // nothing to stream: NaN for a bad request, zeros / empty partials otherwise
@@ -222,25 +282,34 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                 }
             }
         }
+        if (tid == 0 && set_ok) mbar_wait_bounded(&bar[0], 0);   // the K slice copy lands first
         return;
     }
     const int e0 = min(te, a0 + share);
-    const int npg = e0 > a0 ? (e0 - a0 + P - 1) / P : 0;
-
-    // ---- warp 0 issues every copy: K slice, code pages + query, V slice ----
-    const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
-    const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
-                       ((static_cast<size_t>(set) * Hkv + kvh) * 2) * cb_unit +
-                       static_cast<size_t>(rank) * S::CB_HALVES;
-    const __half *gV = gK + cb_unit;
-    if (warp == 0) {
-        __syncwarp();
-        uint64_t pol = 0;
-        if (lane == 0) {
-            pol = policy_evict_first();
-            mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
-            bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
+    // the fused step's new token: position L-1, held by the cluster of its split
+    // and streamed by no CTA (it is scored from its fresh codes instead)
+    const int new_pos = APPEND ? L_raw - 1 : -1;
+    const bool cl_new = APPEND && new_pos >= ts && new_pos < te;
+    const bool own_new = cl_new && new_pos >= a0 && new_pos < e0;
+    const int eS = own_new ? new_pos : e0;
+    const int npg = eS > a0 ? (eS - a0 + P - 1) / P : 0;
+    int pg_new = -1;
+    if (cl_new) {
+        pg_new = __ldg(bt + new_pos / P);
+        if (pg_new < 0 || static_cast<int64_t>(pg_new) >= p.num_pages) {
+            if (tid == 0) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+            pg_new = -1;
         }
+        if (tid < 2 * MC * DSUB) {                     // owned sub-vectors of the new K and V
+            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
+            const __half *xg = reinterpret_cast<const __half *>(p.kv_new) +
+                               ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D + rank * MC * DSUB + r;
+            xnew[tid] = __half2float(__ldg(xg));
+        }
+    }
+
+    // ---- warp 0 issues the rest: code pages + query, then the V slice ------
+    if (warp == 0) {
         bool ok[S::PPL];
         int nvalid = 0, bad = 0;
 #pragma unroll
@@ -268,13 +337,15 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
             bulk_g2s_hint(cbv, gV, S::CB_BYTES, &bar[1], pol);
             if constexpr (C > 1) {
-                mbar_arrive_expect_tx(&bar[2], (C - 1) * S::ROW_FLOATS * 4);
+                mbar_arrive_expect_tx(&bar[2], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
                 mbar_arrive_expect_tx(&bar[3], (C - 1) * (S::ROW_FLOATS + S::STAT_FLOATS) * 4);
             }
         }
     }
     for (int i = tid; i < S::LUT_FLOATS / 4; i += kThreads)
         reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < G) snew[tid] = -INFINITY;
+    grid_launch_dependents();                          // every read of this CTA is issued
     if constexpr (C > 1) {
         cluster_arrive_relaxed();          // peers' mbarriers exist before anyone pushes
         cluster_wait_acquire();
@@ -328,6 +399,27 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             }
         }
     }
+    if constexpr (APPEND) {
+        if (cl_new) {                                  // K codes of the new token, owned subspaces
+#pragma unroll 1
+            for (int mi = 0; mi < MC; ++mi) {
+                const int m = rank * MC + mi;
+                const int code = block_nearest<DSUB>(xnew + mi * DSUB, cbk + static_cast<size_t>(mi) * K * DSUB,
+                                                     keys);
+                if (tid == 0) {
+                    newc[m] = code;
+                    if constexpr (C > 1) {
+                        const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
+#pragma unroll
+                        for (int r = 1; r < C; ++r) {
+                            const uint32_t pr = (rank + r) % C;
+                            st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
+                        }
+                    }
+                }
+            }
+        }
+    }
     if constexpr (C > 1) {
         if (!mbar_wait_bounded(&bar[2], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     }
@@ -339,7 +431,9 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     // of exp2(s - max), (3) scatter of each weight into the 256-bin value
     // accumulators as an unsigned fixed-point integer floor(p * 2^32 / l), so the
     // bins cannot overflow, integer shared-memory atomics are exact and fast,
-    // and the result does not depend on the order of the atomics.
+    // and the result does not depend on the order of the atomics.  The fused
+    // step's new token enters (1) and (2) from its fresh codes; its value bin
+    // is added after the merge, once its V code is known.
     unsigned *ibins = reinterpret_cast<unsigned *>(bins);
     auto score = [&](int t, Codes<M> &cd) -> float {
         cd.load(codes_s + (t - a0) * (2 * M));
@@ -348,13 +442,22 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         for (int m = 0; m < M; ++m) acc += lut[(m * K + cd.k(m)) * G + g];
         return acc;
     };
-    float mx = -INFINITY;
+    float s_new = -INFINITY;
+    if constexpr (APPEND) {
+        if (own_new && tid < G) {
+            s_new = 0.f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) s_new += lut[(m * K + newc[m]) * G + tid];
+            snew[tid] = s_new;
+        }
+    }
+    float mx = s_new;
 #pragma unroll 1
-    for (int cb = a0; cb < e0; cb += S::CHUNK) {
+    for (int cb = a0; cb < eS; cb += S::CHUNK) {
 #pragma unroll
         for (int i = 0; i < TPT; ++i) {
             const int t = cb + i * S::TOK_PER_PASS + jslot;
-            if (t < e0) {
+            if (t < eS) {
                 Codes<M> cd;
                 mx = fmaxf(mx, score(t, cd));
             }
@@ -367,14 +470,14 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     mx = red_max[g];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w * G + g]);
-    float l_run = 0.f;
+    float l_run = (s_new != -INFINITY) ? exp2f(s_new - mx) : 0.f;
     if (mx != -INFINITY) {
 #pragma unroll 1
-        for (int cb = a0; cb < e0; cb += S::CHUNK) {
+        for (int cb = a0; cb < eS; cb += S::CHUNK) {
 #pragma unroll
             for (int i = 0; i < TPT; ++i) {
                 const int t = cb + i * S::TOK_PER_PASS + jslot;
-                if (t < e0) {
+                if (t < eS) {
                     Codes<M> cd;
                     l_run += exp2f(score(t, cd) - mx);
                 }
@@ -392,11 +495,11 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     const float qscale = lsum > 0.f ? 4294901760.0f / lsum : 0.f;
     if (mx != -INFINITY) {
 #pragma unroll 1
-        for (int cb = a0; cb < e0; cb += S::CHUNK) {
+        for (int cb = a0; cb < eS; cb += S::CHUNK) {
 #pragma unroll
             for (int i = 0; i < TPT; ++i) {
                 const int t = cb + i * S::TOK_PER_PASS + jslot;
-                if (t < e0) {
+                if (t < eS) {
                     Codes<M> cd;
                     const unsigned q = __float2uint_rz(exp2f(score(t, cd) - mx) * qscale);
 #pragma unroll
@@ -429,8 +532,9 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             if (tid < G) {
                 st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mst[tid], rbar);
                 st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lst[tid], rbar);
+                st_async_f32(rslot + 4 * (S::ROW_FLOATS + 2 * G + tid), snew[tid], rbar);
             }
-            if (tid == 0) st_async_f32(rslot + 4 * (S::ROW_FLOATS + 2 * G), __int_as_float(sflag[0]), rbar);
+            if (tid == 0) st_async_f32(rslot + 4 * (S::ROW_FLOATS + 3 * G), __int_as_float(sflag[0]), rbar);
         }
         if (!mbar_wait_bounded(&bar[3], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         cluster_arrive_relaxed();                      // all traffic into this CTA has landed
@@ -439,7 +543,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     // ---- merge statistics, then the owned rows of the value bins ------------
     if (tid < G) {
         float mr[C], lr[C];
-        float ms = -INFINITY;
+        float ms = -INFINITY, sn = snew[tid];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
             if (r == rank) { mr[r] = mst[tid]; lr[r] = lst[tid]; }
@@ -447,6 +551,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                 const float *sl = inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE;
                 mr[r] = sl[S::ROW_FLOATS + tid];
                 lr[r] = sl[S::ROW_FLOATS + G + tid];
+                sn = fmaxf(sn, sl[S::ROW_FLOATS + 2 * G + tid]);
             }
             if (lr[r] > 0.f) ms = fmaxf(ms, mr[r]);
         }
@@ -459,13 +564,14 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         }
         mst[tid] = ms;
         lst[tid] = ls;
+        snew[tid] = sn;
     }
     if (tid == 0) {
         int bb = sflag[0];
 #pragma unroll
         for (int r = 0; r < C; ++r)
             if (r != rank)
-                bb |= __float_as_int(inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + S::ROW_FLOATS + 2 * G]);
+                bb |= __float_as_int(inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + S::ROW_FLOATS + 3 * G]);
         sflag[1] = bb;
         if (sflag[0]) flag_status(p.status, sflag[0]);
     }
@@ -497,6 +603,28 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     if (!mbar_wait_bounded(&bar[1], 0)) {
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
+    }
+    if constexpr (APPEND) {
+        if (cl_new) {                                  // V codes of the new token, its value bins
+#pragma unroll 1
+            for (int mi = 0; mi < MC; ++mi) {
+                const int code = block_nearest<DSUB>(xnew + (MC + mi) * DSUB,
+                                                     cbv + static_cast<size_t>(mi) * K * DSUB, keys);
+                if (tid < G && snew[tid] != -INFINITY)
+                    wtot[(static_cast<size_t>(mi) * K + code) * G + tid] += exp2f(snew[tid] - mst[tid]);
+                if (tid == 0) newc[M + rank * MC + mi] = code;
+            }
+            if (tid == 0 && pg_new >= 0) {             // the new token's codes into its page slot
+                uint8_t *dst = p.code_pages_w +
+                               ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) {
+                    dst[rank * MC + mi] = static_cast<uint8_t>(newc[rank * MC + mi]);
+                    dst[M + rank * MC + mi] = static_cast<uint8_t>(newc[M + rank * MC + mi]);
+                }
+            }
+            __syncthreads();
+        }
     }
     float *ored = reinterpret_cast<float *>(cbk);      // [KS][MC*DSUB][G]
     {
@@ -583,10 +711,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     p.out[bh * kHeadDim + d] = nan ? __int_as_float(0x7fc00000) : (den > 0.f ? num / den : 0.f);
 }
 
-template <int M, int G, int C>
+template <int M, int G, int C, bool APPEND>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
-    auto kern = pq_decode_kernel<M, G, C>;
+    auto kern = pq_decode_kernel<M, G, C, APPEND>;
     if (plan.share > kMaxShare || plan.share % kPage) return cudaErrorInvalidValue;
     static size_t attr_bytes = 0;                  // opt-in dynamic shared memory set so far
     const size_t need = S::smem(plan.share);
@@ -600,35 +728,37 @@ cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) 
     cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
                        static_cast<unsigned>(p.batch));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = S::smem(plan.share);
+    cfg.dynamicSmemBytes = need;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.overlap ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int M, int G>
+template <int M, int G, bool APPEND>
 cudaError_t dispatch_c(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     switch (plan.cluster) {
-        case 1: return launch_one<M, G, 1>(p, plan, s);
-        case 2: return launch_one<M, G, 2>(p, plan, s);
-        case 4: return launch_one<M, G, 4>(p, plan, s);
+        case 1: return launch_one<M, G, 1, APPEND>(p, plan, s);
+        case 2: return launch_one<M, G, 2, APPEND>(p, plan, s);
+        case 4: return launch_one<M, G, 4, APPEND>(p, plan, s);
         default: return cudaErrorInvalidConfiguration;
     }
 }
 
-template <int M>
+template <int M, bool APPEND>
 cudaError_t dispatch_g(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s) {
     switch (G) {
-        case 1: return dispatch_c<M, 1>(p, plan, s);
-        case 2: return dispatch_c<M, 2>(p, plan, s);
-        case 4: return dispatch_c<M, 4>(p, plan, s);
-        case 8: return dispatch_c<M, 8>(p, plan, s);
+        case 1: return dispatch_c<M, 1, APPEND>(p, plan, s);
+        case 2: return dispatch_c<M, 2, APPEND>(p, plan, s);
+        case 4: return dispatch_c<M, 4, APPEND>(p, plan, s);
+        case 8: return dispatch_c<M, 8, APPEND>(p, plan, s);
         default: return cudaErrorInvalidConfiguration;
     }
 }
@@ -655,8 +785,18 @@ size_t pq_decode_smem_bytes(int M, int G, int cluster, int share) {
 
 cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
-    if (M == 4) e = dispatch_g<4>(p, G, plan, s);
-    else if (M == 8) e = dispatch_g<8>(p, G, plan, s);
+    if (M == 4) e = dispatch_g<4, false>(p, G, plan, s);
+    else if (M == 8) e = dispatch_g<8, false>(p, G, plan, s);
+    else return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    if (plan.num_splits > 1) return launch_combine(p, s);
+    return cudaSuccess;
+}
+
+cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
+    cudaError_t e;
+    if (M == 4) e = dispatch_g<4, true>(p, G, plan, s);
+    else if (M == 8) e = dispatch_g<8, true>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     if (plan.num_splits > 1) return launch_combine(p, s);

@@ -24,6 +24,9 @@ struct DecodeParams {
     int64_t num_pages, num_sets;
     int32_t max_seq_len, num_splits, split_len;  // split_len: tokens, multiple of P
     int32_t share;                               // tokens per cluster CTA, multiple of P
+    const void *kv_new;     // fp16 [B][Hkv][2][D]: the token appended by a fused decode step
+    uint8_t *code_pages_w;  // writable alias of code_pages (fused decode step)
+    int32_t overlap;        // launched as a programmatic dependent of the previous kernel
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -60,6 +63,10 @@ struct Plan {
 // Returns cudaSuccess or the launch error.
 cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &plan,
                              cudaStream_t s);
+// Fused decode step: append each request's new token (at position seq_len-1)
+// into the code cache, then the PQ decode attention that includes it.
+cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan,
+                                  cudaStream_t s);
 cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);

@@ -86,3 +86,17 @@ def fp16_decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int,
 def kv_tokens_heads(seq_lens, num_kv_heads: int) -> int:
     """The throughput unit: cached tokens times kv heads attended per call."""
     return int(_lens(seq_lens).sum()) * num_kv_heads
+
+
+def pq_step_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, num_subspaces: int,
+                  head_dim: int = 128, num_codewords: int = 256, page_size: int = 16) -> dict:
+    """Bytes of one fused decode step: the decode call's bytes plus the new
+    tokens' fp16 K/V read and their codes written."""
+    d = pq_decode_bytes(seq_lens, num_q_heads, num_kv_heads, num_subspaces, head_dim,
+                        num_codewords, page_size)
+    B = len(_lens(seq_lens))
+    kv_new = B * num_kv_heads * 2 * head_dim * FP16
+    new_codes = B * num_kv_heads * 2 * num_subspaces
+    d = dict(d, kv_new=kv_new, new_codes=new_codes)
+    d["total"] += kv_new + new_codes
+    return d

@@ -208,6 +208,40 @@ aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch,
                               int32_t *device_status, aq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * aq_decode_step -- one fused decode step: append each request's new token to
+ * the PQ code cache, then the decode attention that includes it, in a single
+ * launch that reads every codebook once (aq_encode_append followed by
+ * aq_decode_attention read them twice).
+ *
+ * The new token of request b is the one at position seq_lens[b] - 1: its key
+ * and value kv_new_f16[b] are encoded exactly as aq_encode_append does (AQPIM
+ * blog §3.1 step 3) against set req_set[b] and written to page
+ * block_table[b][(seq_lens[b]-1) / P], slot (seq_lens[b]-1) % P; the output is
+ * aq_decode_attention's over all seq_lens[b] tokens.
+ *
+ *   kv_new_f16    in   fp16 [B][Hkv][2][D]
+ *   code_pages    in/out (only the new tokens' slots are written)
+ *   flags         AQ_STEP_OVERLAP: the call may start reading the codebooks and
+ *                 req_set before the preceding kernel on `stream` has finished
+ *                 (programmatic dependent launch); everything else is read
+ *                 after it.  Set it only when that kernel does not write the
+ *                 codebooks or req_set.  0: plain stream order.
+ *   other arguments as aq_decode_attention.
+ * ------------------------------------------------------------------------- */
+#define AQ_STEP_OVERLAP 1
+aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch,
+                         int32_t num_q_heads, int32_t num_kv_heads,
+                         const float *q, const void *kv_new_f16,
+                         uint8_t *code_pages, int64_t num_pages,
+                         const void *codebooks_f16, int64_t num_sets,
+                         const int32_t *req_set, const int32_t *block_table,
+                         int32_t max_pages, const int32_t *seq_lens,
+                         int32_t max_seq_len, float scale, int32_t num_splits,
+                         int32_t flags, float *out, void *workspace,
+                         size_t workspace_bytes, int32_t *device_status,
+                         aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * aq_decode_attention_fp16 -- the uncompressed comparison point: the same
  * paged decode attention over an fp16 K/V cache (AQPIM blog §2.1 cache).
  * Only cfg->head_dim and cfg->page_size are used.

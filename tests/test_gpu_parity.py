@@ -247,3 +247,62 @@ def test_kmeans_step_matches_oracle(A, orc):
     torch.cuda.synchronize()
     assert np.array_equal(a_g.cpu().numpy(), a_o)
     assert np.array_equal(c_g.cpu().numpy(), c_o.astype(np.float32))
+
+
+# --------------------------------------------------------------------------
+# fused decode step (append the token at position seq_len-1, then attend)
+# --------------------------------------------------------------------------
+STEP_CASES = [
+    # (B, Hq, Hkv, M, lens)
+    (3, 4, 4, 4, [1, 17, 333]),                # new token alone; page boundary at 16
+    (2, 16, 2, 4, [1000, 257]),                # GQA group 8
+    (2, 4, 4, 8, [400, 1500]),                 # M = 8
+    (1, 2, 2, 4, [9001]),                      # long: splits
+    (4, 4, 4, 4, [16, 32, 48, 2048]),          # new token first in its page
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}M{c[3]}" for c in STEP_CASES])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("overlap", [False, True])
+def test_decode_step_matches_oracle(A, orc, case, splits, overlap):
+    B, Hq, Hkv, M, lens = case
+    p = W.paged_codes_problem(hash((B, Hq, M, tuple(lens), 7)) % 10000, B, Hq, Hkv, M, lens,
+                              num_sets=B + 1)
+    rng = np.random.default_rng(len(lens) * 31 + M)
+    kv_new = rng.standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+    # oracle: encode each new token into its slot, then attend
+    want_pages = p["code_pages"].copy()
+    slots = np.array([p["block_table"][b, (L - 1) // 16] * 16 + (L - 1) % 16
+                      for b, L in enumerate(lens)], np.int64)
+    orc.encode_append(kv_new, p["req_set"], slots, p["codebooks"], want_pages, 16)
+    pw = dict(p, code_pages=want_pages)
+    want = oracle_pq(orc, pw)
+    # GPU
+    pages = dev(p["code_pages"])
+    st = A.new_status()
+    out = A.decode_step(dev(p["q"]), dev(kv_new), pages, dev(p["codebooks"]), dev(p["req_set"]),
+                        dev(p["block_table"]), dev(p["seq_lens"]), int(max(lens)),
+                        1.0 / np.sqrt(128), num_splits=splits, overlap=overlap, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(pages.cpu().numpy(), want_pages)    # the new codes, nothing else
+    close(out.cpu().numpy(), want)
+
+
+def test_decode_step_equals_append_then_decode(A):
+    """The fused step gives the two-call sequence's codes and (to fp32
+    rounding) its output."""
+    p = W.paged_codes_problem(77, 4, 32, 32, 4, [2048] * 4)
+    kv_new = np.random.default_rng(5).standard_normal((4, 32, 2, 128)).astype(np.float16)
+    bt, lens = p["block_table"], p["seq_lens"]
+    slots = np.array([bt[b, (L - 1) // 16] * 16 + (L - 1) % 16 for b, L in enumerate(lens)], np.int64)
+    pa, pb = dev(p["code_pages"]), dev(p["code_pages"])
+    A.encode_append(dev(kv_new), dev(p["req_set"]), dev(slots), dev(p["codebooks"]), pa)
+    o1 = A.decode_attention(dev(p["q"]), pa, dev(p["codebooks"]), dev(p["req_set"]), dev(bt),
+                            dev(lens), 2048)
+    o2 = A.decode_step(dev(p["q"]), dev(kv_new), pb, dev(p["codebooks"]), dev(p["req_set"]), dev(bt),
+                       dev(lens), 2048)
+    torch.cuda.synchronize()
+    assert torch.equal(pa, pb)
+    assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-6)
