@@ -21,6 +21,7 @@ HBM copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded sample.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -68,6 +69,24 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_traffic(workload: str, mode: str):
+    """DRAM bytes (read + write) per launch of the decode kernel from one ncu
+    capture, recorded in profiles/traffic.json with the SHA-256 of the kernel
+    source it was taken on; None when there is no capture for this workload
+    and mode or the kernel source has changed since."""
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        e = json.load(f).get(f"{workload}/{mode}")
+    if not e:
+        return None
+    src = os.path.join(ROOT, "decode_attention_product_gb300", "csrc", "decode_pq.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return float(e["dram_bytes"]) if e.get("decode_pq_sha256") == digest else None
 
 
 def workload_desc(w) -> str:
@@ -382,11 +401,7 @@ def run_ours(args, w, rank, world, local_rank):
     dec_avg_ms = float(np.mean(dec_ms))
     peak, peak_kind = measured_peaks()
     achieved = byt["total"] / (dec_avg_ms / 1e3) / 1e9
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            traffic = json.load(f).get(w.name)
+    traffic = measured_traffic(w.name, "two_call" if args.two_call else "step")
     # e2e through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:

@@ -51,10 +51,6 @@ struct PqCfg {
     // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag
     static constexpr int STAT_FLOATS = 3 * G + 1;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
-    // V-product thread mapping
-    static constexpr int NJP = MC * DSUB / 2;               // owned j-pairs
-    static constexpr int KS = kThreads / NJP;               // k slices
-    static constexpr int KSL = K / KS;                      // k per slice
     // shared-memory layout (bytes)
     static constexpr int OFF_BAR = 0;                       // 5 mbarriers
     static constexpr int OFF_MISC = 64;                     // int flags
@@ -62,8 +58,9 @@ struct PqCfg {
     static constexpr int OFF_CBV = OFF_CBK + CB_BYTES;
     static constexpr int OFF_LUT = OFF_CBV + CB_BYTES;
     static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
+    static constexpr int BIN_WORDS = LUT_FLOATS;            // u32 value bins [M][K][G]
     // [C-1][INC_STRIDE] from the peers; sender src lands in slot (src - dst - 1) mod C
-    static constexpr int OFF_INC = OFF_BINS + LUT_FLOATS * 4;
+    static constexpr int OFF_INC = OFF_BINS + BIN_WORDS * 4;
     static constexpr int OFF_Q = OFF_INC + (C > 1 ? (C - 1) * INC_STRIDE * 4 : 0);
     static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_max, red_sum [kWarps][G]
     static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mst, lst, cfac [G], fac [C][G]
@@ -76,8 +73,8 @@ struct PqCfg {
     static constexpr int PPL = kMaxShare / P / 32;          // page ids per lane of warp 0
     static size_t smem(int share) { return OFF_CODES + static_cast<size_t>(share) * 2 * M; }
     static_assert(K == kThreads, "one thread per codeword in the table build");
-    static_assert(KS * NJP == kThreads && KS * KSL == K, "V-product mapping");
-    static_assert(KS * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
+    static_assert((MC * DSUB / 4) <= 32 && 32 % (MC * DSUB / 4) == 0, "V-product quads within a warp");
+    static_assert(kWarps * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
     static_assert(CB_BYTES % 16 == 0 && OFF_LUT % 16 == 0 && OFF_INC % 16 == 0 && OFF_Q % 16 == 0,
                   "alignment");
     static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "vector pushes");
@@ -151,21 +148,48 @@ struct Codes<8> {
     }
 };
 
-// Nearest codeword of x (DSUB floats in shared memory) among the 256 rows of a
-// codebook slice in shared memory: one thread per codeword, fp32 squared
-// distance with separately rounded subtract / multiply / add in increasing j,
-// lowest index on ties (the encode decision rule).  CTA-wide; returns the code
-// to every thread.
-template <int DSUB>
-__device__ __forceinline__ int block_nearest(const float *x, const __half *rows, unsigned long long *keys) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const __half *r = rows + static_cast<size_t>(tid) * DSUB;
+// One codeword row (DSUB halves, NCH 16-byte chunks) into registers, chunk c
+// of the row landing in u[(c - rot) mod NCH]: threads that read neighbouring
+// rows start at different chunks, so a quarter-warp's 16-byte reads fall in
+// distinct banks.
+template <int NCH>
+__device__ __forceinline__ void load_row_rotated(uint4 (&u)[NCH], const __half *row, int rot) {
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+#pragma unroll
+    for (int c0 = 0; c0 < NCH; ++c0) u[c0] = r4[(c0 + rot) % NCH];
+}
+
+// Squared distance between x (NCH*8 floats) and a row held by load_row_rotated:
+// fp32 with separately rounded subtract / multiply / add in increasing
+// dimension order (the encode decision rule).
+template <int NCH>
+__device__ __forceinline__ float row_distance(const uint4 (&u)[NCH], const float *x, int rot) {
     float d = 0.f;
 #pragma unroll
-    for (int j = 0; j < DSUB; ++j) {
-        const float e = __fsub_rn(x[j], __half2float(r[j]));
-        d = __fadd_rn(d, __fmul_rn(e, e));
+    for (int c = 0; c < NCH; ++c) {
+        const int c0 = (c - rot + NCH) % NCH;
+        uint4 w = u[0];
+#pragma unroll
+        for (int i = 1; i < NCH; ++i)
+            if (c0 == i) w = u[i];
+        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float2 f = h2_to_f2(w4[h]);
+            float e = __fsub_rn(x[c * 8 + 2 * h], f.x);
+            d = __fadd_rn(d, __fmul_rn(e, e));
+            e = __fsub_rn(x[c * 8 + 2 * h + 1], f.y);
+            d = __fadd_rn(d, __fmul_rn(e, e));
+        }
     }
+    return d;
+}
+
+// CTA-wide argmin over one distance per thread (thread = codeword), lowest
+// index on ties; returns the code to every thread.  Distances are >= 0, so
+// their bit patterns order like their values.
+__device__ __forceinline__ int block_argmin(float d, unsigned long long *keys) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d)) << 32) | static_cast<unsigned>(tid);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -181,11 +205,16 @@ __device__ __forceinline__ int block_nearest(const float *x, const __half *rows,
     return static_cast<int>(best & 0xffu);
 }
 
+// CTAs per SM the register budget is sized for: shared memory (LUT, bins and
+// pushed rows all scale with G) allows about 4 / 2 / 1 resident CTAs.
+template <int G>
+constexpr int kMinBlocks = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+
 // APPEND = the fused decode step: the token at position seq_len-1 of every
 // request is encoded here (each cluster CTA encodes the subspaces it owns) and
 // written to its page slot, and the attention includes it.
 template <int M, int G, int C, bool APPEND>
-__global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
     constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -240,14 +269,17 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                        static_cast<size_t>(rank) * S::CB_HALVES;
     const __half *gV = gK + cb_unit;
     uint64_t pol = 0;
-    if (warp == 0) {
-        __syncwarp();
-        if (lane == 0 && set_ok) {
+    if (warp == 0) __syncwarp();
+    auto issue_k_slice = [&]() {
+        if (warp == 0 && lane == 0 && set_ok) {
             pol = policy_evict_first();
             mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
             bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
         }
-    }
+    };
+    // overlapped with the preceding kernel, the slice goes first; otherwise it
+    // goes after the length and page-id loads, which it would delay
+    if (p.overlap) issue_k_slice();
     grid_dependency_wait();
 
     // ---- length and page ids ----------------------------------------------
@@ -261,6 +293,16 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             pgw[j] = idx < np_lim ? __ldg(bt + a0 / P + idx) : -1;
         }
     }
+    // the new token's owned K and V sub-vector elements, one per thread
+    __half xreg = __float2half(0.f);
+    if constexpr (APPEND) {
+        if (tid < 2 * MC * DSUB) {
+            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
+            xreg = __ldg(reinterpret_cast<const __half *>(p.kv_new) +
+                         ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D + rank * MC * DSUB + r);
+        }
+    }
+    if (!p.overlap) issue_k_slice();
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -293,20 +335,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     const bool own_new = cl_new && new_pos >= a0 && new_pos < e0;
     const int eS = own_new ? new_pos : e0;
     const int npg = eS > a0 ? (eS - a0 + P - 1) / P : 0;
-    int pg_new = -1;
-    if (cl_new) {
-        pg_new = __ldg(bt + new_pos / P);
-        if (pg_new < 0 || static_cast<int64_t>(pg_new) >= p.num_pages) {
-            if (tid == 0) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
-            pg_new = -1;
-        }
-        if (tid < 2 * MC * DSUB) {                     // owned sub-vectors of the new K and V
-            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
-            const __half *xg = reinterpret_cast<const __half *>(p.kv_new) +
-                               ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D + rank * MC * DSUB + r;
-            xnew[tid] = __half2float(__ldg(xg));
-        }
-    }
+    const int pg_new = cl_new ? __ldg(bt + new_pos / P) : -1;   // checked where it is used
 
     // ---- warp 0 issues the rest: code pages + query, then the V slice ------
     if (warp == 0) {
@@ -345,6 +374,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     for (int i = tid; i < S::LUT_FLOATS / 4; i += kThreads)
         reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < G) snew[tid] = -INFINITY;
+    if (cl_new && tid < 2 * MC * DSUB) xnew[tid] = __half2float(xreg);
     grid_launch_dependents();                          // every read of this CTA is issued
     if constexpr (C > 1) {
         cluster_arrive_relaxed();          // peers' mbarriers exist before anyone pushes
@@ -356,37 +386,36 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     // ---- lookup-table rows of the owned subspaces, pushed to the peers ------
     if (!mbar_wait_bounded(&bar[0], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     if (!mbar_wait_bounded(&bar[4], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    constexpr int NCH = DSUB / 8;                       // 16-byte chunks per codeword row
+    // per-thread chunk order: lanes of a quarter-warp read distinct banks
+    const int rot = (tid / (128 / (DSUB * 2))) % NCH;
     {
-        constexpr int NCH = DSUB / 8;                   // 16-byte chunks per codeword row
-        constexpr int ROWS128 = 128 / (DSUB * 2);       // rows per 128 bytes
-        const int rot = (tid / ROWS128) % NCH;          // bank-conflict-free chunk order
+        // thread tid = codeword k: its row is read once into registers and
+        // gives the G table entries and (fused step) its distance to the new
+        // key's sub-vector
 #pragma unroll
         for (int mi = 0; mi < MC; ++mi) {
             const int m = rank * MC + mi;
-            const __half *row = cbk + (static_cast<size_t>(mi) * K + tid) * DSUB;
+            uint4 u[NCH];
+            load_row_rotated<NCH>(u, cbk + (static_cast<size_t>(mi) * K + tid) * DSUB, rot);
             float acc[G];
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) acc[gg] = 0.f;
+            for (int gg = 0; gg < G; ++gg) {
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < NCH; ++c0) {
-                const int c = (c0 + rot) % NCH;
-                const uint4 u = *reinterpret_cast<const uint4 *>(row + c * 8);
-                const float2 f0 = h2_to_f2(u.x), f1 = h2_to_f2(u.y), f2 = h2_to_f2(u.z),
-                             f3 = h2_to_f2(u.w);
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
+                for (int c0 = 0; c0 < NCH; ++c0) {
+                    const int c = (c0 + rot) % NCH;
+                    const float2 f0 = h2_to_f2(u[c0].x), f1 = h2_to_f2(u[c0].y), f2 = h2_to_f2(u[c0].z),
+                                 f3 = h2_to_f2(u[c0].w);
                     const float4 *qv = reinterpret_cast<const float4 *>(qs + gg * D + m * DSUB + c * 8);
                     const float4 qa = qv[0], qb = qv[1];
-                    float a = acc[gg];
-                    a = fmaf(qa.x, f0.x, a); a = fmaf(qa.y, f0.y, a);
-                    a = fmaf(qa.z, f1.x, a); a = fmaf(qa.w, f1.y, a);
-                    a = fmaf(qb.x, f2.x, a); a = fmaf(qb.y, f2.y, a);
-                    a = fmaf(qb.z, f3.x, a); a = fmaf(qb.w, f3.y, a);
-                    acc[gg] = a;
+                    a0 = fmaf(qa.x, f0.x, a0); a1 = fmaf(qb.x, f2.x, a1);
+                    a0 = fmaf(qa.y, f0.y, a0); a1 = fmaf(qb.y, f2.y, a1);
+                    a0 = fmaf(qa.z, f1.x, a0); a1 = fmaf(qb.z, f3.x, a1);
+                    a0 = fmaf(qa.w, f1.y, a0); a1 = fmaf(qb.w, f3.y, a1);
                 }
+                acc[gg] = (a0 + a1) * p.scale_log2;
             }
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) acc[gg] *= p.scale_log2;
             float *dst = lut + (static_cast<size_t>(m) * K + tid) * G;
             store_vec<G>(dst, acc);
             if constexpr (C > 1) {
@@ -397,23 +426,18 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                     push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
                 }
             }
-        }
-    }
-    if constexpr (APPEND) {
-        if (cl_new) {                                  // K codes of the new token, owned subspaces
-#pragma unroll 1
-            for (int mi = 0; mi < MC; ++mi) {
-                const int m = rank * MC + mi;
-                const int code = block_nearest<DSUB>(xnew + mi * DSUB, cbk + static_cast<size_t>(mi) * K * DSUB,
-                                                     keys);
-                if (tid == 0) {
-                    newc[m] = code;
-                    if constexpr (C > 1) {
-                        const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
+            if constexpr (APPEND) {
+                if (cl_new) {                          // K code of the new token in subspace m
+                    const int code = block_argmin(row_distance<NCH>(u, xnew + mi * DSUB, rot), keys);
+                    if (tid == 0) {
+                        newc[m] = code;
+                        if constexpr (C > 1) {
+                            const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
 #pragma unroll
-                        for (int r = 1; r < C; ++r) {
-                            const uint32_t pr = (rank + r) % C;
-                            st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
+                            for (int r = 1; r < C; ++r) {
+                                const uint32_t pr = (rank + r) % C;
+                                st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
+                            }
                         }
                     }
                 }
@@ -426,17 +450,18 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     __syncthreads();
 
     // ---- code stream: scores, softmax statistics, value bins -------------------
-    // The share's codes are in shared memory, so the scores are recomputed
-    // (M table gathers each) in three passes: (1) per-head max, (2) per-head sum
-    // of exp2(s - max), (3) scatter of each weight into the 256-bin value
-    // accumulators as an unsigned fixed-point integer floor(p * 2^32 / l), so the
-    // bins cannot overflow, integer shared-memory atomics are exact and fast,
-    // and the result does not depend on the order of the atomics.  The fused
-    // step's new token enters (1) and (2) from its fresh codes; its value bin
-    // is added after the merge, once its V code is known.
+    // Three passes over the share: (1) scores by M table gathers and the per-head
+    // max, (2) per-head sum of exp2(s - max), (3) scatter of each weight into the
+    // 256-bin value accumulators as the unsigned fixed-point integer
+    // floor(p 2^32 (1 - 2^-16) / l): the bins cannot overflow (the margin covers
+    // the rounding of the float sum), integer shared-memory atomics are exact
+    // and fast, and the result does not depend on their order.  The first
+    // chunk's codes and scores stay in registers, so (2) and (3) read shared
+    // memory only for the atomics (a share is one chunk whenever G = 1).  The
+    // fused step's new token enters (1) and (2) from its fresh codes; its value
+    // bin is added after the merge, once its V code is known.
     unsigned *ibins = reinterpret_cast<unsigned *>(bins);
-    auto score = [&](int t, Codes<M> &cd) -> float {
-        cd.load(codes_s + (t - a0) * (2 * M));
+    auto gather = [&](const Codes<M> &cd) -> float {
         float acc = 0.f;
 #pragma unroll
         for (int m = 0; m < M; ++m) acc += lut[(m * K + cd.k(m)) * G + g];
@@ -451,6 +476,8 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             snew[tid] = s_new;
         }
     }
+    Codes<M> cc[TPT];
+    float sc[TPT];
     float mx = s_new;
 #pragma unroll 1
     for (int cb = a0; cb < eS; cb += S::CHUNK) {
@@ -459,7 +486,10 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             const int t = cb + i * S::TOK_PER_PASS + jslot;
             if (t < eS) {
                 Codes<M> cd;
-                mx = fmaxf(mx, score(t, cd));
+                cd.load(codes_s + (t - a0) * (2 * M));
+                const float s = gather(cd);
+                if (cb == a0) { cc[i] = cd; sc[i] = s; }
+                mx = fmaxf(mx, s);
             }
         }
     }
@@ -478,8 +508,15 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             for (int i = 0; i < TPT; ++i) {
                 const int t = cb + i * S::TOK_PER_PASS + jslot;
                 if (t < eS) {
-                    Codes<M> cd;
-                    l_run += exp2f(score(t, cd) - mx);
+                    float s;
+                    if (cb == a0) {
+                        s = sc[i];
+                    } else {
+                        Codes<M> cd;
+                        cd.load(codes_s + (t - a0) * (2 * M));
+                        s = gather(cd);
+                    }
+                    l_run += exp2f(s - mx);
                 }
             }
         }
@@ -491,7 +528,6 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) lsum += red_sum[w * G + g];
-    // 2^32 (1 - 2^-16) / l: the margin covers the rounding of the float sum
     const float qscale = lsum > 0.f ? 4294901760.0f / lsum : 0.f;
     if (mx != -INFINITY) {
 #pragma unroll 1
@@ -501,7 +537,15 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
                 const int t = cb + i * S::TOK_PER_PASS + jslot;
                 if (t < eS) {
                     Codes<M> cd;
-                    const unsigned q = __float2uint_rz(exp2f(score(t, cd) - mx) * qscale);
+                    float s;
+                    if (cb == a0) {
+                        cd = cc[i];
+                        s = sc[i];
+                    } else {
+                        cd.load(codes_s + (t - a0) * (2 * M));
+                        s = gather(cd);
+                    }
+                    const unsigned q = __float2uint_rz(exp2f(s - mx) * qscale);
 #pragma unroll
                     for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cd.vv(m)) * G + g], q);
                 }
@@ -511,14 +555,11 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     if (tid < G) {
         mst[tid] = mx;                                 // this CTA's statistics for now
         lst[tid] = lsum;
-        cfac[tid] = qscale > 0.f ? 1.0f / qscale : 0.f;
+        cfac[tid] = qscale > 0.f ? 1.0f / qscale : 0.f;  // integer bin -> weight
     }
     __syncthreads();
-    // integer bins -> float weights in the same storage (relative to this CTA's max)
-    for (int i = tid; i < S::LUT_FLOATS; i += kThreads) bins[i] = static_cast<float>(ibins[i]) * cfac[i % G];
-    __syncthreads();
 
-    // ---- push bins rows and statistics to the peers that own them -----------
+    // ---- push bins rows (as weights) and statistics to the peers that own them
     if constexpr (C > 1) {
         const uint32_t lb = smem_u32(&bar[3]);
 #pragma unroll 1
@@ -527,8 +568,16 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             const int slot = (C - r - 1) % C;          // (rank - pr - 1) mod C
             const uint32_t rslot = mapa_u32(smem_u32(inc + slot * S::INC_STRIDE), pr);
             const uint32_t rbar = mapa_u32(lb, pr);
-            const float4 *src = reinterpret_cast<const float4 *>(bins + pr * S::ROW_FLOATS);
-            for (int i = tid; i < S::ROW_FLOATS / 4; i += kThreads) st_async_v4(rslot + 16 * i, src[i], rbar);
+            const uint4 *src = reinterpret_cast<const uint4 *>(ibins + pr * S::ROW_FLOATS);
+            for (int i = tid; i < S::ROW_FLOATS / 4; i += kThreads) {
+                const uint4 v = src[i];
+                const int g0 = (4 * i) % G;
+                st_async_v4(rslot + 16 * i,
+                            make_float4(static_cast<float>(v.x) * cfac[g0], static_cast<float>(v.y) * cfac[(g0 + 1) % G],
+                                        static_cast<float>(v.z) * cfac[(g0 + 2) % G],
+                                        static_cast<float>(v.w) * cfac[(g0 + 3) % G]),
+                            rbar);
+            }
             if (tid < G) {
                 st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mst[tid], rbar);
                 st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lst[tid], rbar);
@@ -562,6 +611,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             fac[r * G + tid] = f;
             ls += f * lr[r];
         }
+        fac[rank * G + tid] *= cfac[tid];              // own rows are still integers
         mst[tid] = ms;
         lst[tid] = ls;
         snew[tid] = sn;
@@ -580,15 +630,18 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
     float *wtot = lut;                                 // [MC][K][G]; the LUT is no longer read
     {
         constexpr int N4 = S::ROW_FLOATS / 4;
-        const float4 *own = reinterpret_cast<const float4 *>(bins + rank * S::ROW_FLOATS);
+        const uint4 *own = reinterpret_cast<const uint4 *>(ibins + rank * S::ROW_FLOATS);
         for (int i = tid; i < N4; i += kThreads) {
             const int g0 = (4 * i) % G;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint4 o = own[i];
+            float4 acc = make_float4(fac[rank * G + g0] * static_cast<float>(o.x),
+                                     fac[rank * G + (g0 + 1) % G] * static_cast<float>(o.y),
+                                     fac[rank * G + (g0 + 2) % G] * static_cast<float>(o.z),
+                                     fac[rank * G + (g0 + 3) % G] * static_cast<float>(o.w));
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                const float4 v = (r == rank) ? own[i]
-                                             : reinterpret_cast<const float4 *>(
-                                                   inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE)[i];
+                if (r == rank) continue;
+                const float4 v = reinterpret_cast<const float4 *>(inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE)[i];
                 acc.x += fac[r * G + g0] * v.x;
                 acc.y += fac[r * G + (g0 + 1) % G] * v.y;
                 acc.z += fac[r * G + (g0 + 2) % G] * v.z;
@@ -608,13 +661,17 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         if (cl_new) {                                  // V codes of the new token, its value bins
 #pragma unroll 1
             for (int mi = 0; mi < MC; ++mi) {
-                const int code = block_nearest<DSUB>(xnew + (MC + mi) * DSUB,
-                                                     cbv + static_cast<size_t>(mi) * K * DSUB, keys);
+                uint4 u[NCH];
+                load_row_rotated<NCH>(u, cbv + (static_cast<size_t>(mi) * K + tid) * DSUB, rot);
+                const int code = block_argmin(row_distance<NCH>(u, xnew + (MC + mi) * DSUB, rot), keys);
                 if (tid < G && snew[tid] != -INFINITY)
                     wtot[(static_cast<size_t>(mi) * K + code) * G + tid] += exp2f(snew[tid] - mst[tid]);
                 if (tid == 0) newc[M + rank * MC + mi] = code;
             }
-            if (tid == 0 && pg_new >= 0) {             // the new token's codes into its page slot
+            const bool pg_ok = pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages;
+            if (tid == 0 && !pg_ok) flag_status(p.status, AQ_DEV_BAD_PAGE);
+            if (!pg_ok) bad_all |= AQ_DEV_BAD_PAGE;
+            if (tid == 0 && pg_ok) {                   // the new token's codes into its page slot
                 uint8_t *dst = p.code_pages_w +
                                ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
 #pragma unroll
@@ -626,29 +683,47 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
             __syncthreads();
         }
     }
-    float *ored = reinterpret_cast<float *>(cbk);      // [KS][MC*DSUB][G]
+    // thread = (k slice, 4-dim quad of the owned dims): 8-byte codebook loads,
+    // the slices of a warp reduced by shuffles, the warps through shared memory
+    float *ored = reinterpret_cast<float *>(cbk);      // [kWarps][MC*DSUB][G]
     {
-        const int jp = tid % S::NJP, ks = tid / S::NJP;
-        const int mi = jp / (DSUB / 2), j2 = (jp % (DSUB / 2)) * 2;
-        float acc0[G], acc1[G];
+        constexpr int NQ = MC * DSUB / 4, KSQ = kThreads / NQ, KSLQ = K / KSQ;
+        const int qd = tid % NQ, ks = tid / NQ;
+        const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
+        float acc[G][4];
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) { acc0[gg] = 0.f; acc1[gg] = 0.f; }
+        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = acc[gg][2] = acc[gg][3] = 0.f;
 #pragma unroll 4
-        for (int i = 0; i < S::KSL; ++i) {
-            const int k = ks * S::KSL + ((i + ks) % S::KSL);
-            const float2 cv = h2_to_f2(
-                *reinterpret_cast<const uint32_t *>(cbv + (static_cast<size_t>(mi) * K + k) * DSUB + j2));
+        for (int i = 0; i < KSLQ; ++i) {
+            const int k = ks * KSLQ + ((i + ks) % KSLQ);
+            const uint2 cv2 = *reinterpret_cast<const uint2 *>(cbv + (static_cast<size_t>(mi) * K + k) * DSUB + j4);
+            const float2 c01 = h2_to_f2(cv2.x), c23 = h2_to_f2(cv2.y);
             float w[G];
             load_vec<G>(w, wtot + (static_cast<size_t>(mi) * K + k) * G);
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
-                acc0[gg] = fmaf(w[gg], cv.x, acc0[gg]);
-                acc1[gg] = fmaf(w[gg], cv.y, acc1[gg]);
+                acc[gg][0] = fmaf(w[gg], c01.x, acc[gg][0]);
+                acc[gg][1] = fmaf(w[gg], c01.y, acc[gg][1]);
+                acc[gg][2] = fmaf(w[gg], c23.x, acc[gg][2]);
+                acc[gg][3] = fmaf(w[gg], c23.y, acc[gg][3]);
             }
         }
-        float *dst = ored + (static_cast<size_t>(ks) * MC * DSUB + mi * DSUB + j2) * G;
-        store_vec<G>(dst, acc0);
-        store_vec<G>(dst + G, acc1);
+#pragma unroll
+        for (int off = NQ; off < 32; off <<= 1) {
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[gg][e] += __shfl_xor_sync(0xffffffffu, acc[gg][e], off);
+        }
+        if (lane < NQ) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v[G];
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) v[gg] = acc[gg][e];
+                store_vec<G>(ored + (static_cast<size_t>(warp) * MC * DSUB + mi * DSUB + j4 + e) * G, v);
+            }
+        }
     }
     __syncthreads();
     {
@@ -656,7 +731,7 @@ __global__ void __launch_bounds__(kThreads) pq_decode_kernel(const __grid_consta
         for (int i = tid; i < NOUT; i += kThreads) {
             float o = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < S::KS; ++ks) o += ored[static_cast<size_t>(ks) * NOUT + i];
+            for (int w = 0; w < kWarps; ++w) o += ored[static_cast<size_t>(w) * NOUT + i];
             const int gg = i % G, dl = i / G;                 // dl in [0, MC*DSUB)
             const int d = rank * MC * DSUB + dl;
             const size_t bh = static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G + gg;

@@ -102,12 +102,13 @@ def test_decode_plan_variants_agree(A, orc):
 
 
 def test_decode_repeated_calls_agree(A):
-    """The value bins accumulate by shared-memory float atomics, whose order is
-    not fixed: repeated calls agree to fp32 rounding, not bit for bit."""
+    """The value bins accumulate as unsigned fixed-point integers, so the order
+    of the shared-memory atomics cannot change them, and every other reduction
+    has a fixed order: repeated calls agree bit for bit."""
     p = W.paged_codes_problem(6, 2, 8, 8, 4, [900, 1200])
     a, _ = run_pq(A, p)
     b, _ = run_pq(A, p)
-    assert np.allclose(a, b, rtol=1e-5, atol=1e-6)
+    assert np.array_equal(a, b)
 
 
 def test_decode_data_errors_flag_and_nan(A):
@@ -306,3 +307,25 @@ def test_decode_step_equals_append_then_decode(A):
     torch.cuda.synchronize()
     assert torch.equal(pa, pb)
     assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-6)
+
+
+def test_decode_step_bad_new_page_flagged(A):
+    """The new token's page id outside the pool: bad-page status, NaN output for
+    that request, no code written anywhere for it, the other request intact."""
+    p = W.paged_codes_problem(9, 2, 4, 4, 4, [40, 40], num_sets=2)
+    p["block_table"][0, 39 // 16] = p["num_pages"] + 3
+    kv_new = np.random.default_rng(9).standard_normal((2, 4, 2, 128)).astype(np.float16)
+    before = p["code_pages"].copy()
+    pages = dev(p["code_pages"])
+    st = A.new_status()
+    out = A.decode_step(dev(p["q"]), dev(kv_new), pages, dev(p["codebooks"]), dev(p["req_set"]),
+                        dev(p["block_table"]), dev(p["seq_lens"]), 40, 1.0 / np.sqrt(128), status=st)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert int(st.item()) & 1
+    assert np.all(np.isnan(got[0])) and np.all(np.isfinite(got[1]))
+    after = pages.cpu().numpy()
+    for j in range(3):
+        pg = p["block_table"][0, j]
+        if 0 <= pg < p["num_pages"]:
+            assert np.array_equal(after[pg], before[pg])
