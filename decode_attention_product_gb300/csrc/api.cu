@@ -67,17 +67,15 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
     const int max_pages_needed = (max_seq_len + P - 1) / P;
     int C = 1;
-    int share_max = kMaxShare;
+    int share_max = 0;
     if (!fp16) {
         const int M = cfg->num_subspaces;
         C = 0;
         for (int c = 4; c >= 1; c /= 2)
-            if (c <= M && pq_decode_smem_bytes(M, G, c, P) <= smem_cap) { C = c; break; }
+            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
         if (C == 0) return AQ_ERR_UNSUPPORTED;
-        // the largest token share whose codes still fit next to the rest
-        const size_t room = smem_cap - pq_decode_smem_bytes(M, G, C, 0);
-        const int fit = static_cast<int>(room / (2 * M)) / P * P;
-        share_max = fit < kMaxShare ? fit : kMaxShare;
+        share_max = pq_decode_max_share(M, G) / P * P;
+        if (share_max <= 0) return AQ_ERR_UNSUPPORTED;
     }
     int S = req;
     if (S <= 0) {
@@ -93,7 +91,7 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
         }
     }
     if (!fp16) {
-        // each CTA of a cluster stages at most kMaxShare tokens of codes
+        // each CTA of a cluster holds at most share_max tokens
         const int64_t need = (static_cast<int64_t>(max_seq_len) + static_cast<int64_t>(C) * share_max - 1) /
                              (static_cast<int64_t>(C) * share_max);
         if (S < need) S = static_cast<int>(need);
@@ -112,7 +110,7 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     pl->split_len = split_len;
     pl->share = share;
     pl->workspace = S > 1 ? static_cast<size_t>(batch) * Hq * S * (kHeadDim + 2) * sizeof(float) : 0;
-    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C, share);
+    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C);
     return AQ_OK;
 }
 

@@ -20,6 +20,8 @@ constexpr int kCodewords = 256;
 constexpr int kPage = 16;
 // 200 ms: far above any legitimate copy, far below a watchdog.
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+// Longest suspension one mbarrier try-wait asks for (1 ms).
+constexpr uint32_t kSuspendHintNs = 1000000u;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
@@ -54,14 +56,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// Test phase `parity` of `bar`; a thread whose phase is still open is
+// suspended (up to kSuspendHintNs) until it completes instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -97,6 +101,23 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gm
         : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (cp.async.cg): the destination is
+// any 16-byte aligned shared address, so a copy can lay rows out in its own
+// (swizzled) order.  Completion is tracked per thread.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src_gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src_gmem) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed; the arrival is one of the counts the barrier was initialised with.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -120,6 +141,22 @@ __device__ __forceinline__ uint2 ldg_stream_v2(const void *p) {
     return v;
 }
 
+// 8- / 16-byte loads through the coherent path, not kept in L1 (data that a
+// preceding kernel may have written).
+__device__ __forceinline__ uint2 ld_global_na_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_global_na_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void flag_status(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -127,6 +164,52 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t bits) {
 __device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
     __half2 h = *reinterpret_cast<__half2 *>(&u);
     return __half22float2(h);
+}
+
+// ---- packed fp32 pairs (sm_100-family f32x2 arithmetic) ---------------------
+// Each lane of a pair is rounded exactly as the scalar operation would be.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2_unpack(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Two fp16 values (one 32-bit word) as a packed fp32 pair.
+__device__ __forceinline__ unsigned long long h2_to_f2p(uint32_t u) {
+    const float2 f = h2_to_f2(u);
+    return f2_pack(f.x, f.y);
+}
+
+// Warp-wide maximum of a float (all 32 lanes take part).
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 // ---- thread-block cluster helpers ------------------------------------------

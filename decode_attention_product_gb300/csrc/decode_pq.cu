@@ -4,30 +4,35 @@
 // CTA `rank` owns subspaces [rank*M/C, (rank+1)*M/C) of both the key and the
 // value codebook and 1/C of the split's tokens:
 //
-//  1. bulk-copy its key and value codebook slices (64/C KiB each) to shared
-//     memory (cp.async.bulk + mbarrier), load the G query vectors of the GQA
-//     group;
+//  1. copy its key and value codebook slices (64/C KiB each) into shared
+//     memory with cp.async, each codeword row's 16-byte chunks at XOR-swizzled
+//     positions so that rows read in their natural order are bank-conflict
+//     free; load its tokens' uint8 codes straight into registers (page ids
+//     from the block table, PAM article §2.2.2) and the G query vectors of
+//     the GQA group;
 //  2. LUT[m][k][g] = <q_g[m], C^K_m[k]> * scale * log2(e) for its own m
 //     (AQPIM blog §4.1: per-subspace partial dot products with the codebook;
 //     §5.1 item 3: index -> codebook -> sub-dot -> accumulate, nothing
 //     intermediate written to global memory); the rows are exchanged through
 //     distributed shared memory so every CTA holds the full M x 256 x G table;
-//  3. stream its tokens' uint8 codes through the block table (PAM article
-//     §2.2.2), score s = sum_m LUT[m][kcode_m] by table gathers, keep a running
-//     max / sum per query head (online softmax, PAM article §2.2.3 item 1) and
-//     scatter exp2(s - max) into 256-bin value accumulators W[m][vcode_m][g];
+//  3. score its tokens, s = sum_m LUT[m][kcode_m] by table gathers, reduce the
+//     per-head (max, sum) of the block (online softmax statistics, PAM article
+//     §2.2.3 item 1) and scatter exp2(s - max) into 256-bin value
+//     accumulators W[m][vcode_m][g];
 //  4. merge the C CTAs' (max, sum, bins) over distributed shared memory (the
 //     hierarchical reduction of PAM article §2.2.3 item 3, inside one cluster)
 //     and apply the value codebook slice it owns: o[m*Dsub+j] = sum_k W[m][k]
 //     * C^V_m[k][j];
 //  5. normalise and store, or store (max, sum, o) partials for the split-KV
 //     combine kernel.
-#include <cooperative_groups.h>
-
+//
+// The fused decode step (APPEND) also encodes the token at position
+// seq_len-1 of every request in step 2 (each CTA its owned subspaces, from the
+// codebook rows it already holds in registers), scores it from its fresh
+// codes, adds it to the value bins after the merge and writes its codes to
+// its page slot.
 #include "common.cuh"
 #include "internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace aq {
 
@@ -40,17 +45,22 @@ template <int M, int G, int C>
 struct PqCfg {
     static constexpr int D = kHeadDim, K = kCodewords, P = kPage;
     static constexpr int DSUB = D / M;
+    static constexpr int NCH = DSUB / 8;                    // 16-byte chunks per codeword row
     static constexpr int MC = M / C;                        // subspaces owned per CTA
     static constexpr int CB_HALVES = MC * K * DSUB;         // owned part of one codebook
     static constexpr int CB_BYTES = CB_HALVES * 2;
+    static constexpr int CB_CHUNKS = CB_BYTES / 16;
     static constexpr int LUT_FLOATS = M * K * G;
+    static constexpr int BIN_WORDS = LUT_FLOATS;            // u32 value bins [M][K][G]
     static constexpr int ROW_FLOATS = MC * K * G;           // one rank's rows of LUT / bins
-    static constexpr int TPT = 8;                           // tokens per thread per chunk
     static constexpr int TOK_PER_PASS = kThreads / G;
-    static constexpr int CHUNK = TOK_PER_PASS * TPT;
+    // tokens per thread, held in registers (codes and scores)
+    static constexpr int TPT = (M == 8 && G <= 2) ? 4 : 8;
+    static constexpr int MAX_SHARE = TPT * TOK_PER_PASS;    // tokens per CTA
     // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag
     static constexpr int STAT_FLOATS = 3 * G + 1;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
+    static constexpr int NKEY = 2 * MC;                     // new-token argmins: K then V, owned subspaces
     // shared-memory layout (bytes)
     static constexpr int OFF_BAR = 0;                       // 5 mbarriers
     static constexpr int OFF_MISC = 64;                     // int flags
@@ -58,27 +68,58 @@ struct PqCfg {
     static constexpr int OFF_CBV = OFF_CBK + CB_BYTES;
     static constexpr int OFF_LUT = OFF_CBV + CB_BYTES;
     static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
-    static constexpr int BIN_WORDS = LUT_FLOATS;            // u32 value bins [M][K][G]
     // [C-1][INC_STRIDE] from the peers; sender src lands in slot (src - dst - 1) mod C
     static constexpr int OFF_INC = OFF_BINS + BIN_WORDS * 4;
     static constexpr int OFF_Q = OFF_INC + (C > 1 ? (C - 1) * INC_STRIDE * 4 : 0);
-    static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_max, red_sum [kWarps][G]
-    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mst, lst, cfac [G], fac [C][G]
-    // fused step: the new token's owned sub-vectors [2][MC][DSUB] f32, its codes
-    // [2][M] int, its score [G], argmin keys [kWarps] u64
-    static constexpr int OFF_NEW = (OFF_STAT + (3 + C) * G * 4 + 15) / 16 * 16;
-    static constexpr int NEW_BYTES = 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 8 * kWarps + 8;
-    static constexpr int OFF_CODES = (OFF_NEW + NEW_BYTES + 15) / 16 * 16;  // [share][2M] uint8
-    static constexpr int PAGE_BYTES = P * 2 * M;            // one page's codes for one kv head
-    static constexpr int PPL = kMaxShare / P / 32;          // page ids per lane of warp 0
-    static size_t smem(int share) { return OFF_CODES + static_cast<size_t>(share) * 2 * M; }
+    static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_m, red_l [kWarps][G]
+    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // merged mst, lst [G]
+    // new token: owned sub-vectors [2][MC][DSUB] f32, codes [2][M] int, score [G]
+    static constexpr int OFF_NEW = (OFF_STAT + 2 * G * 4 + 15) / 16 * 16;
+    static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8;
+    static constexpr int END = OFF_KEYS + NKEY * kWarps * 8;
+    static size_t smem() { return END; }
     static_assert(K == kThreads, "one thread per codeword in the table build");
+    static_assert(CB_CHUNKS % kThreads == 0, "whole slice chunks per thread");
+    static_assert((NCH & (NCH - 1)) == 0 && NCH <= 8, "XOR swizzle over a power-of-two chunk count");
     static_assert((MC * DSUB / 4) <= 32 && 32 % (MC * DSUB / 4) == 0, "V-product quads within a warp");
     static_assert(kWarps * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
     static_assert(CB_BYTES % 16 == 0 && OFF_LUT % 16 == 0 && OFF_INC % 16 == 0 && OFF_Q % 16 == 0,
                   "alignment");
     static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "vector pushes");
 };
+
+// CTAs per SM the register budget is sized for: shared memory (LUT, bins and
+// pushed rows all scale with G) allows about 4 / 2 / 1 resident CTAs.
+template <int G>
+constexpr int kMinBlocks = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+
+// Position of 16-byte chunk c of codeword row k in shared memory: c XOR a
+// function of k, so that the 8 rows a quarter-warp reads at once (two or four
+// rows per 128-byte line) cover all eight 16-byte bank groups.
+template <int DSUB>
+__device__ __forceinline__ int chunk_pos(int k, int c) {
+    constexpr int NCH = DSUB / 8, ROWS128 = 128 / (DSUB * 2);
+    return c ^ ((k / ROWS128) & (NCH - 1));
+}
+
+// Copy an owned codebook slice [rows][DSUB] fp16 to shared memory in the
+// swizzled layout: thread tid takes chunks tid, tid + kThreads, ... (coalesced
+// global reads) and arrives on `bar` once its copies have landed.
+template <int DSUB, int CHUNKS>
+__device__ __forceinline__ void copy_slice(__half *dst, const __half *src, uint64_t *bar) {
+    constexpr int NCH = DSUB / 8, ROWS128 = 128 / (DSUB * 2);
+    // chunk tid + i*kThreads lies kThreads/NCH rows below chunk tid, a multiple
+    // of the swizzle period, so it keeps chunk tid's position within its row
+    static_assert((kThreads / NCH) % (ROWS128 * NCH) == 0, "swizzle period");
+    const int t = static_cast<int>(threadIdx.x);
+    const int r0 = t / NCH, c = t % NCH;
+    const uint32_t d0 = smem_u32(dst) + static_cast<uint32_t>(r0 * NCH + chunk_pos<DSUB>(r0, c)) * 16u;
+    const __half *s0 = src + static_cast<size_t>(t) * 8;
+#pragma unroll
+    for (int i = 0; i < CHUNKS / kThreads; ++i)
+        cp_async_16(d0 + static_cast<uint32_t>(i * kThreads * 16), s0 + static_cast<size_t>(i) * kThreads * 8);
+    cp_async_mbar_arrive(bar);
+}
 
 template <int N>
 __device__ __forceinline__ void store_vec(float *dst, const float (&v)[N]) {
@@ -132,14 +173,14 @@ struct Codes;
 template <>
 struct Codes<4> {
     uint2 v;
-    __device__ __forceinline__ void load(const uint8_t *p) { v = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v2(p); }
     __device__ __forceinline__ int k(int m) const { return (v.x >> (8 * m)) & 0xff; }
     __device__ __forceinline__ int vv(int m) const { return (v.y >> (8 * m)) & 0xff; }
 };
 template <>
 struct Codes<8> {
     uint4 v;
-    __device__ __forceinline__ void load(const uint8_t *p) { v = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v4(p); }
     __device__ __forceinline__ int k(int m) const {
         return ((m < 4 ? v.x : v.y) >> (8 * (m & 3))) & 0xff;
     }
@@ -148,77 +189,92 @@ struct Codes<8> {
     }
 };
 
-// One codeword row (DSUB halves, NCH 16-byte chunks) into registers, chunk c
-// of the row landing in u[(c - rot) mod NCH]: threads that read neighbouring
-// rows start at different chunks, so a quarter-warp's 16-byte reads fall in
-// distinct banks.
-template <int NCH>
-__device__ __forceinline__ void load_row_rotated(uint4 (&u)[NCH], const __half *row, int rot) {
-    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+// One encode step on 8 consecutive dimensions: fp32 squared distance with
+// separately rounded subtract / multiply / add, the adds in increasing
+// dimension order (the encode decision rule).  Subtracts and squares run as
+// packed pairs (each lane rounded as the scalar operation), the running sum
+// stays scalar.  x: the new token's sub-vector chunk; f: the codeword chunk as
+// four packed pairs.
+__device__ __forceinline__ float sqdist8(float d, const float *x, const unsigned long long (&f)[4]) {
+    const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(x);
+    const ulonglong2 xb = *reinterpret_cast<const ulonglong2 *>(x + 4);
+    const unsigned long long xv[4] = {xa.x, xa.y, xb.x, xb.y};
 #pragma unroll
-    for (int c0 = 0; c0 < NCH; ++c0) u[c0] = r4[(c0 + rot) % NCH];
-}
-
-// Squared distance between x (NCH*8 floats) and a row held by load_row_rotated:
-// fp32 with separately rounded subtract / multiply / add in increasing
-// dimension order (the encode decision rule).
-template <int NCH>
-__device__ __forceinline__ float row_distance(const uint4 (&u)[NCH], const float *x, int rot) {
-    float d = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int c0 = (c - rot + NCH) % NCH;
-        uint4 w = u[0];
-#pragma unroll
-        for (int i = 1; i < NCH; ++i)
-            if (c0 == i) w = u[i];
-        const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const float2 f = h2_to_f2(w4[h]);
-            float e = __fsub_rn(x[c * 8 + 2 * h], f.x);
-            d = __fadd_rn(d, __fmul_rn(e, e));
-            e = __fsub_rn(x[c * 8 + 2 * h + 1], f.y);
-            d = __fadd_rn(d, __fmul_rn(e, e));
-        }
+    for (int e = 0; e < 4; ++e) {
+        const unsigned long long t = f2_sub(xv[e], f[e]);
+        const float2 sq = f2_unpack(f2_mul(t, t));
+        d = __fadd_rn(d, sq.x);
+        d = __fadd_rn(d, sq.y);
     }
     return d;
 }
 
-// CTA-wide argmin over one distance per thread (thread = codeword), lowest
-// index on ties; returns the code to every thread.  Distances are >= 0, so
-// their bit patterns order like their values.
-__device__ __forceinline__ int block_argmin(float d, unsigned long long *keys) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d)) << 32) | static_cast<unsigned>(tid);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-        key = o < key ? o : key;
-    }
-    __syncthreads();                                   // keys[] free from a previous use
-    if (lane == 0) keys[warp] = key;
-    __syncthreads();
-    unsigned long long best = keys[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) best = keys[w] < best ? keys[w] : best;
-    return static_cast<int>(best & 0xffu);
+__device__ __forceinline__ void to_f2p4(const uint4 &u, unsigned long long (&f)[4]) {
+    f[0] = h2_to_f2p(u.x);
+    f[1] = h2_to_f2p(u.y);
+    f[2] = h2_to_f2p(u.z);
+    f[3] = h2_to_f2p(u.w);
 }
 
-// CTAs per SM the register budget is sized for: shared memory (LUT, bins and
-// pushed rows all scale with G) allows about 4 / 2 / 1 resident CTAs.
-template <int G>
-constexpr int kMinBlocks = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+// CTA-wide argmins of NK distances per thread (thread = codeword), lowest
+// index on ties; thread n < NK receives the n-th code.  Distances are >= 0, so
+// their bit patterns order like their values.  Contains one __syncthreads.
+template <int NK>
+__device__ __forceinline__ int block_argmin_n(const float (&d)[NK], unsigned long long *keys) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int n = 0; n < NK; ++n) {
+        unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d[n])) << 32) |
+                                 static_cast<unsigned>(tid);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+            key = o < key ? o : key;
+        }
+        if (lane == 0) keys[n * kWarps + warp] = key;
+    }
+    __syncthreads();
+    int code = 0;
+    if (tid < NK) {
+        unsigned long long best = keys[tid * kWarps];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) best = keys[tid * kWarps + w] < best ? keys[tid * kWarps + w] : best;
+        code = static_cast<int>(best & 0xffu);
+    }
+    return code;
+}
 
-// APPEND = the fused decode step: the token at position seq_len-1 of every
-// request is encoded here (each cluster CTA encodes the subspaces it owns) and
-// written to its page slot, and the attention includes it.
+// Same, every thread receiving all NK codes (no barrier needed after it).
+template <int NK>
+__device__ __forceinline__ void block_argmin_all(const float (&d)[NK], unsigned long long *keys, int (&code)[NK]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int n = 0; n < NK; ++n) {
+        unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d[n])) << 32) |
+                                 static_cast<unsigned>(tid);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+            key = o < key ? o : key;
+        }
+        if (lane == 0) keys[n * kWarps + warp] = key;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NK; ++n) {
+        unsigned long long best = keys[n * kWarps];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) best = keys[n * kWarps + w] < best ? keys[n * kWarps + w] : best;
+        code[n] = static_cast<int>(best & 0xffu);
+    }
+}
+
 template <int M, int G, int C, bool APPEND>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
-    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT;
+    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT, NCH = S::NCH;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in, codes+q
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in, query
     int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);           // [0] local bad, [1] all
     __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
     __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
@@ -226,18 +282,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     float *bins = reinterpret_cast<float *>(smem + S::OFF_BINS);
     float *inc = reinterpret_cast<float *>(smem + S::OFF_INC);
     float *qs = reinterpret_cast<float *>(smem + S::OFF_Q);
-    float *red_max = reinterpret_cast<float *>(smem + S::OFF_RED);
-    float *red_sum = red_max + kWarps * G;
-    float *mst = reinterpret_cast<float *>(smem + S::OFF_STAT);
-    float *lst = mst + G;
-    float *cfac = lst + G;
-    float *fac = cfac + G;                                              // [C][G]
+    float *red_m = reinterpret_cast<float *>(smem + S::OFF_RED);
+    float *red_l = red_m + kWarps * G;
+    float *mst = reinterpret_cast<float *>(smem + S::OFF_STAT);        // merged max [G]
+    float *lst = mst + G;                                               // merged sum [G]
     float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);        // [2][MC][DSUB]
     int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);          // [2][M]
     float *snew = reinterpret_cast<float *>(newc + 2 * M);              // [G]
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(
-        smem + ((S::OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8));
-    uint8_t *codes_s = smem + S::OFF_CODES;
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int rank = 0;
@@ -248,61 +300,48 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     const int S_ = p.num_splits;
 
     if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        mbar_init(&bar[0], kThreads);                  // one cp.async arrival per thread
+        mbar_init(&bar[1], kThreads);
+        mbar_init(&bar[2], 1);
+        mbar_init(&bar[3], 1);
+        mbar_init(&bar[4], 1);
         fence_mbar_init();
         sflag[0] = 0;
     }
-    // ---- codebook set and the K slice first: the only reads allowed before
-    // the preceding kernel on the stream completes (programmatic dependent
-    // launch): codebooks and req_set are not written by it ------------------
+    __syncthreads();
+    // ---- reads allowed before the preceding kernel on the stream completes
+    // (programmatic dependent launch): req_set, seq_lens, the block table and
+    // the codebooks, which that kernel does not write ------------------------
     const int share = p.share;
     const int ts = split * p.split_len;
     const int a0 = ts + rank * share;
     const int g = tid % G, jslot = tid / G;
     const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
     const int set = __ldg(p.req_set + b);
+    const int L_raw = __ldg(p.seq_lens + b);
+    // page ids of this thread's tokens (before the length is known: only
+    // entries inside the block-table row are read)
+    int pid[TPT];
+    {
+        const int t_lim = min(a0 + share, p.max_pages * P);
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            pid[i] = -1;
+            if (i * S::TOK_PER_PASS >= share) break;
+            const int t = a0 + i * S::TOK_PER_PASS + jslot;
+            if (t < t_lim) pid[i] = __ldg(bt + t / P);
+        }
+    }
     const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
     const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
     const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
                        ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
                        static_cast<size_t>(rank) * S::CB_HALVES;
-    const __half *gV = gK + cb_unit;
-    uint64_t pol = 0;
-    if (warp == 0) __syncwarp();
-    auto issue_k_slice = [&]() {
-        if (warp == 0 && lane == 0 && set_ok) {
-            pol = policy_evict_first();
-            mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
-            bulk_g2s_hint(cbk, gK, S::CB_BYTES, &bar[0], pol);
-        }
-    };
-    // overlapped with the preceding kernel, the slice goes first; otherwise it
-    // goes after the length and page-id loads, which it would delay
-    if (p.overlap) issue_k_slice();
+    if (set_ok) {
+        copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
+        copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
+    }
     grid_dependency_wait();
-
-    // ---- length and page ids ----------------------------------------------
-    const int L_raw = __ldg(p.seq_lens + b);
-    int pgw[S::PPL];
-    if (warp == 0) {
-        const int np_lim = min(share / P, p.max_pages - a0 / P);
-#pragma unroll
-        for (int j = 0; j < S::PPL; ++j) {
-            const int idx = lane + 32 * j;
-            pgw[j] = idx < np_lim ? __ldg(bt + a0 / P + idx) : -1;
-        }
-    }
-    // the new token's owned K and V sub-vector elements, one per thread
-    __half xreg = __float2half(0.f);
-    if constexpr (APPEND) {
-        if (tid < 2 * MC * DSUB) {
-            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
-            xreg = __ldg(reinterpret_cast<const __half *>(p.kv_new) +
-                         ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D + rank * MC * DSUB + r);
-        }
-    }
-    if (!p.overlap) issue_k_slice();
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -324,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
                 }
             }
         }
-        if (tid == 0 && set_ok) mbar_wait_bounded(&bar[0], 0);   // the K slice copy lands first
+        if (set_ok) cp_async_wait_all();               // this thread's slice copies land first
         return;
     }
     const int e0 = min(te, a0 + share);
@@ -334,139 +373,136 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     const bool cl_new = APPEND && new_pos >= ts && new_pos < te;
     const bool own_new = cl_new && new_pos >= a0 && new_pos < e0;
     const int eS = own_new ? new_pos : e0;
-    const int npg = eS > a0 ? (eS - a0 + P - 1) / P : 0;
     const int pg_new = cl_new ? __ldg(bt + new_pos / P) : -1;   // checked where it is used
-
-    // ---- warp 0 issues the rest: code pages + query, then the V slice ------
-    if (warp == 0) {
-        bool ok[S::PPL];
-        int nvalid = 0, bad = 0;
-#pragma unroll
-        for (int j = 0; j < S::PPL; ++j) {
-            const int idx = lane + 32 * j;
-            ok[j] = idx < npg && pgw[j] >= 0 && static_cast<int64_t>(pgw[j]) < p.num_pages;
-            bad |= (idx < npg && !ok[j]);
-            nvalid += __popc(__ballot_sync(0xffffffffu, ok[j]));
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[4], G * D * 4);
+        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
+                 &bar[4]);
+        if constexpr (C > 1) {
+            mbar_arrive_expect_tx(&bar[2], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
+            mbar_arrive_expect_tx(&bar[3], (C - 1) * (S::ROW_FLOATS + S::STAT_FLOATS) * 4);
         }
-        if (bad) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
-        if (lane == 0) mbar_arrive_expect_tx(&bar[4], nvalid * S::PAGE_BYTES + G * D * 4);
-        __syncwarp();
+    }
+    // ---- this thread's codes, straight to registers --------------------------
+    Codes<M> cc[TPT];
+    unsigned valid = 0;                                 // bit i: token i is streamed
+    bool bad_pg = false;
+    const int nslot = (eS - a0 + S::TOK_PER_PASS - 1) / S::TOK_PER_PASS;   // token slots in use
 #pragma unroll
-        for (int j = 0; j < S::PPL; ++j) {
-            if (ok[j]) {
-                const int idx = lane + 32 * j;
-                bulk_g2s(codes_s + idx * S::PAGE_BYTES,
-                         p.code_pages + (static_cast<size_t>(pgw[j]) * Hkv + kvh) * S::PAGE_BYTES,
-                         S::PAGE_BYTES, &bar[4]);
-            }
-        }
-        if (lane == 0) {
-            bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
-                     &bar[4]);
-            mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
-            bulk_g2s_hint(cbv, gV, S::CB_BYTES, &bar[1], pol);
-            if constexpr (C > 1) {
-                mbar_arrive_expect_tx(&bar[2], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
-                mbar_arrive_expect_tx(&bar[3], (C - 1) * (S::ROW_FLOATS + S::STAT_FLOATS) * 4);
+    for (int i = 0; i < TPT; ++i) {
+        if (i >= nslot) break;
+        const int t = a0 + i * S::TOK_PER_PASS + jslot;
+        if (t < eS) {
+            const int pg = pid[i];
+            if (pg >= 0 && static_cast<int64_t>(pg) < p.num_pages) {
+                cc[i].load_global(p.code_pages + ((static_cast<size_t>(pg) * Hkv + kvh) * P + t % P) * (2 * M));
+                valid |= 1u << i;
+            } else {
+                bad_pg = true;
             }
         }
     }
-    for (int i = tid; i < S::LUT_FLOATS / 4; i += kThreads)
+    // the new token's owned K and V sub-vector elements, one per thread
+    if constexpr (APPEND) {
+        if (cl_new && tid < 2 * MC * DSUB) {
+            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
+            xnew[tid] = __half2float(__ldg(reinterpret_cast<const __half *>(p.kv_new) +
+                                           ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D +
+                                           rank * MC * DSUB + r));
+        }
+    }
+    for (int i = tid; i < S::BIN_WORDS / 4; i += kThreads)
         reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < G) snew[tid] = -INFINITY;
-    if (cl_new && tid < 2 * MC * DSUB) xnew[tid] = __half2float(xreg);
     grid_launch_dependents();                          // every read of this CTA is issued
-    if constexpr (C > 1) {
-        cluster_arrive_relaxed();          // peers' mbarriers exist before anyone pushes
-        cluster_wait_acquire();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();                                   // bins, new token, flags visible
+    if (bad_pg) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+    if constexpr (C > 1) cluster_arrive_relaxed();     // this CTA's barriers are ready for pushes
 
-    // ---- lookup-table rows of the owned subspaces, pushed to the peers ------
-    if (!mbar_wait_bounded(&bar[0], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-    if (!mbar_wait_bounded(&bar[4], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-    constexpr int NCH = DSUB / 8;                       // 16-byte chunks per codeword row
-    // per-thread chunk order: lanes of a quarter-warp read distinct banks
-    const int rot = (tid / (128 / (DSUB * 2))) % NCH;
-    {
-        // thread tid = codeword k: its row is read once into registers and
-        // gives the G table entries and (fused step) its distance to the new
-        // key's sub-vector
+    // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
+    // new token's K and V codes from the same rows --------------------------
+    bool tmo = !mbar_wait_bounded(&bar[0], 0);
+    tmo |= !mbar_wait_bounded(&bar[4], 0);
+    if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
+    float dkv[MC];
+    int vcode[MC];                                     // the new token's V codes, owned subspaces
 #pragma unroll
-        for (int mi = 0; mi < MC; ++mi) {
-            const int m = rank * MC + mi;
-            uint4 u[NCH];
-            load_row_rotated<NCH>(u, cbk + (static_cast<size_t>(mi) * K + tid) * DSUB, rot);
-            float acc[G];
+    for (int mi = 0; mi < MC; ++mi) vcode[mi] = -1;
+#pragma unroll
+    for (int mi = 0; mi < MC; ++mi) {
+        const int m = rank * MC + mi;
+        const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
+        unsigned long long acc2[G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) acc2[gg] = 0ull;
+        float dk = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            unsigned long long f[4];
+            to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int c0 = 0; c0 < NCH; ++c0) {
-                    const int c = (c0 + rot) % NCH;
-                    const float2 f0 = h2_to_f2(u[c0].x), f1 = h2_to_f2(u[c0].y), f2 = h2_to_f2(u[c0].z),
-                                 f3 = h2_to_f2(u[c0].w);
-                    const float4 *qv = reinterpret_cast<const float4 *>(qs + gg * D + m * DSUB + c * 8);
-                    const float4 qa = qv[0], qb = qv[1];
-                    a0 = fmaf(qa.x, f0.x, a0); a1 = fmaf(qb.x, f2.x, a1);
-                    a0 = fmaf(qa.y, f0.y, a0); a1 = fmaf(qb.y, f2.y, a1);
-                    a0 = fmaf(qa.z, f1.x, a0); a1 = fmaf(qb.z, f3.x, a1);
-                    a0 = fmaf(qa.w, f1.y, a0); a1 = fmaf(qb.w, f3.y, a1);
-                }
-                acc[gg] = (a0 + a1) * p.scale_log2;
+                const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qs + gg * D + m * DSUB + c * 8);
+                const ulonglong2 qa = qv[0], qb = qv[1];
+                unsigned long long a = acc2[gg];
+                a = f2_fma(qa.x, f[0], a);
+                a = f2_fma(qa.y, f[1], a);
+                a = f2_fma(qb.x, f[2], a);
+                a = f2_fma(qb.y, f[3], a);
+                acc2[gg] = a;
             }
-            float *dst = lut + (static_cast<size_t>(m) * K + tid) * G;
-            store_vec<G>(dst, acc);
-            if constexpr (C > 1) {
-                const uint32_t la = smem_u32(dst), lb = smem_u32(&bar[2]);
+            if (APPEND && cl_new) dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
+        }
+        float acc[G];
 #pragma unroll
-                for (int r = 1; r < C; ++r) {
-                    const uint32_t pr = (rank + r) % C;
-                    push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
-                }
+        for (int gg = 0; gg < G; ++gg) {
+            const float2 a = f2_unpack(acc2[gg]);
+            acc[gg] = (a.x + a.y) * p.scale_log2;
+        }
+        float *dst = lut + (static_cast<size_t>(m) * K + tid) * G;
+        store_vec<G>(dst, acc);
+        if constexpr (C > 1) {
+            const uint32_t la = smem_u32(dst), lb = smem_u32(&bar[2]);
+#pragma unroll
+            for (int r = 1; r < C; ++r) {
+                const uint32_t pr = (rank + r) % C;
+                push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
             }
-            if constexpr (APPEND) {
-                if (cl_new) {                          // K code of the new token in subspace m
-                    const int code = block_argmin(row_distance<NCH>(u, xnew + mi * DSUB, rot), keys);
-                    if (tid == 0) {
-                        newc[m] = code;
-                        if constexpr (C > 1) {
-                            const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
+        }
+        dkv[mi] = dk;
+    }
+    if constexpr (APPEND) {
+        if (cl_new) {
+            const int code = block_argmin_n<MC>(dkv, keys);
+            if (tid < MC) {                            // K code of subspace rank*MC + tid, to every CTA
+                const int m = rank * MC + tid;
+                newc[m] = code;
+                if constexpr (C > 1) {
+                    const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
 #pragma unroll
-                            for (int r = 1; r < C; ++r) {
-                                const uint32_t pr = (rank + r) % C;
-                                st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
-                            }
-                        }
+                    for (int r = 1; r < C; ++r) {
+                        const uint32_t pr = (rank + r) % C;
+                        st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
                     }
                 }
             }
         }
     }
-    if constexpr (C > 1) {
-        if (!mbar_wait_bounded(&bar[2], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-    }
+    if constexpr (C > 1) tmo |= !mbar_wait_bounded(&bar[2], 0);
+    if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     __syncthreads();
 
-    // ---- code stream: scores, softmax statistics, value bins -------------------
-    // Three passes over the share: (1) scores by M table gathers and the per-head
-    // max, (2) per-head sum of exp2(s - max), (3) scatter of each weight into the
-    // 256-bin value accumulators as the unsigned fixed-point integer
-    // floor(p 2^32 (1 - 2^-16) / l): the bins cannot overflow (the margin covers
-    // the rounding of the float sum), integer shared-memory atomics are exact
-    // and fast, and the result does not depend on their order.  The first
-    // chunk's codes and scores stay in registers, so (2) and (3) read shared
-    // memory only for the atomics (a share is one chunk whenever G = 1).  The
-    // fused step's new token enters (1) and (2) from its fresh codes; its value
-    // bin is added after the merge, once its V code is known.
+    // ---- scores, softmax statistics, value bins --------------------------------
+    // Scores by M table gathers stay in registers; the block's per-head max
+    // comes first, then each weight p = exp2(s - max) is added to the 256-bin
+    // value accumulators as the unsigned fixed-point integer
+    // round(p (2^32 - 2^12) / n), n = tokens this CTA streams: every p <= 1,
+    // so no bin can overflow, integer shared-memory atomics are exact and fast,
+    // and the result does not depend on their order.  The per-head sum of the
+    // weights is reduced alongside.  The fused step's new token enters the
+    // max and the sum from its fresh codes; its value bin is added after the
+    // merge.
     unsigned *ibins = reinterpret_cast<unsigned *>(bins);
-    auto gather = [&](const Codes<M> &cd) -> float {
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < M; ++m) acc += lut[(m * K + cd.k(m)) * G + g];
-        return acc;
-    };
     float s_new = -INFINITY;
     if constexpr (APPEND) {
         if (own_new && tid < G) {
@@ -476,88 +512,51 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             snew[tid] = s_new;
         }
     }
-    Codes<M> cc[TPT];
     float sc[TPT];
-    float mx = s_new;
-#pragma unroll 1
-    for (int cb = a0; cb < eS; cb += S::CHUNK) {
+    float mt = s_new;
 #pragma unroll
-        for (int i = 0; i < TPT; ++i) {
-            const int t = cb + i * S::TOK_PER_PASS + jslot;
-            if (t < eS) {
-                Codes<M> cd;
-                cd.load(codes_s + (t - a0) * (2 * M));
-                const float s = gather(cd);
-                if (cb == a0) { cc[i] = cd; sc[i] = s; }
-                mx = fmaxf(mx, s);
-            }
+    for (int i = 0; i < TPT; ++i) {
+        if (i >= nslot) break;
+        if (valid & (1u << i)) {
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) s += lut[(m * K + cc[i].k(m)) * G + g];
+            sc[i] = s;
+            mt = fmaxf(mt, s);
         }
     }
+    if constexpr (G == 1) {
+        mt = warp_max_f32(mt);
+    } else {
 #pragma unroll
-    for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane < G) red_max[warp * G + lane] = mx;
+        for (int off = G; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    }
+    if (lane < G) red_m[warp * G + lane] = mt;
     __syncthreads();
-    mx = red_max[g];
+    float mx = red_m[g];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_max[w * G + g]);
-    float l_run = (s_new != -INFINITY) ? exp2f(s_new - mx) : 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll 1
-        for (int cb = a0; cb < eS; cb += S::CHUNK) {
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+    const float qscale = __fdividef(4294963200.0f, static_cast<float>(max(eS - a0, 1)));
+    float lt = (s_new != -INFINITY) ? exp2f(s_new - mx) : 0.f;
 #pragma unroll
-            for (int i = 0; i < TPT; ++i) {
-                const int t = cb + i * S::TOK_PER_PASS + jslot;
-                if (t < eS) {
-                    float s;
-                    if (cb == a0) {
-                        s = sc[i];
-                    } else {
-                        Codes<M> cd;
-                        cd.load(codes_s + (t - a0) * (2 * M));
-                        s = gather(cd);
-                    }
-                    l_run += exp2f(s - mx);
-                }
-            }
+    for (int i = 0; i < TPT; ++i) {
+        if (i >= nslot) break;
+        if (valid & (1u << i)) {
+            const float w = exp2f(sc[i] - mx);
+            lt += w;
+            const unsigned q = __float2uint_rn(w * qscale);
+#pragma unroll
+            for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
         }
     }
 #pragma unroll
-    for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
-    if (lane < G) red_sum[warp * G + lane] = l_run;
+    for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+    if (lane < G) red_l[warp * G + lane] = lt;
     __syncthreads();
     float lsum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) lsum += red_sum[w * G + g];
-    const float qscale = lsum > 0.f ? 4294901760.0f / lsum : 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll 1
-        for (int cb = a0; cb < eS; cb += S::CHUNK) {
-#pragma unroll
-            for (int i = 0; i < TPT; ++i) {
-                const int t = cb + i * S::TOK_PER_PASS + jslot;
-                if (t < eS) {
-                    Codes<M> cd;
-                    float s;
-                    if (cb == a0) {
-                        cd = cc[i];
-                        s = sc[i];
-                    } else {
-                        cd.load(codes_s + (t - a0) * (2 * M));
-                        s = gather(cd);
-                    }
-                    const unsigned q = __float2uint_rz(exp2f(s - mx) * qscale);
-#pragma unroll
-                    for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cd.vv(m)) * G + g], q);
-                }
-            }
-        }
-    }
-    if (tid < G) {
-        mst[tid] = mx;                                 // this CTA's statistics for now
-        lst[tid] = lsum;
-        cfac[tid] = qscale > 0.f ? 1.0f / qscale : 0.f;  // integer bin -> weight
-    }
-    __syncthreads();
+    for (int w = 0; w < kWarps; ++w) lsum += red_l[w * G + g];
+    const float cfac = __fdividef(1.0f, qscale);       // integer bin -> weight
 
     // ---- push bins rows (as weights) and statistics to the peers that own them
     if constexpr (C > 1) {
@@ -571,50 +570,85 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             const uint4 *src = reinterpret_cast<const uint4 *>(ibins + pr * S::ROW_FLOATS);
             for (int i = tid; i < S::ROW_FLOATS / 4; i += kThreads) {
                 const uint4 v = src[i];
-                const int g0 = (4 * i) % G;
                 st_async_v4(rslot + 16 * i,
-                            make_float4(static_cast<float>(v.x) * cfac[g0], static_cast<float>(v.y) * cfac[(g0 + 1) % G],
-                                        static_cast<float>(v.z) * cfac[(g0 + 2) % G],
-                                        static_cast<float>(v.w) * cfac[(g0 + 3) % G]),
+                            make_float4(static_cast<float>(v.x) * cfac, static_cast<float>(v.y) * cfac,
+                                        static_cast<float>(v.z) * cfac, static_cast<float>(v.w) * cfac),
                             rbar);
             }
-            if (tid < G) {
-                st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mst[tid], rbar);
-                st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lst[tid], rbar);
+            if (tid < G) {                             // g == tid here
+                st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mx, rbar);
+                st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lsum, rbar);
                 st_async_f32(rslot + 4 * (S::ROW_FLOATS + 2 * G + tid), snew[tid], rbar);
             }
             if (tid == 0) st_async_f32(rslot + 4 * (S::ROW_FLOATS + 3 * G), __int_as_float(sflag[0]), rbar);
         }
+    }
+    // the new token's V codes (the peers' bins are landing meanwhile), then
+    // its codes into its page slot, its page id checked here
+    if constexpr (APPEND) {
+        if (cl_new) {
+            if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+            float dv[MC];
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) {
+                const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
+                float d = 0.f;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    unsigned long long f[4];
+                    to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
+                    d = sqdist8(d, xnew + (MC + mi) * DSUB + c * 8, f);
+                }
+                dv[mi] = d;
+            }
+            block_argmin_all<MC>(dv, keys + MC * kWarps, vcode);
+            if (tid == 0) {
+                const bool pg_ok = pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages;
+                if (pg_ok) {
+                    uint8_t *dst = p.code_pages_w +
+                                   ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
+#pragma unroll
+                    for (int mi = 0; mi < MC; ++mi) {
+                        dst[rank * MC + mi] = static_cast<uint8_t>(newc[rank * MC + mi]);
+                        dst[M + rank * MC + mi] = static_cast<uint8_t>(vcode[mi]);
+                    }
+                } else {
+                    atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+                }
+            }
+        }
+    }
+    if constexpr (C > 1) {
         if (!mbar_wait_bounded(&bar[3], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         cluster_arrive_relaxed();                      // all traffic into this CTA has landed
     }
 
-    // ---- merge statistics, then the owned rows of the value bins ------------
-    if (tid < G) {
+    // ---- merge: every thread merges the statistics of its head g, then its
+    // elements (e = tid + j*kThreads, so e mod G == g) of the owned bin rows --
+    float ms = -INFINITY, ls = 0.f, sn = snew[g];
+    float fac[C];
+    {
         float mr[C], lr[C];
-        float ms = -INFINITY, sn = snew[tid];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            if (r == rank) { mr[r] = mst[tid]; lr[r] = lst[tid]; }
+            if (r == rank) { mr[r] = mx; lr[r] = lsum; }
             else {
                 const float *sl = inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE;
-                mr[r] = sl[S::ROW_FLOATS + tid];
-                lr[r] = sl[S::ROW_FLOATS + G + tid];
-                sn = fmaxf(sn, sl[S::ROW_FLOATS + 2 * G + tid]);
+                mr[r] = sl[S::ROW_FLOATS + g];
+                lr[r] = sl[S::ROW_FLOATS + G + g];
+                sn = fmaxf(sn, sl[S::ROW_FLOATS + 2 * G + g]);
             }
             if (lr[r] > 0.f) ms = fmaxf(ms, mr[r]);
         }
-        float ls = 0.f;
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            const float f = (lr[r] > 0.f) ? exp2f(mr[r] - ms) : 0.f;
-            fac[r * G + tid] = f;
-            ls += f * lr[r];
+            fac[r] = (lr[r] > 0.f) ? exp2f(mr[r] - ms) : 0.f;
+            ls += fac[r] * lr[r];
         }
-        fac[rank * G + tid] *= cfac[tid];              // own rows are still integers
+    }
+    if (tid < G) {
         mst[tid] = ms;
         lst[tid] = ls;
-        snew[tid] = sn;
     }
     if (tid == 0) {
         int bb = sflag[0];
@@ -625,102 +659,81 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         sflag[1] = bb;
         if (sflag[0]) flag_status(p.status, sflag[0]);
     }
-    __syncthreads();
-    int bad_all = sflag[1];
     float *wtot = lut;                                 // [MC][K][G]; the LUT is no longer read
     {
-        constexpr int N4 = S::ROW_FLOATS / 4;
-        const uint4 *own = reinterpret_cast<const uint4 *>(ibins + rank * S::ROW_FLOATS);
-        for (int i = tid; i < N4; i += kThreads) {
-            const int g0 = (4 * i) % G;
-            const uint4 o = own[i];
-            float4 acc = make_float4(fac[rank * G + g0] * static_cast<float>(o.x),
-                                     fac[rank * G + (g0 + 1) % G] * static_cast<float>(o.y),
-                                     fac[rank * G + (g0 + 2) % G] * static_cast<float>(o.z),
-                                     fac[rank * G + (g0 + 3) % G] * static_cast<float>(o.w));
+        const float fown = fac[rank] * cfac;           // own rows are still integers
+        const float wnew = (APPEND && cl_new && sn != -INFINITY) ? exp2f(sn - ms) : 0.f;
+        for (int e = tid; e < S::ROW_FLOATS; e += kThreads) {
+            float a = fown * static_cast<float>(ibins[rank * S::ROW_FLOATS + e]);
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                if (r == rank) continue;
-                const float4 v = reinterpret_cast<const float4 *>(inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE)[i];
-                acc.x += fac[r * G + g0] * v.x;
-                acc.y += fac[r * G + (g0 + 1) % G] * v.y;
-                acc.z += fac[r * G + (g0 + 2) % G] * v.z;
-                acc.w += fac[r * G + (g0 + 3) % G] * v.w;
+            for (int r = 0; r < C; ++r)
+                if (r != rank) a += fac[r] * inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + e];
+            if constexpr (APPEND) {
+                // the new token's value bin
+                const int k = (e / G) % K, mi = e / (K * G);
+                if (cl_new && k == vcode[mi]) a += wnew;
             }
-            reinterpret_cast<float4 *>(wtot)[i] = acc;
+            wtot[e] = a;
         }
     }
     __syncthreads();
+    int bad_all = sflag[1];
 
     // ---- value codebook product for the owned subspaces -----------------------
     if (!mbar_wait_bounded(&bar[1], 0)) {
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
     }
-    if constexpr (APPEND) {
-        if (cl_new) {                                  // V codes of the new token, its value bins
-#pragma unroll 1
-            for (int mi = 0; mi < MC; ++mi) {
-                uint4 u[NCH];
-                load_row_rotated<NCH>(u, cbv + (static_cast<size_t>(mi) * K + tid) * DSUB, rot);
-                const int code = block_argmin(row_distance<NCH>(u, xnew + (MC + mi) * DSUB, rot), keys);
-                if (tid < G && snew[tid] != -INFINITY)
-                    wtot[(static_cast<size_t>(mi) * K + code) * G + tid] += exp2f(snew[tid] - mst[tid]);
-                if (tid == 0) newc[M + rank * MC + mi] = code;
-            }
-            const bool pg_ok = pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages;
-            if (tid == 0 && !pg_ok) flag_status(p.status, AQ_DEV_BAD_PAGE);
-            if (!pg_ok) bad_all |= AQ_DEV_BAD_PAGE;
-            if (tid == 0 && pg_ok) {                   // the new token's codes into its page slot
-                uint8_t *dst = p.code_pages_w +
-                               ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
-#pragma unroll
-                for (int mi = 0; mi < MC; ++mi) {
-                    dst[rank * MC + mi] = static_cast<uint8_t>(newc[rank * MC + mi]);
-                    dst[M + rank * MC + mi] = static_cast<uint8_t>(newc[M + rank * MC + mi]);
-                }
-            }
-            __syncthreads();
-        }
-    }
     // thread = (k slice, 4-dim quad of the owned dims): 8-byte codebook loads,
     // the slices of a warp reduced by shuffles, the warps through shared memory
     float *ored = reinterpret_cast<float *>(cbk);      // [kWarps][MC*DSUB][G]
     {
         constexpr int NQ = MC * DSUB / 4, KSQ = kThreads / NQ, KSLQ = K / KSQ;
+        constexpr int ROWS128 = 128 / (DSUB * 2);
+        static_assert(KSQ % (ROWS128 * NCH) == 0, "row step keeps the swizzle position");
         const int qd = tid % NQ, ks = tid / NQ;
         const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
-        float acc[G][4];
+        const int cj = j4 / 8, hj = j4 % 8;
+        // rows k = ks + i*KSQ: consecutive k-slices of a warp read neighbouring
+        // rows (conflict-free), and every row of a thread holds chunk cj at the
+        // same swizzled position, so all loads are at fixed offsets
+        const __half *vrow = cbv + ((mi * K + ks) * NCH + chunk_pos<DSUB>(ks, cj)) * 8 + hj;
+        const float *wrow = wtot + (static_cast<size_t>(mi) * K + ks) * G;
+        unsigned long long acc[G][2];
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = acc[gg][2] = acc[gg][3] = 0.f;
-#pragma unroll 4
+        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
+#pragma unroll 8
         for (int i = 0; i < KSLQ; ++i) {
-            const int k = ks * KSLQ + ((i + ks) % KSLQ);
-            const uint2 cv2 = *reinterpret_cast<const uint2 *>(cbv + (static_cast<size_t>(mi) * K + k) * DSUB + j4);
-            const float2 c01 = h2_to_f2(cv2.x), c23 = h2_to_f2(cv2.y);
+            const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
+            const unsigned long long c01 = h2_to_f2p(cv2.x), c23 = h2_to_f2p(cv2.y);
             float w[G];
-            load_vec<G>(w, wtot + (static_cast<size_t>(mi) * K + k) * G);
+            load_vec<G>(w, wrow + i * KSQ * G);
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
-                acc[gg][0] = fmaf(w[gg], c01.x, acc[gg][0]);
-                acc[gg][1] = fmaf(w[gg], c01.y, acc[gg][1]);
-                acc[gg][2] = fmaf(w[gg], c23.x, acc[gg][2]);
-                acc[gg][3] = fmaf(w[gg], c23.y, acc[gg][3]);
+                const unsigned long long ww = f2_pack(w[gg], w[gg]);
+                acc[gg][0] = f2_fma(ww, c01, acc[gg][0]);
+                acc[gg][1] = f2_fma(ww, c23, acc[gg][1]);
             }
+        }
+        float accf[G][4];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const float2 a01 = f2_unpack(acc[gg][0]), a23 = f2_unpack(acc[gg][1]);
+            accf[gg][0] = a01.x; accf[gg][1] = a01.y; accf[gg][2] = a23.x; accf[gg][3] = a23.y;
         }
 #pragma unroll
         for (int off = NQ; off < 32; off <<= 1) {
 #pragma unroll
             for (int gg = 0; gg < G; ++gg)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[gg][e] += __shfl_xor_sync(0xffffffffu, acc[gg][e], off);
+                for (int e = 0; e < 4; ++e) accf[gg][e] += __shfl_xor_sync(0xffffffffu, accf[gg][e], off);
         }
         if (lane < NQ) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 float v[G];
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg) v[gg] = acc[gg][e];
+                for (int gg = 0; gg < G; ++gg) v[gg] = accf[gg][e];
                 store_vec<G>(ored + (static_cast<size_t>(warp) * MC * DSUB + mi * DSUB + j4 + e) * G, v);
             }
         }
@@ -738,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             const float nan = __int_as_float(0x7fc00000);
             if (S_ == 1) {
                 const float l = lst[gg];
-                p.out[bh * D + d] = bad_all ? nan : (l > 0.f ? o / l : 0.f);
+                p.out[bh * D + d] = bad_all ? nan : (l > 0.f ? __fdividef(o, l) : 0.f);
             } else {
                 p.part_o[(bh * S_ + split) * D + d] = o;
                 if (rank == 0 && dl == 0) {
@@ -751,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // A wait that ran out may leave a copy or a push still landing: wait again
     // (bounded) before the shared memory is released.
     if (sflag[0] & AQ_DEV_TIMEOUT) {
+        cp_async_wait_all();
         mbar_wait_bounded(&bar[0], 0);
         mbar_wait_bounded(&bar[1], 0);
         mbar_wait_bounded(&bar[4], 0);
@@ -790,9 +804,9 @@ template <int M, int G, int C, bool APPEND>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
     auto kern = pq_decode_kernel<M, G, C, APPEND>;
-    if (plan.share > kMaxShare || plan.share % kPage) return cudaErrorInvalidValue;
+    if (plan.share > S::MAX_SHARE || plan.share % kPage) return cudaErrorInvalidValue;
     static size_t attr_bytes = 0;                  // opt-in dynamic shared memory set so far
-    const size_t need = S::smem(plan.share);
+    const size_t need = S::smem();
     if (need > attr_bytes) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(need));
@@ -839,9 +853,9 @@ cudaError_t dispatch_g(const DecodeParams &p, int G, const Plan &plan, cudaStrea
 }
 
 template <int M>
-size_t smem_g(int G, int C, int share) {
+size_t smem_g(int G, int C) {
 #define AQ_SM(GG, CC) \
-    if (G == GG && C == CC) return PqCfg<M, GG, CC>::smem(share);
+    if (G == GG && C == CC) return PqCfg<M, GG, CC>::smem();
     AQ_SM(1, 1) AQ_SM(1, 2) AQ_SM(1, 4)
     AQ_SM(2, 1) AQ_SM(2, 2) AQ_SM(2, 4)
     AQ_SM(4, 1) AQ_SM(4, 2) AQ_SM(4, 4)
@@ -852,9 +866,18 @@ size_t smem_g(int G, int C, int share) {
 
 }  // namespace
 
-size_t pq_decode_smem_bytes(int M, int G, int cluster, int share) {
-    if (M == 4) return smem_g<4>(G, cluster, share);
-    if (M == 8) return smem_g<8>(G, cluster, share);
+size_t pq_decode_smem_bytes(int M, int G, int cluster) {
+    if (M == 4) return smem_g<4>(G, cluster);
+    if (M == 8) return smem_g<8>(G, cluster);
+    return 0;
+}
+
+int pq_decode_max_share(int M, int G) {
+#define AQ_MS(MM, GG) \
+    if (M == MM && G == GG) return PqCfg<MM, GG, 1>::MAX_SHARE;
+    AQ_MS(4, 1) AQ_MS(4, 2) AQ_MS(4, 4) AQ_MS(4, 8)
+    AQ_MS(8, 1) AQ_MS(8, 2) AQ_MS(8, 4) AQ_MS(8, 8)
+#undef AQ_MS
     return 0;
 }
 

@@ -72,11 +72,11 @@ cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
 cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s);
 
-// Shared-memory bytes a PQ decode CTA needs for (M, G, cluster) and a share of
-// `share` tokens per CTA (their codes are staged in shared memory).
-size_t pq_decode_smem_bytes(int M, int G, int cluster, int share);
-// Largest per-CTA token share the PQ decode kernel stages at once.
-constexpr int kMaxShare = 2048;
+// Shared-memory bytes a PQ decode CTA needs for (M, G, cluster).
+size_t pq_decode_smem_bytes(int M, int G, int cluster);
+// Largest token share one cluster CTA handles (its tokens' codes live in
+// registers, a fixed number per thread); 0 for an unsupported (M, G).
+int pq_decode_max_share(int M, int G);
 size_t fit_smem_bytes(int M, int n_samples);
 // Record a CUDA error for aq_last_error_message() and clear the runtime's
 // last-error state.
