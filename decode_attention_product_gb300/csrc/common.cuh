@@ -205,6 +205,14 @@ __device__ __forceinline__ unsigned long long h2_to_f2p(uint32_t u) {
     return f2_pack(f.x, f.y);
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0,
+// 2^0 = 1): the softmax weights need no more.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Warp-wide maximum of a float (all 32 lanes take part).
 __device__ __forceinline__ float warp_max_f32(float v) {
     float r;

@@ -76,7 +76,7 @@ struct PqCfg {
     // new token: owned sub-vectors [2][MC][DSUB] f32, codes [2][M] int, score [G]
     static constexpr int OFF_NEW = (OFF_STAT + 2 * G * 4 + 15) / 16 * 16;
     static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8;
-    static constexpr int END = OFF_KEYS + NKEY * kWarps * 8;
+    static constexpr int END = OFF_KEYS + NKEY * 8;
     static size_t smem() { return END; }
     static_assert(K == kThreads, "one thread per codeword in the table build");
     static_assert(CB_CHUNKS % kThreads == 0, "whole slice chunks per thread");
@@ -174,18 +174,18 @@ template <>
 struct Codes<4> {
     uint2 v;
     __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v2(p); }
-    __device__ __forceinline__ int k(int m) const { return (v.x >> (8 * m)) & 0xff; }
-    __device__ __forceinline__ int vv(int m) const { return (v.y >> (8 * m)) & 0xff; }
+    __device__ __forceinline__ int k(int m) const { return static_cast<int>(__byte_perm(v.x, 0u, 0x4440u | m)); }
+    __device__ __forceinline__ int vv(int m) const { return static_cast<int>(__byte_perm(v.y, 0u, 0x4440u | m)); }
 };
 template <>
 struct Codes<8> {
     uint4 v;
     __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v4(p); }
     __device__ __forceinline__ int k(int m) const {
-        return ((m < 4 ? v.x : v.y) >> (8 * (m & 3))) & 0xff;
+        return static_cast<int>(__byte_perm(m < 4 ? v.x : v.y, 0u, 0x4440u | (m & 3)));
     }
     __device__ __forceinline__ int vv(int m) const {
-        return ((m < 4 ? v.z : v.w) >> (8 * (m & 3))) & 0xff;
+        return static_cast<int>(__byte_perm(m < 4 ? v.z : v.w, 0u, 0x4440u | (m & 3)));
     }
 };
 
@@ -216,57 +216,18 @@ __device__ __forceinline__ void to_f2p4(const uint4 &u, unsigned long long (&f)[
     f[3] = h2_to_f2p(u.w);
 }
 
-// CTA-wide argmins of NK distances per thread (thread = codeword), lowest
-// index on ties; thread n < NK receives the n-th code.  Distances are >= 0, so
-// their bit patterns order like their values.  Contains one __syncthreads.
-template <int NK>
-__device__ __forceinline__ int block_argmin_n(const float (&d)[NK], unsigned long long *keys) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int n = 0; n < NK; ++n) {
-        unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d[n])) << 32) |
-                                 static_cast<unsigned>(tid);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-            key = o < key ? o : key;
-        }
-        if (lane == 0) keys[n * kWarps + warp] = key;
-    }
-    __syncthreads();
-    int code = 0;
-    if (tid < NK) {
-        unsigned long long best = keys[tid * kWarps];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) best = keys[tid * kWarps + w] < best ? keys[tid * kWarps + w] : best;
-        code = static_cast<int>(best & 0xffu);
-    }
-    return code;
-}
-
-// Same, every thread receiving all NK codes (no barrier needed after it).
-template <int NK>
-__device__ __forceinline__ void block_argmin_all(const float (&d)[NK], unsigned long long *keys, int (&code)[NK]) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int n = 0; n < NK; ++n) {
-        unsigned long long key = (static_cast<unsigned long long>(__float_as_uint(d[n])) << 32) |
-                                 static_cast<unsigned>(tid);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-            key = o < key ? o : key;
-        }
-        if (lane == 0) keys[n * kWarps + warp] = key;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int n = 0; n < NK; ++n) {
-        unsigned long long best = keys[n * kWarps];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) best = keys[n * kWarps + w] < best ? keys[n * kWarps + w] : best;
-        code[n] = static_cast<int>(best & 0xffu);
-    }
+// CTA-wide argmin, lowest index on ties, of one distance per thread (thread =
+// codeword): the warp's smallest distance by an integer min-reduction over the
+// bit patterns (distances are >= 0, so they order like their values), its
+// lowest lane by a ballot, then one 64-bit (distance, index) atomic minimum per
+// warp into `slot`, which holds ~0 beforehand.  The code is slot & 0xff once a
+// __syncthreads has passed.
+__device__ __forceinline__ void warp_argmin_into(float d, unsigned long long *slot) {
+    const unsigned db = __float_as_uint(d);
+    const unsigned mn = __reduce_min_sync(0xffffffffu, db);
+    const unsigned ball = __ballot_sync(0xffffffffu, db == mn);
+    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(ball) - 1))
+        atomicMin(slot, (static_cast<unsigned long long>(mn) << 32) | threadIdx.x);
 }
 
 template <int M, int G, int C, bool APPEND>
@@ -289,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);        // [2][MC][DSUB]
     int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);          // [2][M]
     float *snew = reinterpret_cast<float *>(newc + 2 * M);              // [G]
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);  // [2][MC] argmin slots
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int rank = 0;
@@ -329,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             pid[i] = -1;
             if (i * S::TOK_PER_PASS >= share) break;
             const int t = a0 + i * S::TOK_PER_PASS + jslot;
-            if (t < t_lim) pid[i] = __ldg(bt + t / P);
+            if (t < t_lim) pid[i] = __ldg(bt + static_cast<unsigned>(t) / P);
         }
     }
     const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
@@ -387,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     Codes<M> cc[TPT];
     unsigned valid = 0;                                 // bit i: token i is streamed
     bool bad_pg = false;
+    const size_t page_stride = static_cast<size_t>(Hkv) * (P * 2 * M);  // one page, all kv heads
+    const uint8_t *codes_kvh = p.code_pages + static_cast<size_t>(kvh) * (P * 2 * M);
     const int nslot = (eS - a0 + S::TOK_PER_PASS - 1) / S::TOK_PER_PASS;   // token slots in use
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
@@ -395,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         if (t < eS) {
             const int pg = pid[i];
             if (pg >= 0 && static_cast<int64_t>(pg) < p.num_pages) {
-                cc[i].load_global(p.code_pages + ((static_cast<size_t>(pg) * Hkv + kvh) * P + t % P) * (2 * M));
+                cc[i].load_global(codes_kvh + static_cast<size_t>(pg) * page_stride +
+                                  (static_cast<unsigned>(t) % P) * (2 * M));
                 valid |= 1u << i;
             } else {
                 bad_pg = true;
@@ -414,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     for (int i = tid; i < S::BIN_WORDS / 4; i += kThreads)
         reinterpret_cast<float4 *>(bins)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < G) snew[tid] = -INFINITY;
+    if (tid < S::NKEY) keys[tid] = ~0ull;
     grid_launch_dependents();                          // every read of this CTA is issued
     __syncthreads();                                   // bins, new token, flags visible
     if (bad_pg) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
@@ -431,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
 #pragma unroll
     for (int mi = 0; mi < MC; ++mi) {
         const int m = rank * MC + mi;
+        const float *qm = qs + m * DSUB;
         const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
         unsigned long long acc2[G];
 #pragma unroll
@@ -442,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
-                const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qs + gg * D + m * DSUB + c * 8);
+                const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qm + gg * D + c * 8);
                 const ulonglong2 qa = qv[0], qb = qv[1];
                 unsigned long long a = acc2[gg];
                 a = f2_fma(qa.x, f[0], a);
@@ -465,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             const uint32_t la = smem_u32(dst), lb = smem_u32(&bar[2]);
 #pragma unroll
             for (int r = 1; r < C; ++r) {
-                const uint32_t pr = (rank + r) % C;
+                const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
                 push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
             }
         }
@@ -473,15 +439,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     }
     if constexpr (APPEND) {
         if (cl_new) {
-            const int code = block_argmin_n<MC>(dkv, keys);
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dkv[mi], &keys[mi]);
+            __syncthreads();
             if (tid < MC) {                            // K code of subspace rank*MC + tid, to every CTA
                 const int m = rank * MC + tid;
+                const int code = static_cast<int>(keys[tid] & 0xffu);
                 newc[m] = code;
                 if constexpr (C > 1) {
                     const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[2]);
 #pragma unroll
                     for (int r = 1; r < C; ++r) {
-                        const uint32_t pr = (rank + r) % C;
+                        const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
                         st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
                     }
                 }
@@ -496,9 +465,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // Scores by M table gathers stay in registers; the block's per-head max
     // comes first, then each weight p = exp2(s - max) is added to the 256-bin
     // value accumulators as the unsigned fixed-point integer
-    // round(p (2^32 - 2^12) / n), n = tokens this CTA streams: every p <= 1,
-    // so no bin can overflow, integer shared-memory atomics are exact and fast,
-    // and the result does not depend on their order.  The per-head sum of the
+    // round(p (2^32 - 2^12) / n), n = tokens this CTA streams (<= 2048): every
+    // p <= 1 to within the exp2 approximation, and the 2^12 margin covers that
+    // and the roundings, so no bin can overflow; integer shared-memory atomics
+    // are exact and fast, and the result does not depend on their order.  The
+    // per-head sum of the
     // weights is reduced alongside.  The fused step's new token enters the
     // max and the sum from its fresh codes; its value bin is added after the
     // merge.
@@ -537,12 +508,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
     const float qscale = __fdividef(4294963200.0f, static_cast<float>(max(eS - a0, 1)));
-    float lt = (s_new != -INFINITY) ? exp2f(s_new - mx) : 0.f;
+    float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mx) : 0.f;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
         if (i >= nslot) break;
         if (valid & (1u << i)) {
-            const float w = exp2f(sc[i] - mx);
+            const float w = fast_exp2(sc[i] - mx);
             lt += w;
             const unsigned q = __float2uint_rn(w * qscale);
 #pragma unroll
@@ -563,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         const uint32_t lb = smem_u32(&bar[3]);
 #pragma unroll 1
         for (int r = 1; r < C; ++r) {
-            const uint32_t pr = (rank + r) % C;
-            const int slot = (C - r - 1) % C;          // (rank - pr - 1) mod C
+            const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
+            const int slot = C - r - 1;                // (rank - pr - 1) mod C
             const uint32_t rslot = mapa_u32(smem_u32(inc + slot * S::INC_STRIDE), pr);
             const uint32_t rbar = mapa_u32(lb, pr);
             const uint4 *src = reinterpret_cast<const uint4 *>(ibins + pr * S::ROW_FLOATS);
@@ -601,7 +572,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
                 }
                 dv[mi] = d;
             }
-            block_argmin_all<MC>(dv, keys + MC * kWarps, vcode);
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[MC + mi]);
+            __syncthreads();
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) vcode[mi] = static_cast<int>(keys[MC + mi] & 0xffu);
             if (tid == 0) {
                 const bool pg_ok = pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages;
                 if (pg_ok) {
@@ -625,25 +600,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
 
     // ---- merge: every thread merges the statistics of its head g, then its
     // elements (e = tid + j*kThreads, so e mod G == g) of the owned bin rows --
+    // peers by distance d = 1..C-1 from this CTA: the CTA of rank (rank+d) mod C
+    // pushed into slot d-1, so every index below is a compile-time constant
     float ms = -INFINITY, ls = 0.f, sn = snew[g];
-    float fac[C];
+    float fac[C];                                      // [d]: scale of distance d's rows
     {
-        float mr[C], lr[C];
+        float md[C], ld[C];
+        md[0] = mx;
+        ld[0] = lsum;
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            if (r == rank) { mr[r] = mx; lr[r] = lsum; }
-            else {
-                const float *sl = inc + ((r - rank - 1 + C) % C) * S::INC_STRIDE;
-                mr[r] = sl[S::ROW_FLOATS + g];
-                lr[r] = sl[S::ROW_FLOATS + G + g];
-                sn = fmaxf(sn, sl[S::ROW_FLOATS + 2 * G + g]);
-            }
-            if (lr[r] > 0.f) ms = fmaxf(ms, mr[r]);
+        for (int d = 1; d < C; ++d) {
+            const float *sl = inc + (d - 1) * S::INC_STRIDE + S::ROW_FLOATS;
+            md[d] = sl[g];
+            ld[d] = sl[G + g];
+            sn = fmaxf(sn, sl[2 * G + g]);
         }
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            fac[r] = (lr[r] > 0.f) ? exp2f(mr[r] - ms) : 0.f;
-            ls += fac[r] * lr[r];
+        for (int d = 0; d < C; ++d)
+            if (ld[d] > 0.f) ms = fmaxf(ms, md[d]);
+#pragma unroll
+        for (int d = 0; d < C; ++d) {
+            fac[d] = (ld[d] > 0.f) ? fast_exp2(md[d] - ms) : 0.f;
+            ls += fac[d] * ld[d];
         }
     }
     if (tid < G) {
@@ -653,27 +631,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     if (tid == 0) {
         int bb = sflag[0];
 #pragma unroll
-        for (int r = 0; r < C; ++r)
-            if (r != rank)
-                bb |= __float_as_int(inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + S::ROW_FLOATS + 3 * G]);
+        for (int d = 1; d < C; ++d) bb |= __float_as_int(inc[(d - 1) * S::INC_STRIDE + S::ROW_FLOATS + 3 * G]);
         sflag[1] = bb;
         if (sflag[0]) flag_status(p.status, sflag[0]);
     }
     float *wtot = lut;                                 // [MC][K][G]; the LUT is no longer read
     {
-        const float fown = fac[rank] * cfac;           // own rows are still integers
-        const float wnew = (APPEND && cl_new && sn != -INFINITY) ? exp2f(sn - ms) : 0.f;
-        for (int e = tid; e < S::ROW_FLOATS; e += kThreads) {
-            float a = fown * static_cast<float>(ibins[rank * S::ROW_FLOATS + e]);
+        const float fown = fac[0] * cfac;              // own rows are still integers
+        const float wnew = (APPEND && cl_new && sn != -INFINITY) ? fast_exp2(sn - ms) : 0.f;
+        const unsigned *own = ibins + rank * S::ROW_FLOATS;
 #pragma unroll
-            for (int r = 0; r < C; ++r)
-                if (r != rank) a += fac[r] * inc[((r - rank - 1 + C) % C) * S::INC_STRIDE + e];
-            if constexpr (APPEND) {
-                // the new token's value bin
-                const int k = (e / G) % K, mi = e / (K * G);
-                if (cl_new && k == vcode[mi]) a += wnew;
+        for (int mi = 0; mi < MC; ++mi) {
+            for (int e1 = tid; e1 < K * G; e1 += kThreads) {   // e1 mod G == g
+                const int e = mi * K * G + e1;
+                float a = fown * static_cast<float>(own[e]);
+#pragma unroll
+                for (int d = 1; d < C; ++d) a += fac[d] * inc[(d - 1) * S::INC_STRIDE + e];
+                if constexpr (APPEND) {
+                    // the new token's value bin
+                    if (cl_new && static_cast<unsigned>(e1) / G == static_cast<unsigned>(vcode[mi])) a += wnew;
+                }
+                wtot[e] = a;
             }
-            wtot[e] = a;
         }
     }
     __syncthreads();
