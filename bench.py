@@ -293,10 +293,11 @@ def run_ours(args, w, rank, world, local_rank):
     def step(i, ev0=None, ev1=None):
         c = copies[i % R]
         if not args.two_call:
-            # one fused launch: append the new token + attention; overlapping the
-            # previous step's tail (codebooks and req_set are not written by it)
+            # one fused launch: append the new token + attention, overlapping the
+            # previous step's tail, which wrote another copy's pages (with a
+            # single copy the previous step wrote these pages: no overlap)
             api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
-                            c["seq_lens"], Lmax, w.scale, overlap=True, out=outs[i % R], workspace=ws,
+                            c["seq_lens"], Lmax, w.scale, overlap=R > 1, out=outs[i % R], workspace=ws,
                             status=status)
             return
         api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)

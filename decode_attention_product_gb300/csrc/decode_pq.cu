@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     }
     __syncthreads();
     // ---- reads allowed before the preceding kernel on the stream completes
-    // (programmatic dependent launch): req_set, seq_lens, the block table and
-    // the codebooks, which that kernel does not write ------------------------
+    // (programmatic dependent launch): req_set, seq_lens, the block table, the
+    // codebooks and the code pages, which that kernel does not write ---------
     const int share = p.share;
     const int ts = split * p.split_len;
     const int a0 = ts + rank * share;
@@ -302,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
         copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
     }
-    grid_dependency_wait();
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -311,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
     if (bad0 || ts >= te) {
         // nothing to stream: NaN for a bad request, zeros / empty partials otherwise
+        grid_dependency_wait();
         if (rank == 0) {
             if (bad0 && tid == 0) flag_status(p.status, bad0);
             const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
@@ -335,11 +335,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     const bool own_new = cl_new && new_pos >= a0 && new_pos < e0;
     const int eS = own_new ? new_pos : e0;
     const int pg_new = cl_new ? __ldg(bt + new_pos / P) : -1;   // checked where it is used
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&bar[4], G * D * 4);
-        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
-                 &bar[4]);
-        if constexpr (C > 1) {
+    if constexpr (C > 1) {
+        if (tid == 0) {
             mbar_arrive_expect_tx(&bar[2], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
             mbar_arrive_expect_tx(&bar[3], (C - 1) * (S::ROW_FLOATS + S::STAT_FLOATS) * 4);
         }
@@ -365,6 +362,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
                 bad_pg = true;
             }
         }
+    }
+    // ---- the query and the new token come from the preceding kernel ------------
+    grid_dependency_wait();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[4], G * D * 4);
+        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
+                 &bar[4]);
     }
     // the new token's owned K and V sub-vector elements, one per thread
     if constexpr (APPEND) {

@@ -222,12 +222,14 @@ aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch,
  *   kv_new_f16    in   fp16 [B][Hkv][2][D]
  *   code_pages    in/out (only the new tokens' slots are written)
  *   flags         AQ_STEP_OVERLAP: the call may start reading the codebooks,
- *                 req_set, seq_lens and block_table before the preceding
- *                 kernel on `stream` has finished (programmatic dependent
- *                 launch); q, kv_new_f16 and code_pages are read, and out,
+ *                 req_set, seq_lens, block_table and code_pages before the
+ *                 preceding kernel on `stream` has finished (programmatic
+ *                 dependent launch); q and kv_new_f16 are read, and out,
  *                 code_pages, workspace and device_status written, only after
- *                 it.  Set it only when that kernel writes none of the four
- *                 inputs read early.  0: plain stream order.
+ *                 it.  Set it only when that kernel writes none of the five
+ *                 inputs read early -- not, for example, right after another
+ *                 aq_decode_step on the same code_pages.  0: plain stream
+ *                 order.
  *   other arguments as aq_decode_attention.
  * ------------------------------------------------------------------------- */
 #define AQ_STEP_OVERLAP 1
