@@ -228,6 +228,18 @@ __device__ __forceinline__ uint32_t mapa_u32(uint32_t local_smem_addr, uint32_t 
     return r;
 }
 
+// Bulk copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory to a shared-memory address of the cluster (from
+// mapa_u32); the bytes are counted on the destination CTA's mbarrier, given
+// as a cluster address.  Writes to the source by the generic proxy must be
+// fenced (fence_proxy_async_shared) before the copy is issued.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
 // Asynchronous store into a peer CTA's shared memory; the bytes are counted
 // on the peer's mbarrier (complete_tx), which orders them for its waiters.
 __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {

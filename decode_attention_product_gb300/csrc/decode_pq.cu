@@ -57,8 +57,9 @@ struct PqCfg {
     // tokens per thread, held in registers (codes and scores)
     static constexpr int TPT = (M == 8 && G <= 2) ? 4 : 8;
     static constexpr int MAX_SHARE = TPT * TOK_PER_PASS;    // tokens per CTA
-    // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag
-    static constexpr int STAT_FLOATS = 3 * G + 1;
+    // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag,
+    // the scale of the (integer) bins
+    static constexpr int STAT_FLOATS = 3 * G + 2;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
     static constexpr int NKEY = 2 * MC;                     // new-token argmins: K then V, owned subspaces
     // shared-memory layout (bytes)
@@ -85,7 +86,7 @@ struct PqCfg {
     static_assert(kWarps * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
     static_assert(CB_BYTES % 16 == 0 && OFF_LUT % 16 == 0 && OFF_INC % 16 == 0 && OFF_Q % 16 == 0,
                   "alignment");
-    static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "vector pushes");
+    static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "bulk copies of whole rows");
 };
 
 // CTAs per SM the register budget is sized for: shared memory (LUT, bins and
@@ -149,21 +150,6 @@ __device__ __forceinline__ void load_vec(float (&v)[N], const float *src) {
     } else {
 #pragma unroll
         for (int i = 0; i < N; ++i) v[i] = src[i];
-    }
-}
-
-// Push N floats from registers to the same offset in a peer's shared memory.
-template <int N>
-__device__ __forceinline__ void push_vec(uint32_t raddr, const float (&v)[N], uint32_t rbar) {
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < N; i += 4)
-            st_async_v4(raddr + 4 * i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]), rbar);
-    } else if constexpr (N == 2) {
-        st_async_v2(raddr, v[0], v[1], rbar);
-    } else {
-#pragma unroll
-        for (int i = 0; i < N; ++i) st_async_f32(raddr + 4 * i, v[i], rbar);
     }
 }
 
@@ -429,23 +415,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             const float2 a = f2_unpack(acc2[gg]);
             acc[gg] = (a.x + a.y) * p.scale_log2;
         }
-        float *dst = lut + (static_cast<size_t>(m) * K + tid) * G;
-        store_vec<G>(dst, acc);
-        if constexpr (C > 1) {
-            const uint32_t la = smem_u32(dst), lb = smem_u32(&bar[2]);
-#pragma unroll
-            for (int r = 1; r < C; ++r) {
-                const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
-                push_vec<G>(mapa_u32(la, pr), acc, mapa_u32(lb, pr));
-            }
-        }
+        store_vec<G>(lut + (static_cast<size_t>(m) * K + tid) * G, acc);
         dkv[mi] = dk;
     }
     if constexpr (APPEND) {
         if (cl_new) {
 #pragma unroll
             for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dkv[mi], &keys[mi]);
-            __syncthreads();
+        }
+    }
+    if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
+    __syncthreads();
+    if constexpr (C > 1) {
+        // this CTA's rows to every peer in one bulk copy each; the source is not
+        // written again before every peer has received it (each peer scores,
+        // and pushes its bins, only once it has)
+        if (tid < C - 1) {
+            const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) & (C - 1);
+            const uint32_t rows = smem_u32(lut + rank * S::ROW_FLOATS);
+            bulk_s2cluster(mapa_u32(rows, pr), rows, S::ROW_FLOATS * 4, mapa_u32(smem_u32(&bar[2]), pr));
+        }
+    }
+    if constexpr (APPEND) {
+        if (cl_new) {
             if (tid < MC) {                            // K code of subspace rank*MC + tid, to every CTA
                 const int m = rank * MC + tid;
                 const int code = static_cast<int>(keys[tid] & 0xffu);
@@ -513,49 +505,65 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
     const float qscale = __fdividef(4294963200.0f, static_cast<float>(max(eS - a0, 1)));
     float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mx) : 0.f;
+    unsigned lq = 0;                                   // G == 1: the weights' fixed-point sum
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
         if (i >= nslot) break;
         if (valid & (1u << i)) {
             const float w = fast_exp2(sc[i] - mx);
-            lt += w;
             const unsigned q = __float2uint_rn(w * qscale);
+            if constexpr (G == 1) lq += q;
+            else lt += w;
 #pragma unroll
             for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
         }
     }
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-    if (lane < G) red_l[warp * G + lane] = lt;
-    __syncthreads();
-    float lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) lsum += red_l[w * G + g];
+    if constexpr (C > 1) fence_proxy_async_shared();  // the bins, for the bulk copies below
     const float cfac = __fdividef(1.0f, qscale);       // integer bin -> weight
+    float lsum = 0.f;
+    if constexpr (G == 1) {
+        // the sum of the fixed-point weights, exact, then the new token's
+        lq = __reduce_add_sync(0xffffffffu, lq);
+        if (lane == 0) reinterpret_cast<unsigned *>(red_l)[warp] = lq;
+        __syncthreads();
+        unsigned qsum = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) qsum += reinterpret_cast<const unsigned *>(red_l)[w];
+        const float sn0 = snew[0];                     // this CTA's new token, if it holds it
+        lsum = static_cast<float>(qsum) * cfac + (sn0 != -INFINITY ? fast_exp2(sn0 - mx) : 0.f);
+    } else {
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+        if (lane < G) red_l[warp * G + lane] = lt;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) lsum += red_l[w * G + g];
+    }
 
-    // ---- push bins rows (as weights) and statistics to the peers that own them
+    // ---- bins rows (integers, one bulk copy per peer) and statistics to the
+    // peers that own them; sender rank lands in slot (rank - pr - 1) mod C ----
     if constexpr (C > 1) {
         const uint32_t lb = smem_u32(&bar[3]);
-#pragma unroll 1
-        for (int r = 1; r < C; ++r) {
+        if (tid < C - 1) {
+            const int r = tid + 1;
             const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
-            const int slot = C - r - 1;                // (rank - pr - 1) mod C
-            const uint32_t rslot = mapa_u32(smem_u32(inc + slot * S::INC_STRIDE), pr);
-            const uint32_t rbar = mapa_u32(lb, pr);
-            const uint4 *src = reinterpret_cast<const uint4 *>(ibins + pr * S::ROW_FLOATS);
-            for (int i = tid; i < S::ROW_FLOATS / 4; i += kThreads) {
-                const uint4 v = src[i];
-                st_async_v4(rslot + 16 * i,
-                            make_float4(static_cast<float>(v.x) * cfac, static_cast<float>(v.y) * cfac,
-                                        static_cast<float>(v.z) * cfac, static_cast<float>(v.w) * cfac),
-                            rbar);
+            bulk_s2cluster(mapa_u32(smem_u32(inc + (C - r - 1) * S::INC_STRIDE), pr),
+                           smem_u32(ibins + pr * S::ROW_FLOATS), S::ROW_FLOATS * 4, mapa_u32(lb, pr));
+        }
+        if (tid < G) {                                 // g == tid here
+#pragma unroll
+            for (int r = 1; r < C; ++r) {
+                const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
+                const uint32_t st = mapa_u32(smem_u32(inc + (C - r - 1) * S::INC_STRIDE + S::ROW_FLOATS), pr);
+                const uint32_t rbar = mapa_u32(lb, pr);
+                st_async_f32(st + 4 * tid, mx, rbar);
+                st_async_f32(st + 4 * (G + tid), lsum, rbar);
+                st_async_f32(st + 4 * (2 * G + tid), snew[tid], rbar);
+                if (tid == 0) {
+                    st_async_f32(st + 4 * (3 * G), __int_as_float(sflag[0]), rbar);
+                    st_async_f32(st + 4 * (3 * G + 1), cfac, rbar);
+                }
             }
-            if (tid < G) {                             // g == tid here
-                st_async_f32(rslot + 4 * (S::ROW_FLOATS + tid), mx, rbar);
-                st_async_f32(rslot + 4 * (S::ROW_FLOATS + G + tid), lsum, rbar);
-                st_async_f32(rslot + 4 * (S::ROW_FLOATS + 2 * G + tid), snew[tid], rbar);
-            }
-            if (tid == 0) st_async_f32(rslot + 4 * (S::ROW_FLOATS + 3 * G), __int_as_float(sflag[0]), rbar);
         }
     }
     // the new token's V codes (the peers' bins are landing meanwhile), then
@@ -608,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // pushed into slot d-1, so every index below is a compile-time constant
     float ms = -INFINITY, ls = 0.f, sn = snew[g];
     float fac[C];                                      // [d]: scale of distance d's rows
+    float pscale[C];                                   // [d]: distance d's integer-bin scale
+    pscale[0] = cfac;
     {
         float md[C], ld[C];
         md[0] = mx;
@@ -618,14 +628,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
             md[d] = sl[g];
             ld[d] = sl[G + g];
             sn = fmaxf(sn, sl[2 * G + g]);
+            pscale[d] = sl[3 * G + 1];
         }
 #pragma unroll
         for (int d = 0; d < C; ++d)
             if (ld[d] > 0.f) ms = fmaxf(ms, md[d]);
 #pragma unroll
         for (int d = 0; d < C; ++d) {
-            fac[d] = (ld[d] > 0.f) ? fast_exp2(md[d] - ms) : 0.f;
-            ls += fac[d] * ld[d];
+            const float f = (ld[d] > 0.f) ? fast_exp2(md[d] - ms) : 0.f;
+            ls += f * ld[d];
+            fac[d] = f * pscale[d];                    // integer bin -> weight relative to ms
         }
     }
     if (tid < G) {
@@ -641,16 +653,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     }
     float *wtot = lut;                                 // [MC][K][G]; the LUT is no longer read
     {
-        const float fown = fac[0] * cfac;              // own rows are still integers
         const float wnew = (APPEND && cl_new && sn != -INFINITY) ? fast_exp2(sn - ms) : 0.f;
         const unsigned *own = ibins + rank * S::ROW_FLOATS;
 #pragma unroll
         for (int mi = 0; mi < MC; ++mi) {
             for (int e1 = tid; e1 < K * G; e1 += kThreads) {   // e1 mod G == g
                 const int e = mi * K * G + e1;
-                float a = fown * static_cast<float>(own[e]);
+                float a = fac[0] * static_cast<float>(own[e]);
 #pragma unroll
-                for (int d = 1; d < C; ++d) a += fac[d] * inc[(d - 1) * S::INC_STRIDE + e];
+                for (int d = 1; d < C; ++d)
+                    a += fac[d] * static_cast<float>(reinterpret_cast<const unsigned *>(inc)[(d - 1) * S::INC_STRIDE + e]);
                 if constexpr (APPEND) {
                     // the new token's value bin
                     if (cl_new && static_cast<unsigned>(e1) / G == static_cast<unsigned>(vcode[mi])) a += wnew;
