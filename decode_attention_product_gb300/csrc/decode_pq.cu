@@ -284,10 +284,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
                        ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
                        static_cast<size_t>(rank) * S::CB_HALVES;
-    if (set_ok) {
-        copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
-        copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
-    }
+    // the K slice now; the V slice, needed only after the scores, once the K
+    // slice has landed, so that no CTA's first data queues behind V slices
+    if (set_ok) copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -377,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
     // new token's K and V codes from the same rows --------------------------
     bool tmo = !mbar_wait_bounded(&bar[0], 0);
+    copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
     tmo |= !mbar_wait_bounded(&bar[4], 0);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
@@ -544,25 +544,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // peers that own them; sender rank lands in slot (rank - pr - 1) mod C ----
     if constexpr (C > 1) {
         const uint32_t lb = smem_u32(&bar[3]);
-        if (tid < C - 1) {
-            const int r = tid + 1;
+        // warp r-1 serves peer r: lane 0 the bulk copy, lanes g < G the statistics
+        if (warp < C - 1 && lane < G) {                // g == lane here
+            const int r = warp + 1;
             const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
-            bulk_s2cluster(mapa_u32(smem_u32(inc + (C - r - 1) * S::INC_STRIDE), pr),
-                           smem_u32(ibins + pr * S::ROW_FLOATS), S::ROW_FLOATS * 4, mapa_u32(lb, pr));
-        }
-        if (tid < G) {                                 // g == tid here
-#pragma unroll
-            for (int r = 1; r < C; ++r) {
-                const uint32_t pr = static_cast<uint32_t>(rank + r) & (C - 1);
-                const uint32_t st = mapa_u32(smem_u32(inc + (C - r - 1) * S::INC_STRIDE + S::ROW_FLOATS), pr);
-                const uint32_t rbar = mapa_u32(lb, pr);
-                st_async_f32(st + 4 * tid, mx, rbar);
-                st_async_f32(st + 4 * (G + tid), lsum, rbar);
-                st_async_f32(st + 4 * (2 * G + tid), snew[tid], rbar);
-                if (tid == 0) {
-                    st_async_f32(st + 4 * (3 * G), __int_as_float(sflag[0]), rbar);
-                    st_async_f32(st + 4 * (3 * G + 1), cfac, rbar);
-                }
+            const uint32_t rslot = smem_u32(inc + (C - r - 1) * S::INC_STRIDE);
+            const uint32_t rbar = mapa_u32(lb, pr);
+            if (lane == 0)
+                bulk_s2cluster(mapa_u32(rslot, pr), smem_u32(ibins + pr * S::ROW_FLOATS), S::ROW_FLOATS * 4, rbar);
+            const uint32_t st = mapa_u32(rslot + 4 * S::ROW_FLOATS, pr);
+            st_async_f32(st + 4 * lane, mx, rbar);
+            st_async_f32(st + 4 * (G + lane), lsum, rbar);
+            st_async_f32(st + 4 * (2 * G + lane), snew[lane], rbar);
+            if (lane == 0) {
+                st_async_f32(st + 4 * (3 * G), __int_as_float(sflag[0]), rbar);
+                st_async_f32(st + 4 * (3 * G + 1), cfac, rbar);
             }
         }
     }
