@@ -440,9 +440,17 @@ def run_ours(args, w, rank, world, local_rank):
     if rank == 0 and not args.no_cpu:
         ost = OracleStep(w)
         units_c, secs_c, n_c = ost.run(args.cpu_budget)
+        cores = ost.oracle.num_threads()
+        # the same oracle on one thread, a third of the budget
+        ost.oracle.set_num_threads(1)
+        units_1, secs_1, n_1 = ost.run(args.cpu_budget / 3)
+        ost.oracle.set_num_threads(cores)
         line["cpu_baseline"] = {"value": units_c / secs_c, "unit": UNIT,
-                                "cores": ost.oracle.num_threads(), "kind": "oracle",
-                                "sample": ost.describe(n_c) + f", {secs_c:.1f} s"}
+                                "cores": cores, "kind": "oracle",
+                                "sample": ost.describe(n_c) + f", {secs_c:.1f} s",
+                                "value_1_thread": units_1 / secs_1,
+                                "sample_1_thread": ost.describe(n_1) + f", {secs_1:.1f} s",
+                                "host_cpus": os.cpu_count()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
