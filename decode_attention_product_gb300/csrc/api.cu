@@ -55,28 +55,20 @@ constexpr size_t kPlanSmemCap = 232448;
 //   PQ:   cluster C = 4 CTAs per split when M >= 4 (each owns M/C subspaces of
 //         both codebooks, so every codebook byte is read once and a split's
 //         tokens spread over 4 SMs), smaller if shared memory does not fit.
+//         When C = 4 would give many waves of CTAs anyway (a long ragged
+//         batch), C = 2: the per-(request, kv head) work -- table build, the
+//         new token's encode, value product -- then runs with half the
+//         exchanges and per-CTA overhead, and the GPU is still full.
 //         Splits are added only when (request, kv head) clusters cannot fill
 //         the GPU and each split keeps >= 1024 tokens, since every split
 //         re-reads the codebooks.
 //   fp16: splits so that (request, kv head, split) CTAs reach 2 per SM, each
 //         keeping >= 256 tokens.
-static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
-                           int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
-    const int P = cfg->page_size;
-    const int G = Hq / Hkv;
-    const int64_t units = static_cast<int64_t>(batch) * Hkv;
+constexpr int kManyWaves = 8;          // waves of 4 CTAs per SM
+
+static void split_plan(int C, int share_max, bool fp16, int64_t units, int max_seq_len, int req, int sms, int P,
+                       Plan *pl) {
     const int max_pages_needed = (max_seq_len + P - 1) / P;
-    int C = 1;
-    int share_max = 0;
-    if (!fp16) {
-        const int M = cfg->num_subspaces;
-        C = 0;
-        for (int c = 4; c >= 1; c /= 2)
-            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
-        if (C == 0) return AQ_ERR_UNSUPPORTED;
-        share_max = pq_decode_max_share(M, G) / P * P;
-        if (share_max <= 0) return AQ_ERR_UNSUPPORTED;
-    }
     int S = req;
     if (S <= 0) {
         const int64_t target = 2ll * sms;
@@ -103,14 +95,38 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     if (split_pages < 1) split_pages = 1;
     S = (max_pages_needed + split_pages - 1) / split_pages;
     if (S < 1) S = 1;
-    const int split_len = split_pages * P;
-    const int share = ((split_len + C - 1) / C + P - 1) / P * P;
     pl->num_splits = S;
     pl->cluster = C;
-    pl->split_len = split_len;
-    pl->share = share;
-    pl->workspace = S > 1 ? static_cast<size_t>(batch) * Hq * S * (kHeadDim + 2) * sizeof(float) : 0;
-    pl->smem = fp16 ? 0 : pq_decode_smem_bytes(cfg->num_subspaces, G, C);
+    pl->split_len = split_pages * P;
+    pl->share = ((pl->split_len + C - 1) / C + P - 1) / P * P;
+}
+
+static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
+                           int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
+    const int P = cfg->page_size;
+    const int G = Hq / Hkv;
+    const int64_t units = static_cast<int64_t>(batch) * Hkv;
+    if (fp16) {
+        split_plan(1, 0, true, units, max_seq_len, req, sms, P, pl);
+        pl->smem = 0;
+    } else {
+        const int M = cfg->num_subspaces;
+        int C = 0;
+        for (int c = 4; c >= 1; c /= 2)
+            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
+        if (C == 0) return AQ_ERR_UNSUPPORTED;
+        const int share_max = pq_decode_max_share(M, G) / P * P;
+        if (share_max <= 0) return AQ_ERR_UNSUPPORTED;
+        split_plan(C, share_max, false, units, max_seq_len, req, sms, P, pl);
+        const int64_t ctas = units * pl->num_splits * C;
+        if (C == 4 && ctas >= static_cast<int64_t>(kManyWaves) * sms * 4 &&
+            pq_decode_smem_bytes(M, G, 2) <= smem_cap)
+            split_plan(2, share_max, false, units, max_seq_len, req, sms, P, pl);
+        pl->smem = pq_decode_smem_bytes(M, G, pl->cluster);
+    }
+    pl->workspace = pl->num_splits > 1
+                        ? static_cast<size_t>(batch) * Hq * pl->num_splits * (kHeadDim + 2) * sizeof(float)
+                        : 0;
     return AQ_OK;
 }
 

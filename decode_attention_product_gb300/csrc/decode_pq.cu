@@ -65,8 +65,13 @@ struct PqCfg {
     // shared-memory layout (bytes)
     static constexpr int OFF_BAR = 0;                       // 5 mbarriers
     static constexpr int OFF_MISC = 64;                     // int flags
-    static constexpr int OFF_CBK = 128;
-    static constexpr int OFF_CBV = OFF_CBK + CB_BYTES;
+    // codebook slices: with clusters of 4 (4 resident CTAs per SM either way)
+    // one buffer each, the V slice issued as soon as the K slice has landed;
+    // with fewer CTAs per cluster (larger slices) one buffer holds the K slice
+    // until the table build and the new key's encode are done, then the V slice
+    static constexpr bool SHARED_CB = C < 4;
+    static constexpr int OFF_CB = 128;
+    static constexpr int OFF_CBV = OFF_CB + (SHARED_CB ? 0 : CB_BYTES);
     static constexpr int OFF_LUT = OFF_CBV + CB_BYTES;
     static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
     // [C-1][INC_STRIDE] from the peers; sender src lands in slot (src - dst - 1) mod C
@@ -83,7 +88,10 @@ struct PqCfg {
     static_assert(CB_CHUNKS % kThreads == 0, "whole slice chunks per thread");
     static_assert((NCH & (NCH - 1)) == 0 && NCH <= 8, "XOR swizzle over a power-of-two chunk count");
     static_assert((MC * DSUB / 4) <= 32 && 32 % (MC * DSUB / 4) == 0, "V-product quads within a warp");
-    static_assert(kWarps * MC * DSUB * G * 4 <= CB_BYTES, "V-product reduction fits in the K slice");
+    // V-product partials: in the peers' rows once merged (this CTA's own bins may
+    // still be in flight to its peers), or in the bins without peers
+    static_assert(C > 1 ? kWarps * MC * DSUB * G <= (C - 1) * INC_STRIDE : kWarps * MC * DSUB * G <= BIN_WORDS,
+                  "V-product reduction space");
     static_assert(CB_BYTES % 16 == 0 && OFF_LUT % 16 == 0 && OFF_INC % 16 == 0 && OFF_Q % 16 == 0,
                   "alignment");
     static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "bulk copies of whole rows");
@@ -223,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in, query
     int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);           // [0] local bad, [1] all
-    __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
-    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
+    __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CB);       // K slice
+    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);      // V slice (may alias it)
     float *lut = reinterpret_cast<float *>(smem + S::OFF_LUT);
     float *bins = reinterpret_cast<float *>(smem + S::OFF_BINS);
     float *inc = reinterpret_cast<float *>(smem + S::OFF_INC);
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
                        ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
                        static_cast<size_t>(rank) * S::CB_HALVES;
     // the K slice now; the V slice, needed only after the scores, once the K
-    // slice has landed, so that no CTA's first data queues behind V slices
+    // slice has landed (own buffer) or is no longer read (shared buffer)
     if (set_ok) copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
 
     // ---- request-level checks: uniform over the cluster ------------------
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
     // new token's K and V codes from the same rows --------------------------
     bool tmo = !mbar_wait_bounded(&bar[0], 0);
-    copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
+    if constexpr (!S::SHARED_CB) copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
     tmo |= !mbar_wait_bounded(&bar[4], 0);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
@@ -425,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         }
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
-    __syncthreads();
+    __syncthreads();                                   // every read of the K slice is done
+    if constexpr (S::SHARED_CB) copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
     if constexpr (C > 1) {
         // this CTA's rows to every peer in one bulk copy each; the source is not
         // written again before every peer has received it (each peer scores,
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
     }
     // thread = (k slice, 4-dim quad of the owned dims): 8-byte codebook loads,
     // the slices of a warp reduced by shuffles, the warps through shared memory
-    float *ored = reinterpret_cast<float *>(cbk);      // [kWarps][MC*DSUB][G]
+    float *ored = C > 1 ? inc : bins;                  // [kWarps][MC*DSUB][G]; merged, not in flight
     {
         constexpr int NQ = MC * DSUB / 4, KSQ = kThreads / NQ, KSLQ = K / KSQ;
         constexpr int ROWS128 = 128 / (DSUB * 2);

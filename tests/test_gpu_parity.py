@@ -90,6 +90,25 @@ def test_decode_matches_oracle(A, orc, case, splits):
             assert np.all(got[b] == 0.0)
 
 
+# many (request, kv head) units: the planner switches to clusters of 2 CTAs
+MANY = [(48, 32, 32, 4), (48, 32, 32, 8)]
+
+
+def _many_lens(n, seed):
+    return [int(x) for x in np.random.default_rng(seed).integers(1, 300, size=n)]
+
+
+@pytest.mark.parametrize("case", MANY, ids=[f"B{c[0]}H{c[1]}M{c[3]}" for c in MANY])
+def test_decode_many_units_cluster2(A, orc, case):
+    B, Hq, Hkv, M = case
+    lens = _many_lens(B, M)
+    assert A.decode_plan(B, Hq, Hkv, max(lens), M)[1] == 2
+    p = W.paged_codes_problem(31 + M, B, Hq, Hkv, M, lens, num_sets=B)
+    got, st = run_pq(A, p)
+    assert st == 0
+    close(got, oracle_pq(orc, p))
+
+
 def test_decode_plan_variants_agree(A, orc):
     """Cluster sizes 4 and the split counts the planner picks for the long shape
     give the same answer as the oracle."""
@@ -288,6 +307,30 @@ def test_decode_step_matches_oracle(A, orc, case, splits, overlap):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert np.array_equal(pages.cpu().numpy(), want_pages)    # the new codes, nothing else
+    close(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("case", MANY, ids=[f"B{c[0]}H{c[1]}M{c[3]}" for c in MANY])
+@pytest.mark.parametrize("overlap", [False, True])
+def test_decode_step_many_units_cluster2(A, orc, case, overlap):
+    B, Hq, Hkv, M = case
+    lens = _many_lens(B, M + 1)
+    assert A.decode_plan(B, Hq, Hkv, max(lens), M)[1] == 2
+    p = W.paged_codes_problem(41 + M, B, Hq, Hkv, M, lens, num_sets=B)
+    kv_new = np.random.default_rng(M).standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+    want_pages = p["code_pages"].copy()
+    slots = np.array([p["block_table"][b, (L - 1) // 16] * 16 + (L - 1) % 16 for b, L in enumerate(lens)],
+                     np.int64)
+    orc.encode_append(kv_new, p["req_set"], slots, p["codebooks"], want_pages, 16)
+    want = oracle_pq(orc, dict(p, code_pages=want_pages))
+    pages = dev(p["code_pages"])
+    st = A.new_status()
+    out = A.decode_step(dev(p["q"]), dev(kv_new), pages, dev(p["codebooks"]), dev(p["req_set"]),
+                        dev(p["block_table"]), dev(p["seq_lens"]), int(max(lens)), 1.0 / np.sqrt(128),
+                        overlap=overlap, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(pages.cpu().numpy(), want_pages)
     close(out.cpu().numpy(), want)
 
 
