@@ -61,7 +61,11 @@ struct PqCfg {
     // the scale of the (integer) bins
     static constexpr int STAT_FLOATS = 3 * G + 2;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
-    static constexpr int NKEY = 2 * MC;                     // new-token argmins: K then V, owned subspaces
+    static constexpr int NKEY = 2 * MC;
+    // value product: the k-slice order of subspace mi is XOR-ed with mi * VP_XOR,
+    // so that the rows one half-warp reads (several subspaces, neighbouring
+    // k-slices) fall in distinct 32- or 64-byte parts of their lines
+    static constexpr int VP_XOR = (M == 8 && C == 4) ? 2 : 1;                     // new-token argmins: K then V, owned subspaces
     // shared-memory layout (bytes)
     static constexpr int OFF_BAR = 0;                       // 5 mbarriers
     static constexpr int OFF_MISC = 64;                     // int flags
@@ -694,11 +698,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(cons
         const int qd = tid % NQ, ks = tid / NQ;
         const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
         const int cj = j4 / 8, hj = j4 % 8;
-        // rows k = ks + i*KSQ: consecutive k-slices of a warp read neighbouring
-        // rows (conflict-free), and every row of a thread holds chunk cj at the
+        // rows k = kx + i*KSQ, kx = ks ^ (mi * VP_XOR): the rows of one load are
+        // bank-conflict-free, and every row of a thread holds chunk cj at the
         // same swizzled position, so all loads are at fixed offsets
-        const __half *vrow = cbv + ((mi * K + ks) * NCH + chunk_pos<DSUB>(ks, cj)) * 8 + hj;
-        const float *wrow = wtot + (static_cast<size_t>(mi) * K + ks) * G;
+        const int kx = ks ^ ((mi * S::VP_XOR) & (KSQ - 1));
+        const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
+        const float *wrow = wtot + (static_cast<size_t>(mi) * K + kx) * G;
         unsigned long long acc[G][2];
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
