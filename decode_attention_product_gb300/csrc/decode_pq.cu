@@ -103,8 +103,8 @@ struct PqCfg {
 
 // CTAs per SM the register budget is sized for: shared memory (LUT, bins and
 // pushed rows all scale with G) allows about 4 / 2 / 1 resident CTAs.
-template <int G>
-constexpr int kMinBlocks = G <= 2 ? 4 : (G == 4 ? 2 : 1);
+template <int G, int C>
+constexpr int kMinBlocks = G <= 2 ? (C == 2 ? 5 : 4) : (G == 4 ? 2 : 1);
 
 // Position of 16-byte chunk c of codeword row k in shared memory: c XOR a
 // function of k, so that the 8 rows a quarter-warp reads at once (two or four
@@ -229,7 +229,7 @@ __device__ __forceinline__ void warp_argmin_into(float d, unsigned long long *sl
 }
 
 template <int M, int G, int C, bool APPEND>
-__global__ void __launch_bounds__(kThreads, kMinBlocks<G>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
     constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT, NCH = S::NCH;
     extern __shared__ __align__(128) unsigned char smem[];
