@@ -1,10 +1,12 @@
 // common.cuh -- shared device helpers of libaqpq (sm_103a).
 //
-// Inline-PTX wrappers for the Blackwell async-copy machinery used by the
-// kernels: mbarrier (init / expect-tx / bounded try-wait) and the bulk
-// global->shared copy engine (cp.async.bulk, completion counted in bytes on an
-// mbarrier).  Every wait here is bounded in wall-clock time: a wait that runs
-// out returns false, and the caller records AQ_DEV_TIMEOUT instead of hanging.
+// Inline-PTX wrappers used by the kernels: mbarriers (init / expect-tx /
+// bounded try-wait), the bulk copy engine (global -> shared, and shared -> a
+// peer CTA's shared memory, completion counted in bytes on an mbarrier),
+// per-thread cp.async copies, cluster barriers and addressing, packed fp32
+// pair arithmetic, programmatic dependent launch.  Every wait here is bounded
+// in wall-clock time: a wait that runs out returns false, and the caller
+// records AQ_DEV_TIMEOUT instead of hanging.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -91,16 +93,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
-// Same, with an L2 eviction-priority hint created by createpolicy.
-__device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gmem,
-                                              uint32_t bytes, uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
-        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 // 16-byte global -> shared copy through L2 (cp.async.cg): the destination is
 // any 16-byte aligned shared address, so a copy can lay rows out in its own
 // (swizzled) order.  Completion is tracked per thread.
@@ -118,21 +110,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// 16-byte streaming load through the non-coherent path, not kept in L1.
-__device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
+// 8-byte streaming load through the non-coherent path, not kept in L1 (data
+// that no kernel writes while this one runs).
 __device__ __forceinline__ uint2 ldg_stream_v2(const void *p) {
     uint2 v;
     asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
@@ -249,28 +228,8 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
         : "memory");
 }
 
-__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-            remote_addr),
-        "f"(a), "f"(b), "r"(remote_bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-            remote_addr),
-        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait_acquire() {
