@@ -62,6 +62,9 @@ constexpr size_t kPlanSmemCap = 232448;
 //         Splits are added only when (request, kv head) clusters cannot fill
 //         the GPU and each split keeps >= 1024 tokens, since every split
 //         re-reads the codebooks.
+//         A GQA group is split over several clusters (query heads per
+//         cluster G / head_split) before any KV split when the (request, kv
+//         head) clusters alone would not fill the GPU.
 //   fp16: splits so that (request, kv head, split) CTAs reach 2 per SM, each
 //         keeping >= 256 tokens.
 constexpr int kManyWaves = 8;          // waves of 4 CTAs per SM
@@ -108,21 +111,32 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
     if (fp16) {
         split_plan(1, 0, true, units, max_seq_len, req, sms, P, pl);
+        pl->head_split = 1;
         pl->smem = 0;
     } else {
         const int M = cfg->num_subspaces;
+        // a GQA group's query heads over several clusters while (request, kv
+        // head) clusters of 4 would not give 2 CTAs per SM: each cluster builds
+        // the table, scores and takes the value product for its heads only, so
+        // only the codebook and code reads (from L2 after the first) and the
+        // new token's encode repeat -- much cheaper than more KV splits
+        int nsub = 1;
+        while (nsub < G && units * 4 * nsub < 2ll * sms) nsub *= 2;
+        const int Gs = G / nsub;
         int C = 0;
         for (int c = 4; c >= 1; c /= 2)
-            if (c <= M && pq_decode_smem_bytes(M, G, c) <= smem_cap) { C = c; break; }
+            if (c <= M && pq_decode_smem_bytes(M, Gs, c) <= smem_cap) { C = c; break; }
         if (C == 0) return AQ_ERR_UNSUPPORTED;
-        const int share_max = pq_decode_max_share(M, G) / P * P;
+        const int share_max = pq_decode_max_share(M, Gs) / P * P;
         if (share_max <= 0) return AQ_ERR_UNSUPPORTED;
-        split_plan(C, share_max, false, units, max_seq_len, req, sms, P, pl);
-        const int64_t ctas = units * pl->num_splits * C;
+        const int64_t clusters = units * nsub;         // per split
+        split_plan(C, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+        const int64_t ctas = clusters * pl->num_splits * C;
         if (C == 4 && ctas >= static_cast<int64_t>(kManyWaves) * sms * 4 &&
-            pq_decode_smem_bytes(M, G, 2) <= smem_cap)
-            split_plan(2, share_max, false, units, max_seq_len, req, sms, P, pl);
-        pl->smem = pq_decode_smem_bytes(M, G, pl->cluster);
+            pq_decode_smem_bytes(M, Gs, 2) <= smem_cap)
+            split_plan(2, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+        pl->head_split = nsub;
+        pl->smem = pq_decode_smem_bytes(M, Gs, pl->cluster);
     }
     pl->workspace = pl->num_splits > 1
                         ? static_cast<size_t>(batch) * Hq * pl->num_splits * (kHeadDim + 2) * sizeof(float)
@@ -305,6 +319,8 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.kv_new = kv_new;
     p.code_pages_w = code_pages_w;
     p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
+    p.head_split_log2 = 0;
+    while ((1 << p.head_split_log2) < pl.head_split) ++p.head_split_log2;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = fp16     ? launch_fp16_decode(p, Hq / Hkv, pl, s)
                     : kv_new ? launch_pq_decode_step(p, cfg->num_subspaces, Hq / Hkv, pl, s)

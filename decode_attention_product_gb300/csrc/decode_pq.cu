@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     int rank = 0;
     if constexpr (C > 1) rank = static_cast<int>(cluster_ctarank());
     const int split = blockIdx.x / C;
-    const int kvh = blockIdx.y, b = blockIdx.z;
+    // blockIdx.y = kv head * 2^head_split_log2 + sub-group: this cluster serves
+    // query heads [blockIdx.y * G, +G) of kv head blockIdx.y >> head_split_log2
+    const int kvh = static_cast<int>(blockIdx.y >> p.head_split_log2), b = blockIdx.z;
+    const int hq0 = static_cast<int>(blockIdx.y) * G;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
             for (int i = tid; i < G * D; i += kThreads) {
                 const int gg = i / D, d = i % D;
-                const size_t bh = static_cast<size_t>(b) * Hq + kvh * G + gg;
+                const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
                 if (S_ == 1) p.out[bh * D + d] = v;
                 else if (d == 0) {
                     p.part_ml[(bh * S_ + split) * 2 + 0] = bad0 ? v : -INFINITY;
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     grid_dependency_wait();
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar[4], G * D * 4);
-        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G) * D, G * D * 4,
+        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + hq0) * D, G * D * 4,
                  &bar[4]);
     }
     // the new token's owned K and V sub-vector elements, one per thread
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             for (int w = 0; w < kWarps; ++w) o += ored[static_cast<size_t>(w) * NOUT + i];
             const int gg = i % G, dl = i / G;                 // dl in [0, MC*DSUB)
             const int d = rank * MC * DSUB + dl;
-            const size_t bh = static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G + gg;
+            const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
             const float nan = __int_as_float(0x7fc00000);
             if (S_ == 1) {
                 const float l = lst[gg];
@@ -819,7 +822,8 @@ cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) 
         attr_bytes = need;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
+    cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits),
+                       static_cast<unsigned>(p.num_kv_heads) << p.head_split_log2,
                        static_cast<unsigned>(p.batch));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = need;
@@ -888,6 +892,7 @@ int pq_decode_max_share(int M, int G) {
 
 cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
+    G /= plan.head_split;                          // query heads per cluster
     if (M == 4) e = dispatch_g<4, false>(p, G, plan, s);
     else if (M == 8) e = dispatch_g<8, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
@@ -898,6 +903,7 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
 
 cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
+    G /= plan.head_split;
     if (M == 4) e = dispatch_g<4, true>(p, G, plan, s);
     else if (M == 8) e = dispatch_g<8, true>(p, G, plan, s);
     else return cudaErrorInvalidValue;

@@ -27,6 +27,7 @@ struct DecodeParams {
     const void *kv_new;     // fp16 [B][Hkv][2][D]: the token appended by a fused decode step
     uint8_t *code_pages_w;  // writable alias of code_pages (fused decode step)
     int32_t overlap;        // launched as a programmatic dependent of the previous kernel
+    int32_t head_split_log2;  // PQ: 2^this clusters per kv head, each for Hq/Hkv >> this query heads
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -56,6 +57,7 @@ struct Plan {
     int32_t cluster;      // CTAs per split
     int32_t split_len;    // tokens per split (multiple of the page size)
     int32_t share;        // tokens per CTA of a cluster (multiple of the page size)
+    int32_t head_split;   // PQ: query-head sub-groups per kv head, each its own cluster
     size_t workspace;     // bytes
     size_t smem;          // dynamic shared memory per CTA
 };

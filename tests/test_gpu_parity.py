@@ -73,6 +73,7 @@ CASES = [
     (1, 16, 2, 8, [3001]),                     # M = 8 with group 8
     (1, 2, 2, 4, [9001]),                      # group 1, several chunks per CTA
     (4, 4, 4, 4, [0, 16, 15, 48]),             # empty request, page-exact lengths
+    (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # Qwen-shaped GQA: 2 head sub-groups
 ]
 
 
@@ -279,6 +280,7 @@ STEP_CASES = [
     (2, 4, 4, 8, [400, 1500]),                 # M = 8
     (1, 2, 2, 4, [9001]),                      # long: splits
     (4, 4, 4, 4, [16, 32, 48, 2048]),          # new token first in its page
+    (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # GQA with 2 head sub-groups per kv head
 ]
 
 
