@@ -62,6 +62,8 @@ constexpr size_t kPlanSmemCap = 232448;
 //         Splits are added only when (request, kv head) clusters cannot fill
 //         the GPU and each split keeps >= 1024 tokens, since every split
 //         re-reads the codebooks.
+//         With M = 8 and a request long enough for several splits, clusters
+//         of 8 (one subspace per CTA) halve the splits.
 //         A GQA group is split over several clusters (query heads per
 //         cluster G / head_split) before any KV split when the (request, kv
 //         head) clusters alone would not fill the GPU.
@@ -135,6 +137,11 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
         if (C == 4 && ctas >= static_cast<int64_t>(kManyWaves) * sms * 4 &&
             pq_decode_smem_bytes(M, Gs, 2) <= smem_cap)
             split_plan(2, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+        else if (C == 4 && M == 8 && pl->num_splits >= 2 && pq_decode_smem_bytes(M, Gs, 8) > 0 &&
+                 pq_decode_smem_bytes(M, Gs, 8) <= smem_cap)
+            // a long request with 8 subspaces: clusters of 8, one subspace per
+            // CTA, half the splits and so half the per-split fixed work
+            split_plan(8, share_max, false, clusters, max_seq_len, req, sms, P, pl);
         pl->head_split = nsub;
         pl->smem = pq_decode_smem_bytes(M, Gs, pl->cluster);
     }

@@ -846,6 +846,9 @@ cudaError_t dispatch_c(const DecodeParams &p, const Plan &plan, cudaStream_t s) 
         case 1: return launch_one<M, G, 1, APPEND>(p, plan, s);
         case 2: return launch_one<M, G, 2, APPEND>(p, plan, s);
         case 4: return launch_one<M, G, 4, APPEND>(p, plan, s);
+        case 8:                                    // one subspace per CTA
+            if constexpr (M == 8) return launch_one<M, G, 8, APPEND>(p, plan, s);
+            else return cudaErrorInvalidConfiguration;
         default: return cudaErrorInvalidConfiguration;
     }
 }
@@ -870,6 +873,12 @@ size_t smem_g(int G, int C) {
     AQ_SM(4, 1) AQ_SM(4, 2) AQ_SM(4, 4)
     AQ_SM(8, 1) AQ_SM(8, 2) AQ_SM(8, 4)
 #undef AQ_SM
+    if constexpr (M == 8) {
+        if (C == 8 && G == 1) return PqCfg<M, 1, 8>::smem();
+        if (C == 8 && G == 2) return PqCfg<M, 2, 8>::smem();
+        if (C == 8 && G == 4) return PqCfg<M, 4, 8>::smem();
+        if (C == 8 && G == 8) return PqCfg<M, 8, 8>::smem();
+    }
     return 0;
 }
 

@@ -281,6 +281,7 @@ STEP_CASES = [
     (1, 2, 2, 4, [9001]),                      # long: splits
     (4, 4, 4, 4, [16, 32, 48, 2048]),          # new token first in its page
     (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # GQA with 2 head sub-groups per kv head
+    (1, 4, 4, 8, [20000]),                     # M = 8, long: clusters of 8 over several splits
 ]
 
 
