@@ -22,6 +22,9 @@ aq_status cuda_fail(cudaError_t e) {
     return AQ_ERR_CUDA;
 }
 
+// Device tensors are read with 16-byte vector, cp.async and bulk copies.
+bool misaligned(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
 aq_status check_cfg(const aq_pq_config *cfg, bool need_pq) {
     if (!cfg) return AQ_ERR_INVALID_ARGUMENT;
     if (cfg->head_dim <= 0 || cfg->page_size <= 0) return AQ_ERR_INVALID_ARGUMENT;
@@ -180,6 +183,7 @@ aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_t n
     if (num_units < 0 || n_samples < 1 || iters < 1 || iters > 1000) return AQ_ERR_INVALID_ARGUMENT;
     if (n_samples > 1024) return AQ_ERR_UNSUPPORTED;
     if (num_units > 0 && (!samples_f16 || !codebooks_f16)) return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(samples_f16) || misaligned(codebooks_f16)) return AQ_ERR_INVALID_ARGUMENT;
     if (num_units > 2147483647ll) return AQ_ERR_UNSUPPORTED;
     if (num_units == 0) return AQ_OK;
     FitParams p{};
@@ -201,6 +205,8 @@ aq_status aq_kmeans_step(const aq_pq_config *cfg, int64_t num_units, int32_t n_s
     if (num_units < 0 || n_samples < 1) return AQ_ERR_INVALID_ARGUMENT;
     if (n_samples > 1024) return AQ_ERR_UNSUPPORTED;
     if (num_units > 0 && (!samples_f16 || !centroids_in || !centroids_out || !assign_out))
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(samples_f16) || misaligned(centroids_in) || misaligned(centroids_out))
         return AQ_ERR_INVALID_ARGUMENT;
     if (num_units > 2147483647ll) return AQ_ERR_UNSUPPORTED;
     if (num_units == 0) return AQ_OK;
@@ -226,6 +232,8 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens, int32_t 
         return AQ_ERR_INVALID_ARGUMENT;
     if (num_tokens == 0) return AQ_OK;
     if (!kv_f16 || !token_set || !slot_mapping || !codebooks_f16 || !code_pages)
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(kv_f16) || misaligned(codebooks_f16) || misaligned(code_pages))
         return AQ_ERR_INVALID_ARGUMENT;
     EncodeParams p{};
     p.kv = kv_f16;
@@ -292,6 +300,9 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     if (!q || !out || !block_table || !seq_lens) return AQ_ERR_INVALID_ARGUMENT;
     if (fp16 ? !kv_pages : (!code_pages || !codebooks || !req_set)) return AQ_ERR_INVALID_ARGUMENT;
     if (kv_new && !code_pages_w) return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(q) || misaligned(out) || misaligned(code_pages) || misaligned(kv_pages) ||
+        misaligned(kv_new) || misaligned(code_pages_w) || misaligned(codebooks) || misaligned(ws))
+        return AQ_ERR_INVALID_ARGUMENT;
     if (flags & ~AQ_STEP_OVERLAP) return AQ_ERR_INVALID_ARGUMENT;
     if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
     Plan pl{};

@@ -22,6 +22,9 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; arrays are
  *     contiguous and row-major with the shapes given below.  libaqpq never
  *     allocates device memory and keeps no state between calls.
+ *   - The fp16, fp32 and uint8 tensors (vectors, codebooks, code pages,
+ *     queries, outputs, workspace) start on a 16-byte boundary, as every CUDA
+ *     allocation does; a misaligned one returns AQ_ERR_INVALID_ARGUMENT.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *     legacy default stream).  A status other than AQ_OK from argument checks
  *     means nothing was launched.

@@ -111,7 +111,9 @@ void oracle_pq_encode(int64_t n, int D, int M, int K, const float *x,
  *   kv        [T][Hkv][2][D]  (exact fp16 values, as float)
  *   codebooks [S][Hkv][2][M][K][Dsub] (exact fp16 values, as float)
  *   code_pages[NP][Hkv][P][2][M] (written; untouched elsewhere)
- *   gap       [T][Hkv][2][M] or NULL                                       */
+ *   gap       [T][Hkv][2][M] or NULL
+ * A negative slot marks a padding token: it is skipped (its gap entries are
+ * left as they were).                                                      */
 void oracle_encode_append(int T, int Hkv, int D, int M, int K, int P,
                           const float *kv, const int32_t *token_set,
                           const int64_t *slot_mapping, const float *codebooks,
@@ -120,6 +122,7 @@ void oracle_encode_append(int T, int Hkv, int D, int M, int K, int P,
     const size_t cb_stride = (size_t)M * K * Dsub;
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
+        if (slot_mapping[t] < 0) continue;        /* padding token: nothing to store */
         const int64_t page = slot_mapping[t] / P, slot = slot_mapping[t] % P;
         for (int h = 0; h < Hkv; ++h) {
             for (int w = 0; w < 2; ++w) {

@@ -78,6 +78,15 @@ def test_decode_argument_checks(lib):
     assert _decode(lib, _cfg(), max_seq_len=100, splits=3) == WS
 
 
+def test_misaligned_tensors_rejected(lib):
+    odd = ctypes.c_void_p(0x10008)                      # 8-byte but not 16-byte aligned
+    assert _decode(lib, _cfg(), q=odd) == 1
+    cfg = _cfg()
+    assert lib.aq_encode_append(ctypes.byref(cfg), 4, 2, odd, FAKE, FAKE, FAKE, 1, FAKE, 1, None,
+                                None) == 1
+    assert lib.aq_fit_codebooks(ctypes.byref(cfg), 4, 64, 10, FAKE, odd, None, None) == 1
+
+
 def test_fp16_decode_argument_checks(lib):
     cfg = _cfg()
     r = lib.aq_decode_attention_fp16(ctypes.byref(cfg), 2, 4, 4, FAKE, None, 8, FAKE, 8, FAKE, 100,

@@ -226,6 +226,65 @@ def test_encode_prefill_tiles(A, orc):
     _encode_case(A, orc, w, 0, 10**9)
 
 
+def test_encode_prefill_tensor_core_tiles(A, orc):
+    # more than 8192 token-heads: 128-token tiles on the tensor cores; ragged
+    # requests, tiles shared by two requests, a ragged tail
+    w = W.make("ragged", seq_lens=[1000, 333, 65, 700, 129], num_q_heads=8, num_kv_heads=8)
+    assert _encode_case(A, orc, w, 0, 10**9) > 0.99
+    w = W.make("long", seq_lens=[1500, 700], num_q_heads=8, num_kv_heads=8)       # M = 8
+    assert _encode_case(A, orc, w, 0, 10**9) > 0.99
+
+
+def _encode_direct(A, orc, kv, tset, slots, cbs, npages):
+    """Both sides encode the same arrays; every written slot must agree."""
+    Hkv, M = kv.shape[1], cbs.shape[3]
+    want = np.zeros((npages, Hkv, 16, 2, M), np.uint8)
+    orc.encode_append(kv, tset, slots, cbs, want, 16)
+    pages = torch.zeros((npages, Hkv, 16, 2, M), dtype=torch.uint8, device="cuda")
+    st = A.new_status()
+    A.encode_append(dev(kv), dev(tset), dev(slots), dev(cbs), pages, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = pages.cpu().numpy()
+    assert np.array_equal(got, want)
+    return got
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_encode_tensor_core_near_ties(A, orc, M):
+    """Codebooks that defeat any approximate filter: set 0 holds every row four
+    times (as the k-means seeding leaves them), set 1 one row repeated with a
+    one-ulp change in one element per row (all 256 codewords tie to within
+    rounding: the full-scan fallback), set 2 random rows.  Tokens sit on or
+    near codewords, the sets interleave token by token (several passes per
+    tile), some tokens are padding and one has an infinite component."""
+    g = np.random.default_rng(11 + M)
+    T, Hkv, S, Dsub = 1100, 8, 3, 128 // M
+    cbs = g.standard_normal((S, Hkv, 2, M, 256, Dsub)).astype(np.float16)
+    cbs[0] = np.concatenate([cbs[0][..., :64, :]] * 4, axis=-2)
+    one = np.repeat(cbs[1][..., :1, :], 256, axis=-2)
+    bits = one.view(np.uint16)
+    j = g.integers(0, Dsub, size=bits.shape[:-1])
+    np.put_along_axis(bits, j[..., None],
+                      np.take_along_axis(bits, j[..., None], -1) + g.integers(0, 2, j.shape)[..., None]
+                      .astype(np.uint16), -1)
+    cbs[1] = one
+    tset = (np.arange(T) % S).astype(np.int32)
+    pick = g.integers(0, 256, size=(T, Hkv, 2, M))
+    hh = np.arange(Hkv)[None, :, None, None]
+    ww = np.arange(2)[None, None, :, None]
+    mm = np.arange(M)[None, None, None, :]
+    words = cbs[tset[:, None, None, None], hh, ww, mm, pick].astype(np.float32)   # [T][Hkv][2][M][Dsub]
+    noise = g.standard_normal(words.shape).astype(np.float32) * 0.02
+    noise[::7] = 0.0                                       # exactly on a codeword
+    kv = (words + noise).reshape(T, Hkv, 2, 128).astype(np.float16)
+    kv[5, 3, 1, 7] = np.inf
+    npages = (T + 15) // 16 + 3
+    slots = g.permutation(npages * 16)[:T].astype(np.int64)
+    slots[::97] = -1                                       # padding tokens
+    _encode_direct(A, orc, kv, tset, slots, cbs, npages)
+
+
 def test_encode_bad_slots_flagged(A):
     kv = torch.zeros((2, 1, 2, 128), dtype=torch.float16, device="cuda")
     cbs = torch.zeros((1, 1, 2, 4, 256, 32), dtype=torch.float16, device="cuda")

@@ -210,6 +210,25 @@ def test_encode_append_writes_page_slots(orc):
     assert np.all(pages[untouched] == 0xEE)
 
 
+def test_encode_append_skips_padding_tokens(orc):
+    """A negative slot marks a padding token: nothing of it is stored (the
+    boundary's convention), and the other tokens land as usual."""
+    rng = _rng(4)
+    T, H, M, K, P = 4, 1, 4, 256, 16
+    cbs = rng.standard_normal((1, H, 2, M, K, D // M)).astype(np.float16)
+    kv = rng.standard_normal((T, H, 2, D)).astype(np.float16)
+    slots = np.array([-1, 5, -7, 17], np.int64)
+    pages = np.full((2, H, P, 2, M), 0xEE, np.uint8)
+    orc.encode_append(kv, np.zeros(T, np.int32), slots, cbs, pages, P)
+    written = np.zeros(pages.shape[:3], bool)
+    written[0, :, 5] = written[1, :, 1] = True
+    assert np.all(pages[~written] == 0xEE)
+    for t, (pg, sl) in ((1, (0, 5)), (3, (1, 1))):
+        for w_ in range(2):
+            want = orc.pq_encode(kv[t, 0, w_][None], cbs[0, 0, w_])[0]
+            assert list(pages[pg, 0, sl, w_]) == list(want)
+
+
 # --------------------------------------------------------------------------
 # Attention: closed forms and invariants
 # --------------------------------------------------------------------------
