@@ -71,6 +71,63 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor-core peak (TFLOP/s, burst) and where it came from."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def measure_prefill(w, api, torch, base, hbm_peak):
+    """Warm timings of the cache build: the codebook fit on each request's
+    first tokens and the tensor-core encode of every prefill token (the same
+    inputs build_cache used).  The encode reads each K/V vector once and forms
+    its dot products with all 256 codewords of every subspace on the tensor
+    cores (2 x 128 x 256 FLOP per vector), so both bounds are reported."""
+    kvs, bt = base["kvs"], base["bt_np"]
+    Hkv, M = w.num_kv_heads, w.num_subspaces
+    kv = torch.from_numpy(np.concatenate(kvs)).cuda()
+    tset = torch.from_numpy(np.concatenate([np.full(len(k), b, np.int32) for b, k in enumerate(kvs)])).cuda()
+    slots = torch.from_numpy(np.concatenate([w.slot_mapping(bt, b, 0, len(k)) for b, k in enumerate(kvs)])).cuda()
+    samples = np.stack([w.fit_samples(k) for k in kvs])
+    samples_d = torch.from_numpy(samples.reshape(-1, *samples.shape[3:])).cuda()
+    pages = torch.zeros_like(base["pages"])
+    st = api.new_status()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    enc_ms = timed(lambda: api.encode_append(kv, tset, slots, base["codebooks"], pages, st))
+    fit_ms = timed(lambda: api.fit_codebooks(samples_d, M, w.fit_iters))
+    assert int(st.item()) == 0 and torch.equal(pages, base["pages"])
+    T = kv.shape[0]
+    vecs = T * Hkv * 2
+    s = enc_ms / 1e3
+    tf_peak, tf_kind = measured_tensor_peak()
+    gbs = vecs * 128 * 2 / s / 1e9
+    tflops = vecs * 2 * 128 * 256 / s / 1e12
+    return {"fit_ms": fit_ms, "fit_units": int(samples_d.shape[0]), "fit_iters": w.fit_iters,
+            "encode_ms": enc_ms, "encode_tokens": T,
+            "encode_vectors_per_s": vecs / s,
+            "encode_kv_read": {"gbs": gbs, "frac": gbs / hbm_peak},
+            "encode_mma": {"tflops": tflops, "frac": tflops / tf_peak, "peak_kind": tf_kind},
+            "encode_kernel": "encode_mma_kernel (tcgen05)",
+            "cold_first_call_ms": {"fit": base["fit_ms"], "encode": base["encode_prefill_ms"]}}
+
+
 def measured_traffic(workload: str, mode: str):
     """DRAM bytes (read + write) per launch of the decode kernel from one ncu
     capture, recorded in profiles/traffic.json with the SHA-256 of the kernel
@@ -407,6 +464,7 @@ def run_ours(args, w, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist)
+    prefill = measure_prefill(w, api, torch, base, peak)
     # fp16 comparison kernel on the same shape (cache of the same raw vectors)
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
     line = {
@@ -431,7 +489,7 @@ def run_ours(args, w, rank, world, local_rank):
                         "frac_of_peak": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9 / peak},
         "gpu_launches": args.steps * ((2 if args.two_call else 1) + (1 if splits > 1 else 0)),
         "clocks": clk,
-        "prefill": {"fit_ms": base["fit_ms"], "encode_ms": base["encode_prefill_ms"]},
+        "prefill": prefill,
     }
     if e2e:
         line["e2e"] = e2e

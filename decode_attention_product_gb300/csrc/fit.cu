@@ -11,7 +11,10 @@
 //   update  each centroid with members to their mean.  Member sums are formed
 //           exactly: an fp16 value is an integer multiple of 2^-24 below 2^16,
 //           so x * 2^24 is an int64 and sums of up to 1024 of them are exact in
-//           int64 and in double.  The mean is that exact sum divided by the
+//           int64 and in double.  Only centroids with members need a sum row:
+//           each takes a slot of a compact [min(N, K)][Dsub] array, which keeps
+//           the shared memory of a small sample set low enough for several
+//           CTAs per SM.  The mean is that exact sum divided by the
 //           count in double (correctly rounded), then rounded to fp32 for the
 //           next assignment and to fp16 (nearest even) for the codebook.  A
 //           centroid without members keeps both values.
@@ -32,20 +35,16 @@ struct FitCfg {
     static constexpr int CSTR = DSUB + 4;                   // padded fp32 centroid row
     static size_t smem(int n) {
         size_t b = 0;
-        b += static_cast<size_t>(K) * DSUB * 8;             // isum  int64 [K][DSUB]
+        b += static_cast<size_t>(n < K ? n : K) * DSUB * 8;  // isum  int64 [min(N,K)][DSUB]
         b += static_cast<size_t>(K) * CSTR * 4;             // cent  fp32  [K][CSTR]
         b += static_cast<size_t>(K) * DSUB * 2;             // c16   fp16  [K][DSUB]
         b += static_cast<size_t>(n) * DSUB * 2;             // xs    fp16  [N][DSUB]
         b += static_cast<size_t>(n) * 4;                    // assign int  [N]
         b += static_cast<size_t>(K) * 4;                    // cnt   int   [K]
+        b += static_cast<size_t>(K) * 4;                    // slot  int   [K]
         return b + 64;
     }
 };
-
-__device__ __forceinline__ float sqdist_step(float acc, float x, float c) {
-    const float e = __fsub_rn(x, c);
-    return __fadd_rn(acc, __fmul_rn(e, e));
-}
 
 template <int M>
 __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ FitParams p) {
@@ -53,12 +52,15 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
     constexpr int D = F::D, K = F::K, DSUB = F::DSUB, CSTR = F::CSTR;
     extern __shared__ __align__(16) unsigned char smem[];
     const int N = p.n_samples;
+    const int nslot = N < K ? N : K;
     long long *isum = reinterpret_cast<long long *>(smem);
-    float *cent = reinterpret_cast<float *>(isum + K * DSUB);
+    float *cent = reinterpret_cast<float *>(isum + nslot * DSUB);
     __half *c16 = reinterpret_cast<__half *>(cent + K * CSTR);
     __half *xs = c16 + K * DSUB;
     int *asg = reinterpret_cast<int *>(xs + static_cast<size_t>(N) * DSUB);
     int *cnt = asg + N;
+    int *slot = cnt + K;
+    int *nused = slot + K;
 
     const int64_t u = blockIdx.x;
     const int m = blockIdx.y, tid = threadIdx.x;
@@ -89,22 +91,27 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
             const int n = n0 + tid / nch;
             unsigned long long key = ~0ull;
             if (n < N) {
-                float x[DSUB];
+                unsigned long long x2[DSUB / 2];
 #pragma unroll
-                for (int j = 0; j < DSUB; ++j) x[j] = __half2float(xs[n * DSUB + j]);
+                for (int j = 0; j < DSUB; j += 2)
+                    x2[j / 2] = h2_to_f2p(*reinterpret_cast<const uint32_t *>(xs + n * DSUB + j));
                 float best = INFINITY;
                 int bk = 0;
                 for (int i = 0; i < kspan; ++i) {
                     const int k = ch * kspan + ((i + ch) % kspan);   // staggered: no bank conflicts
                     const float4 *c4 = reinterpret_cast<const float4 *>(cent + k * CSTR);
+                    // separately rounded subtract and multiply (pairs), adds in increasing j
                     float d = 0.f;
 #pragma unroll
                     for (int j = 0; j < DSUB; j += 4) {
                         const float4 c = c4[j / 4];
-                        d = sqdist_step(d, x[j], c.x);
-                        d = sqdist_step(d, x[j + 1], c.y);
-                        d = sqdist_step(d, x[j + 2], c.z);
-                        d = sqdist_step(d, x[j + 3], c.w);
+                        const unsigned long long e0 = f2_sub(x2[j / 2], f2_pack(c.x, c.y));
+                        const unsigned long long e1 = f2_sub(x2[j / 2 + 1], f2_pack(c.z, c.w));
+                        const float2 s0 = f2_unpack(f2_mul(e0, e0)), s1 = f2_unpack(f2_mul(e1, e1));
+                        d = __fadd_rn(d, s0.x);
+                        d = __fadd_rn(d, s0.y);
+                        d = __fadd_rn(d, s1.x);
+                        d = __fadd_rn(d, s1.y);
                     }
                     if (d < best || (d == best && k < bk)) { best = d; bk = k; }
                 }
@@ -116,24 +123,30 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
             }
             if (n < N && ch == 0) asg[n] = static_cast<int>(key & 0xffffffffu);
         }
-        for (int i = tid; i < K * DSUB; i += kThreads) isum[i] = 0;
+        for (int i = tid; i < nslot * DSUB; i += kThreads) isum[i] = 0;
         for (int i = tid; i < K; i += kThreads) cnt[i] = 0;
+        if (tid == 0) *nused = 0;
+        __syncthreads();
+        // member counts; the first member of a centroid claims its sum slot
+        for (int n = tid; n < N; n += kThreads) {
+            const int k = asg[n];
+            if (atomicAdd(&cnt[k], 1) == 0) slot[k] = atomicAdd(nused, 1);
+        }
         __syncthreads();
         for (int i = tid; i < N * DSUB; i += kThreads) {
             const int n = i / DSUB, j = i % DSUB;
-            const int k = asg[n];
             // fp16 -> exact int64 multiple of 2^-24
             const long long v = static_cast<long long>(ldexpf(__half2float(xs[i]), 24));
-            atomicAdd(reinterpret_cast<unsigned long long *>(&isum[k * DSUB + j]),
+            atomicAdd(reinterpret_cast<unsigned long long *>(&isum[slot[asg[n]] * DSUB + j]),
                       static_cast<unsigned long long>(v));
-            if (j == 0) atomicAdd(&cnt[k], 1);
         }
         __syncthreads();
         for (int i = tid; i < K * DSUB; i += kThreads) {
             const int k = i / DSUB, j = i % DSUB;
             const int c = cnt[k];
             if (c > 0) {
-                const double mean = __ddiv_rn(ldexp(static_cast<double>(isum[i]), -24), static_cast<double>(c));
+                const double mean = __ddiv_rn(ldexp(static_cast<double>(isum[slot[k] * DSUB + j]), -24),
+                                              static_cast<double>(c));
                 cent[k * CSTR + j] = __double2float_rn(mean);
                 c16[i] = __double2half(mean);
             }
