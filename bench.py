@@ -84,7 +84,7 @@ def measured_tensor_peak():
 def measure_prefill(w, api, torch, base, hbm_peak):
     """Warm timings of the cache build: the codebook fit on each request's
     first tokens and the tensor-core encode of every prefill token (the same
-    inputs build_cache used).  The encode reads each K/V vector once and forms
+    inputs build_cache used), and of one periodic codebook refresh.  The encode reads each K/V vector once and forms
     its dot products with all 256 codewords of every subspace on the tensor
     cores (2 x 128 x 256 FLOP per vector), so both bounds are reported."""
     kvs, bt = base["kvs"], base["bt_np"]
@@ -112,6 +112,12 @@ def measure_prefill(w, api, torch, base, hbm_peak):
 
     enc_ms = timed(lambda: api.encode_append(kv, tset, slots, base["codebooks"], pages, st))
     fit_ms = timed(lambda: api.fit_codebooks(samples_d, M, w.fit_iters))
+    # periodic refresh (every 64 generated tokens): 3 Lloyd steps on the 64 most
+    # recent vectors of every unit, in place on a copy of the codebooks
+    recent = np.stack([w.fit_samples(k[-64:]) for k in kvs])
+    recent_d = torch.from_numpy(recent.reshape(-1, *recent.shape[3:])).cuda()
+    cb_copy = base["codebooks"].reshape(-1, M, 256, w.dsub).clone()
+    refresh_ms = timed(lambda: api.refine_codebooks(recent_d, cb_copy, 3))
     assert int(st.item()) == 0 and torch.equal(pages, base["pages"])
     T = kv.shape[0]
     vecs = T * Hkv * 2
@@ -120,6 +126,7 @@ def measure_prefill(w, api, torch, base, hbm_peak):
     gbs = vecs * 128 * 2 / s / 1e9
     tflops = vecs * 2 * 128 * 256 / s / 1e12
     return {"fit_ms": fit_ms, "fit_units": int(samples_d.shape[0]), "fit_iters": w.fit_iters,
+            "refresh_ms": refresh_ms, "refresh": "3 Lloyd steps on each unit's 64 most recent vectors",
             "encode_ms": enc_ms, "encode_tokens": T,
             "encode_vectors_per_s": vecs / s,
             "encode_kv_read": {"gbs": gbs, "frac": gbs / hbm_peak},

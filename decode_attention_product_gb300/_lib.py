@@ -28,6 +28,7 @@ SIGNATURES = {
     "aq_version": ([], ctypes.c_char_p),
     "aq_fit_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),
     "aq_kmeans_step": ([P, i64, i32, P, P, P, P, P], i32),
+    "aq_refine_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),
     "aq_encode_append": ([P, i32, i32, P, P, P, P, i64, P, i64, P, P], i32),
     "aq_decode_plan": ([P, i32, i32, i32, i32, i32, i32, P, P, P], i32),
     "aq_decode_attention": ([P, i32, i32, i32, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32,

@@ -59,6 +59,25 @@ def fit_codebooks(samples: torch.Tensor, num_subspaces: int, iters: int = 10,
     return (cb, asg) if with_assign else cb
 
 
+def refine_codebooks(samples: torch.Tensor, codebooks: torch.Tensor, iters: int = 3,
+                     with_assign: bool = False):
+    """Periodic codebook update in place: `iters` Lloyd steps on samples [U][N][D]
+    fp16 starting from codebooks [U][M][K][Dsub] fp16 (returns the assignment
+    [U][N][M] of the last step when asked)."""
+    _need(samples, torch.float16, "samples", 3)
+    _need(codebooks, torch.float16, "codebooks", 4)
+    U, N, D = samples.shape
+    M = codebooks.shape[1]
+    if codebooks.shape[0] != U:
+        raise ValueError("one codebook per sample unit")
+    asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
+    cfg = _lib.config(M, head_dim=D)
+    st = _lib.load().aq_refine_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(codebooks),
+                                         _ptr(asg), _stream())
+    _lib.check(st, "aq_refine_codebooks")
+    return asg
+
+
 def kmeans_step(samples: torch.Tensor, centroids: torch.Tensor):
     """One Lloyd step from fp32 centroids [U][M][K][Dsub]: (centroids_out, assign)."""
     _need(samples, torch.float16, "samples", 3)

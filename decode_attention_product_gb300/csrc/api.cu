@@ -197,6 +197,29 @@ aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_t n
     return e == cudaSuccess ? AQ_OK : cuda_fail(e);
 }
 
+aq_status aq_refine_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
+                              int32_t iters, const void *samples_f16, void *codebooks_f16,
+                              int32_t *assign_out, aq_stream_t stream) {
+    aq_status st = check_cfg(cfg, true);
+    if (st != AQ_OK) return st;
+    if (num_units < 0 || n_samples < 1 || iters < 1 || iters > 1000) return AQ_ERR_INVALID_ARGUMENT;
+    if (n_samples > 1024) return AQ_ERR_UNSUPPORTED;
+    if (num_units > 0 && (!samples_f16 || !codebooks_f16)) return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(samples_f16) || misaligned(codebooks_f16)) return AQ_ERR_INVALID_ARGUMENT;
+    if (num_units > 2147483647ll) return AQ_ERR_UNSUPPORTED;
+    if (num_units == 0) return AQ_OK;
+    FitParams p{};
+    p.samples = samples_f16;
+    p.cb_init = codebooks_f16;
+    p.codebooks = codebooks_f16;
+    p.assign = assign_out;
+    p.num_units = num_units;
+    p.n_samples = n_samples;
+    p.iters = iters;
+    cudaError_t e = launch_fit(p, cfg->num_subspaces, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
 aq_status aq_kmeans_step(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
                          const void *samples_f16, const float *centroids_in, float *centroids_out,
                          int32_t *assign_out, aq_stream_t stream) {

@@ -18,7 +18,11 @@
 //           count in double (correctly rounded), then rounded to fp32 for the
 //           next assignment and to fp16 (nearest even) for the codebook.  A
 //           centroid without members keeps both values.
-// Initial centroid k is sample (k mod N).
+// Initial centroid k is sample (k mod N), or (refine) row k of a given codebook:
+// the periodic codebook update of AQPIM blog §6.1 item 3 (a few k-means
+// iterations on recent vectors, starting from the codebook in use).  A CTA
+// reads its own codebook slice before it writes it, so the update may be in
+// place.
 #include "common.cuh"
 #include "internal.h"
 
@@ -72,6 +76,10 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
         const int k = i / DSUB, j = i % DSUB;
         if (p.cent_in) {
             cent[k * CSTR + j] = p.cent_in[cbase + i];
+        } else if (p.cb_init) {                          // refine: start from a codebook
+            const __half h = reinterpret_cast<const __half *>(p.cb_init)[cbase + i];
+            cent[k * CSTR + j] = __half2float(h);
+            c16[i] = h;
         } else {
             const __half h = xs[(k % N) * DSUB + j];
             cent[k * CSTR + j] = __half2float(h);

@@ -45,6 +45,7 @@ struct EncodeParams {
 struct FitParams {
     const void *samples;       // fp16 [U][N][D]
     const float *cent_in;      // fp32 [U][M][K][Dsub] (step) or nullptr (fit)
+    const void *cb_init;       // fp16 [U][M][K][Dsub] starting centroids (refine) or nullptr
     float *cent_out;           // fp32 [U][M][K][Dsub] (step) or nullptr
     void *codebooks;           // fp16 [U][M][K][Dsub] (fit) or nullptr
     int32_t *assign;           // [U][N][M] or nullptr

@@ -117,6 +117,28 @@ aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units,
                            const void *samples_f16, void *codebooks_f16,
                            int32_t *assign_out, aq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * aq_refine_codebooks -- periodic codebook update (AQPIM blog §6.1 item 3:
+ * every so many generated tokens, e.g. 64, fine-tune the codebooks with a few
+ * k-means iterations on the most recent K/V vectors).
+ *
+ * The same `iters` Lloyd steps as aq_fit_codebooks, but centroid k starts as
+ * row k of the given codebook instead of a sample; the result replaces the
+ * codebook in place (a centroid that never gains members keeps its fp16
+ * value bit for bit).  Codes already in the cache keep pointing at the moved
+ * rows; the recent tokens used as samples are re-encoded by calling
+ * aq_encode_append with the refined codebooks.
+ *
+ *   samples_f16   in      fp16 [U][N][D] (the recent vectors of each unit)
+ *   codebooks_f16 in/out  fp16 [U][M][K][Dsub], same unit order as the fit
+ *   assign_out    out     int32 [U][N][M], the assignment of the last step, or NULL
+ * Requires 1 <= n_samples <= 1024, 1 <= iters <= 1000.
+ * ------------------------------------------------------------------------- */
+aq_status aq_refine_codebooks(const aq_pq_config *cfg, int64_t num_units,
+                              int32_t n_samples, int32_t iters,
+                              const void *samples_f16, void *codebooks_f16,
+                              int32_t *assign_out, aq_stream_t stream);
+
 /* One Lloyd step from given fp32 centroids (the step of aq_fit_codebooks,
  * exposed for step-by-step checking).
  *   centroids_in   in  fp32 [U][M][K][Dsub]

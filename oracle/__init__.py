@@ -77,6 +77,7 @@ def _load():
             "oracle_decode_attention": ([i32] * 7 + [P, P, P, P, P, i32, P, dbl, P], None),
             "oracle_decode_attention_fp16": ([i32] * 5 + [P, P, P, i32, P, dbl, P], None),
             "oracle_kmeans_fit": ([i64, i32, i32, i32, i32, i32, P, P, P, P], None),
+            "oracle_kmeans_refine": ([i64, i32, i32, i32, i32, i32, P, P, P, P], None),
             "oracle_kmeans_step": ([i64, i32, i32, i32, i32, P, P, P, P, P], None),
             "oracle_kmeans_distortion": ([i32, i32, i32, i32, i32, P, P], dbl),
         }
@@ -202,6 +203,23 @@ def kmeans_fit(samples, M, K, iters):
     assign = np.zeros((U, N, M), np.int32)
     mg = np.zeros((U, M), np.float32)
     _load().oracle_kmeans_fit(U, D, M, K, N, iters, _p(x), _p(cent), _p(assign), _p(mg))
+    return cent.astype(np.float16), cent, assign, mg
+
+
+def kmeans_refine(samples, codebook16, iters):
+    """Refresh codebooks [U][M][K][Dsub] (fp16 values) with `iters` Lloyd steps on
+    samples [U][N][D], starting from the codebook.
+
+    Returns (codebook_f16, centroids_f64, assign [U][N][M], min_gap [U][M]).
+    """
+    x = _c(samples, np.float32)
+    U, N, D = x.shape
+    cent = _c(np.asarray(codebook16, np.float16), np.float64)
+    _, M, K, Dsub = cent.shape
+    assert cent.shape[0] == U and M * Dsub == D
+    assign = np.zeros((U, N, M), np.int32)
+    mg = np.zeros((U, M), np.float32)
+    _load().oracle_kmeans_refine(U, D, M, K, N, iters, _p(x), _p(cent), _p(assign), _p(mg))
     return cent.astype(np.float16), cent, assign, mg
 
 

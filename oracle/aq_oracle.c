@@ -322,17 +322,12 @@ static void kmeans_one_step(int N, int D, int off, int K, int Dsub,
                 cent[(size_t)k * Dsub + j] = sum[(size_t)k * Dsub + j] / (double)cnt[k];
 }
 
-/* Codebook fit: for every unit u (one request/layer, kv head, K-or-V) and every
- * subspace m, initialise centroid k to sample (k mod N) and run `iters` Lloyd
- * steps.
- *   samples   [U][N][D]   (exact fp16 values, as float)
- *   centroids [U][M][K][Dsub] out, double (the caller rounds to fp16)
- *   assign    [U][N][M] out: the assignment of the last step (iters >= 1)
- *   min_gap   [U][M] out (may be NULL): smallest relative runner-up gap met
- *             in any assignment decision of any step                       */
-void oracle_kmeans_fit(int64_t U, int D, int M, int K, int N, int iters,
-                       const float *samples, double *centroids,
-                       int32_t *assign, float *min_gap) {
+/* Run `iters` Lloyd steps for every unit u and subspace m.  With
+ * from_samples, centroid k starts as sample (k mod N); otherwise it starts as
+ * the value already in `centroids`.                                          */
+static void kmeans_run(int64_t U, int D, int M, int K, int N, int iters, int from_samples,
+                       const float *samples, double *centroids, int32_t *assign,
+                       float *min_gap) {
     const int Dsub = D / M;
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int64_t u = 0; u < U; ++u) {
@@ -345,9 +340,10 @@ void oracle_kmeans_fit(int64_t U, int D, int M, int K, int N, int iters,
             int64_t *cnt = (int64_t *)malloc(sizeof(int64_t) * (size_t)K);
             int32_t *a = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
             float *g = (float *)malloc(sizeof(float) * (size_t)N);
-            for (int k = 0; k < K; ++k)
-                for (int j = 0; j < Dsub; ++j)
-                    cent[(size_t)k * Dsub + j] = (double)x[(size_t)(k % N) * D + (size_t)m * Dsub + j];
+            if (from_samples)
+                for (int k = 0; k < K; ++k)
+                    for (int j = 0; j < Dsub; ++j)
+                        cent[(size_t)k * Dsub + j] = (double)x[(size_t)(k % N) * D + (size_t)m * Dsub + j];
             float mg = INFINITY;
             for (int it = 0; it < iters; ++it) {
                 kmeans_one_step(N, D, m * Dsub, K, Dsub, x, cent, a, g, xs, cf, sum, cnt);
@@ -358,6 +354,32 @@ void oracle_kmeans_fit(int64_t U, int D, int M, int K, int N, int iters,
             free(xs); free(cf); free(sum); free(cnt); free(a); free(g);
         }
     }
+}
+
+/* Codebook fit: for every unit u (one request/layer, kv head, K-or-V) and every
+ * subspace m, initialise centroid k to sample (k mod N) and run `iters` Lloyd
+ * steps.
+ *   samples   [U][N][D]   (exact fp16 values, as float)
+ *   centroids [U][M][K][Dsub] out, double (the caller rounds to fp16)
+ *   assign    [U][N][M] out: the assignment of the last step (iters >= 1)
+ *   min_gap   [U][M] out (may be NULL): smallest relative runner-up gap met
+ *             in any assignment decision of any step                       */
+void oracle_kmeans_fit(int64_t U, int D, int M, int K, int N, int iters,
+                       const float *samples, double *centroids,
+                       int32_t *assign, float *min_gap) {
+    kmeans_run(U, D, M, K, N, iters, 1, samples, centroids, assign, min_gap);
+}
+
+/* Codebook refresh (AQPIM blog §6.1 item 3: a few k-means iterations on the
+ * recent vectors, starting from the codebook in use): the fit's steps with
+ * centroid k starting at row k of the given codebook.
+ *   centroids [U][M][K][Dsub] double, in: the codebook (exact fp16 values),
+ *             out: the refined centroids (the caller rounds to fp16)
+ * other arguments as for oracle_kmeans_fit.                                 */
+void oracle_kmeans_refine(int64_t U, int D, int M, int K, int N, int iters,
+                          const float *samples, double *centroids,
+                          int32_t *assign, float *min_gap) {
+    kmeans_run(U, D, M, K, N, iters, 0, samples, centroids, assign, min_gap);
 }
 
 /* One Lloyd step from given float centroids (the step-parity check).

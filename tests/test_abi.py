@@ -110,6 +110,12 @@ def test_encode_and_fit_argument_checks(lib):
     assert lib.aq_fit_codebooks(ctypes.byref(cfg), 4, 64, 0, FAKE, FAKE, None, None) == 1
     assert lib.aq_fit_codebooks(ctypes.byref(cfg), 0, 64, 10, None, None, None, None) == 0
     assert lib.aq_kmeans_step(ctypes.byref(cfg), 4, 64, FAKE, FAKE, FAKE, None, None) == 1
+    assert lib.aq_refine_codebooks(ctypes.byref(cfg), 4, 64, 0, FAKE, FAKE, None, None) == 1   # iters
+    assert lib.aq_refine_codebooks(ctypes.byref(cfg), 4, 2048, 3, FAKE, FAKE, None, None) == 2
+    assert lib.aq_refine_codebooks(ctypes.byref(cfg), 4, 64, 3, None, FAKE, None, None) == 1
+    assert lib.aq_refine_codebooks(ctypes.byref(cfg), 4, 64, 3, FAKE, ctypes.c_void_p(0x10008), None,
+                                   None) == 1                          # misaligned codebooks
+    assert lib.aq_refine_codebooks(ctypes.byref(cfg), 0, 64, 3, None, None, None, None) == 0
 
 
 def _plan(lib, B, Hq, Hkv, L, M=4, splits=0, fp16=0):

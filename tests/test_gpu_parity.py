@@ -329,6 +329,35 @@ def test_kmeans_step_matches_oracle(A, orc):
     assert np.array_equal(c_g.cpu().numpy(), c_o.astype(np.float32))
 
 
+@pytest.mark.parametrize("name", ["page1", "long"])
+def test_refine_matches_oracle(A, orc, name):
+    """Periodic codebook refresh: codebooks fitted on tokens [0, 64) of each
+    request, refined in place on tokens [64, 128) for 3 steps; codebooks and
+    assignments bit-exact, then the 64 recent tokens re-encode identically."""
+    w = W.make(name, seq_lens=[256, 256]) if name == "long" else W.make(name)
+    M, Hkv = w.num_subspaces, w.num_kv_heads
+    B = 2
+    first = np.concatenate([np.ascontiguousarray(w.kv(b, t1=64).transpose(1, 2, 0, 3)).reshape(-1, 64, 128)
+                            for b in range(B)])
+    recent_kv = [w.kv(b, t0=64, t1=128) for b in range(B)]
+    recent = np.concatenate([np.ascontiguousarray(k.transpose(1, 2, 0, 3)).reshape(-1, 64, 128)
+                             for k in recent_kv])
+    cb16, _, _, _ = orc.kmeans_fit(first, M, 256, 10)
+    cb_ref, _, asg_ref, _ = orc.kmeans_refine(recent, cb16, 3)
+    cb_gpu = dev(cb16)
+    asg_gpu = A.refine_codebooks(dev(recent), cb_gpu, 3, with_assign=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(asg_gpu.cpu().numpy(), asg_ref)
+    assert np.array_equal(cb_gpu.cpu().numpy().view(np.uint16), cb_ref.view(np.uint16))
+    assert not np.array_equal(cb_ref.view(np.uint16), cb16.view(np.uint16))   # it did move
+    # re-encode the recent tokens with the refreshed codebooks
+    cbs = cb_ref.reshape(B, Hkv, 2, M, 256, 128 // M)
+    kv = np.concatenate(recent_kv)
+    tset = np.repeat(np.arange(B, dtype=np.int32), 64)
+    slots = np.arange(B * 64, dtype=np.int64)
+    _encode_direct(A, orc, kv, tset, slots, cbs, (B * 64) // 16)
+
+
 # --------------------------------------------------------------------------
 # fused decode step (append the token at position seq_len-1, then attend)
 # --------------------------------------------------------------------------

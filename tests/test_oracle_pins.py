@@ -508,6 +508,60 @@ def test_kmeans_step_continues_fit(orc):
     assert np.allclose(c, c4, rtol=1e-15, atol=0)
 
 
+def test_kmeans_refine_closed_forms(orc):
+    """Refresh from a given codebook (AQPIM blog §6.1 item 3).  1-D, K = 4:
+    rows at -1 and 12 pull the two clumps and land on their exact means; rows
+    at 100 (twice) get no members and keep their value; from four identical
+    rows every sample ties onto row 0, which becomes the mean of all."""
+    left = [0.5, -0.25, 0.0, 0.125, 1.0]
+    right = [10.0, 9.5, 11.25, 10.5]
+    samples = np.array(left + right, np.float16).reshape(1, -1, 1).repeat(2, axis=2)   # D=2, M=2
+    start = np.array([-1.0, 12.0, 100.0, 100.0], np.float16).reshape(1, 1, 4, 1).repeat(2, axis=1)
+    for iters in (1, 3):
+        cb16, cent, assign, _ = orc.kmeans_refine(samples, start, iters)
+        for m in range(2):
+            assert cent[0, m, 0, 0] == float(sum(Fraction(v) for v in left) / len(left))
+            assert cent[0, m, 1, 0] == float(sum(Fraction(v) for v in right) / len(right))
+            assert cent[0, m, 2, 0] == 100.0 and cent[0, m, 3, 0] == 100.0
+            assert list(assign[0, :, m]) == [0] * 5 + [1] * 4
+    same = np.full((1, 2, 4, 1), 5.0, np.float16)
+    _, cent, assign, _ = orc.kmeans_refine(samples, same, 1)
+    assert np.all(assign == 0)
+    assert cent[0, 0, 0, 0] == float(sum(Fraction(v) for v in left + right) / 9)
+    assert np.all(cent[0, :, 1:, 0] == 5.0)
+
+
+def test_kmeans_refine_from_the_seeding_is_the_fit(orc):
+    """Starting from the fit's own seeding (row k = sample k mod N, exact fp16),
+    the refresh runs exactly the fit's steps."""
+    rng = _rng(46)
+    U, N, M, K = 2, 300, 4, 32
+    samples = rng.standard_normal((U, N, D)).astype(np.float16)
+    seed = np.stack([samples[:, np.arange(K) % N, m * (D // M):(m + 1) * (D // M)] for m in range(M)], axis=1)
+    for iters in (1, 4):
+        cf, cent_f, a_f, g_f = orc.kmeans_fit(samples, M=M, K=K, iters=iters)
+        cr, cent_r, a_r, g_r = orc.kmeans_refine(samples, seed, iters)
+        assert np.array_equal(cent_f, cent_r) and np.array_equal(a_f, a_r)
+        assert np.array_equal(cf.view(np.uint16), cr.view(np.uint16))
+
+
+def test_kmeans_refine_distortion_never_increases(orc):
+    """Lloyd's objective on the recent samples never rises from the starting
+    codebook on."""
+    rng = _rng(47)
+    N, M, K = 400, 4, 16
+    centres = rng.standard_normal((8, D)) * 2
+    samples = (centres[rng.integers(0, 8, N)] + 0.5 * rng.standard_normal((N, D))).astype(np.float16)[None]
+    start = rng.standard_normal((1, M, K, D // M)).astype(np.float16)
+    prev = [orc.kmeans_distortion(samples[0], start[0, m].astype(np.float64), M, m) for m in range(M)]
+    for it in range(1, 7):
+        _, cent, _, _ = orc.kmeans_refine(samples, start, it)
+        for m in range(M):
+            d = orc.kmeans_distortion(samples[0], cent[0, m], M, m)
+            assert d <= prev[m] * (1 + 1e-6)
+            prev[m] = d
+
+
 def test_kmeans_update_is_member_mean(orc):
     """After a step, each non-empty centroid is the exact mean of the samples
     assigned to it and empty ones keep their input value."""
