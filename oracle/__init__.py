@@ -80,6 +80,8 @@ def _load():
             "oracle_kmeans_refine": ([i64, i32, i32, i32, i32, i32, P, P, P, P], None),
             "oracle_kmeans_step": ([i64, i32, i32, i32, i32, P, P, P, P, P], None),
             "oracle_kmeans_distortion": ([i32, i32, i32, i32, i32, P, P], dbl),
+            "oracle_e4m3_from_float": ([i64, P, P], None),
+            "oracle_e4m3_to_float": ([i64, P, P], None),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -188,6 +190,25 @@ def decode_attention_fp16(q, kv_pages, block_table, seq_lens, scale):
         B, Hq, Hkv, D, P, _p(q), _p(kvp), _p(bt), bt.shape[1],
         _p(_c(seq_lens, np.int32)), scale, _p(out))
     return out
+
+
+def e4m3_from_float(x):
+    """FP8 E4M3 codes (uint8, same shape) of x: nearest, ties to even, |x| > 448
+    saturated, NaN -> 0x7F."""
+    x = np.asarray(x, np.float32)
+    xc = _c(x.reshape(-1), np.float32)
+    out = np.zeros(xc.shape, np.uint8)
+    _load().oracle_e4m3_from_float(xc.size, _p(xc), _p(out))
+    return out.reshape(x.shape)
+
+
+def e4m3_to_float(codes):
+    """Values (float32, same shape) of FP8 E4M3 codes."""
+    c = np.asarray(codes, np.uint8)
+    cc = _c(c.reshape(-1), np.uint8)
+    out = np.zeros(cc.shape, np.float32)
+    _load().oracle_e4m3_to_float(cc.size, _p(cc), _p(out))
+    return out.reshape(c.shape)
 
 
 def kmeans_fit(samples, M, K, iters):

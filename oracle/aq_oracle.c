@@ -142,6 +142,49 @@ void oracle_encode_append(int T, int Hkv, int D, int M, int K, int P,
     }
 }
 
+/* FP8 E4M3 codebook storage (AQPIM blog §4.2: codebooks kept in a low-precision
+ * float such as FP8).  The OCP E4M3 format: 1 sign bit, 4 exponent bits (bias
+ * 7), 3 fraction bits; exponent field 0 holds the subnormals m * 2^-9; no
+ * infinities; S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 * 2^8 = 448.
+ * Value of one code.                                                         */
+static double e4m3_value(uint8_t b) {
+    const int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest code, ties to the even fraction, magnitudes beyond 448 (and
+ * infinities) saturated to 448; NaN gives 0x7F.                              */
+static uint8_t e4m3_round(double x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t s = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a == 0.0) return s;        /* +0 / -0 */
+    if (a >= 448.0) return s | 0x7E;
+    int e;
+    frexp(a, &e);                  /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                        /* a in [2^e, 2^(e+1)) */
+    if (e < -6) e = -6;            /* subnormal spacing below 2^-6 */
+    double q = nearbyint(ldexp(a, 3 - e));   /* units of 2^(e-3), half to even */
+    if (q >= 16.0) { q = 8.0; e += 1; }      /* rounded up into the next binade */
+    if (e == -6 && q < 8.0) return s | (uint8_t)q;          /* subnormal (or zero) */
+    const int code = ((e + 7) << 3) | ((int)q - 8);
+    if (code > 0x7E) return s | 0x7E;        /* 480 would be the NaN pattern */
+    return s | (uint8_t)code;
+}
+
+void oracle_e4m3_from_float(int64_t n, const float *x, uint8_t *codes) {
+    for (int64_t i = 0; i < n; ++i) codes[i] = e4m3_round((double)x[i]);
+}
+
+void oracle_e4m3_to_float(int64_t n, const uint8_t *codes, float *x) {
+    for (int64_t i = 0; i < n; ++i) x[i] = (float)e4m3_value(codes[i]);
+}
+
 /* Reconstruction: x̂[m*Dsub + j] = C_m[c_m][j].  AQPIM blog §3.1 ("take the
  * codeword each index points to and concatenate").                          */
 void oracle_pq_reconstruct(int64_t n, int D, int M, int K, const double *cb,

@@ -432,6 +432,70 @@ def test_decode_attention_special_lengths(orc):
 
 
 # --------------------------------------------------------------------------
+# FP8 E4M3 codebook storage (AQPIM blog §4.2)
+# --------------------------------------------------------------------------
+def _e4m3_table():
+    """Every finite E4M3 magnitude with its code (0..0x7E), from the format's
+    definition: exponent field e (bias 7), fraction m/8, e = 0 subnormal."""
+    vals, codes = [], []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue                                  # the NaN pattern
+            vals.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+            codes.append((e << 3) | m)
+    return np.array(vals), np.array(codes)
+
+
+def test_e4m3_code_values(orc):
+    got = orc.e4m3_to_float(np.array([0x38, 0x7E, 0x01, 0x08, 0x07, 0x3F, 0x40, 0x80, 0xFE, 0x7F, 0xFF],
+                                     np.uint8))
+    assert list(got[:7]) == [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, 7 * 2.0 ** -9, 1.875, 2.0]
+    assert got[7] == 0.0 and np.signbit(got[7]) and got[8] == -448.0
+    assert np.isnan(got[9]) and np.isnan(got[10])
+
+
+def test_e4m3_rounding_by_hand(orc):
+    x = np.array([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, 447.9, 460.0, 470.0, 1e4, -1e4, np.inf,
+                  -0.0, 0.09375], np.float32)
+    want = [0x38,   # halfway 1 / 1.125: even fraction
+            0x3A,   # halfway 1.125 / 1.25: even fraction (1.25)
+            0x00,   # halfway 0 / 2^-9
+            0x02,   # halfway 2^-9 / 2^-8
+            0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E,   # 448 and saturation
+            0x80,   # -0 keeps its sign
+            0x1C]   # 0.09375 = 1.5 * 2^-4 exactly
+    assert [int(v) for v in orc.e4m3_from_float(x)] == want
+    assert orc.e4m3_from_float(np.array([np.nan], np.float32))[0] == 0x7F
+
+
+def test_e4m3_every_code_round_trips(orc):
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    assert np.array_equal(orc.e4m3_from_float(orc.e4m3_to_float(codes)), codes)
+
+
+def test_e4m3_rounding_exhaustive_over_fp16(orc):
+    """Every finite fp16 value goes to the nearest E4M3 value (brute force over
+    the format's table), ties to the even code, magnitudes beyond 448
+    saturated; the sign is kept."""
+    h = np.arange(65536, dtype=np.uint16).view(np.float16)
+    h = h[np.isfinite(h)]
+    x = h.astype(np.float64)
+    vals, codes = _e4m3_table()
+    a = np.abs(x)
+    dist = np.abs(a[:, None] - vals[None, :])
+    best = dist.min(1, keepdims=True)
+    tied = dist == best
+    # among the nearest, the even code (at most two candidates)
+    pick = np.where(tied & (codes[None, :] % 2 == 0), 1, 0) + tied
+    want = codes[pick.argmax(1)]
+    want = np.where(a >= 448.0, 0x7E, want)
+    want = want | np.where(np.signbit(x), 0x80, 0)
+    got = orc.e4m3_from_float(h.astype(np.float32))
+    assert np.array_equal(got.astype(np.int64), want.astype(np.int64))
+
+
+# --------------------------------------------------------------------------
 # k-means
 # --------------------------------------------------------------------------
 def test_kmeans_two_clumps_closed_form(orc):
