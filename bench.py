@@ -474,6 +474,7 @@ def run_ours(args, w, rank, world, local_rank):
     prefill = measure_prefill(w, api, torch, base, peak)
     # fp16 comparison kernel on the same shape (cache of the same raw vectors)
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
+    e4m3 = None if args.two_call else measure_e4m3(args, w, api, torch, base, Lmax, units, T)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -502,6 +503,8 @@ def run_ours(args, w, rank, world, local_rank):
         line["e2e"] = e2e
     if fp16:
         line["fp16_comparison"] = fp16
+    if e4m3:
+        line["e4m3_codebooks"] = e4m3
     if rank == 0 and not args.no_cpu:
         ost = OracleStep(w)
         units_c, secs_c, n_c = ost.run(args.cpu_budget)
@@ -594,6 +597,53 @@ def measure_fp16(args, w, api, torch, base, Lmax, units, T):
     return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_call": ms,
             "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
             "splits": splits}
+
+
+def measure_e4m3(args, w, api, torch, base, Lmax, units, T):
+    """The fused step with the same codebooks stored as FP8 E4M3 codes (half
+    the codebook bytes; AQPIM blog §4.2), timed like the main step: graph
+    replays over rotated copies of codebooks and pages larger than 2 x L2."""
+    Hq, Hkv, M = w.num_q_heads, w.num_kv_heads, w.num_subspaces
+    cb8 = api.to_e4m3(base["codebooks"])
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    per = cb8.numel() + base["pages"].numel()
+    R = max(1, min(16, math.ceil(2.2 * l2 / per)))
+    books = [cb8] + [cb8.clone() for _ in range(R - 1)]
+    pages = [base["pages"].clone() for _ in range(R)]
+    splits, _, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
+    st = api.new_status()
+
+    def step(i):
+        api.decode_step(base["q"], base["new_kv"], pages[i % R], books[i % R], base["req_set"], base["bt"],
+                        base["seq_lens"], Lmax, w.scale, overlap=R > 1, out=out, workspace=ws, status=st)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(R):
+            step(i)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(2, -(-max(10, args.steps) // R))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ms = e0.elapsed_time(e1) / (reps * R)
+    byt = T.pq_step_bytes_e4m3(w.seq_lens, Hq, Hkv, M)
+    peak, _ = measured_peaks()
+    del books, pages
+    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "bytes_per_step": byt["total"],
+            "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
+            "codebooks": "FP8 E4M3 (same codebooks, rounded to nearest even)"}
 
 
 def main():

@@ -18,6 +18,7 @@ STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARGUMENT", 2: "AQ_ERR_UNSUPPORTED
                 3: "AQ_ERR_WORKSPACE_TOO_SMALL", 4: "AQ_ERR_CUDA"}
 DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_SET, DEV_TIMEOUT = 1, 2, 4, 8
 STEP_OVERLAP = 1
+STEP_E4M3 = 2
 
 # every symbol include/aqpq.h declares, with its ctypes signature
 P = ctypes.c_void_p
@@ -29,6 +30,8 @@ SIGNATURES = {
     "aq_fit_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),
     "aq_kmeans_step": ([P, i64, i32, P, P, P, P, P], i32),
     "aq_refine_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),
+    "aq_codebooks_to_e4m3": ([i64, P, P, P], i32),
+    "aq_codebooks_from_e4m3": ([i64, P, P, P], i32),
     "aq_encode_append": ([P, i32, i32, P, P, P, P, i64, P, i64, P, P], i32),
     "aq_decode_plan": ([P, i32, i32, i32, i32, i32, i32, P, P, P], i32),
     "aq_decode_attention": ([P, i32, i32, i32, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32,

@@ -78,6 +78,25 @@ def refine_codebooks(samples: torch.Tensor, codebooks: torch.Tensor, iters: int 
     return asg
 
 
+def to_e4m3(x: torch.Tensor) -> torch.Tensor:
+    """FP8 E4M3 codes (uint8, same shape) of an fp16 tensor (nearest, ties to
+    even, saturating)."""
+    _need(x, torch.float16, "x")
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    st = _lib.load().aq_codebooks_to_e4m3(x.numel(), _ptr(x), _ptr(out), _stream())
+    _lib.check(st, "aq_codebooks_to_e4m3")
+    return out
+
+
+def from_e4m3(codes: torch.Tensor) -> torch.Tensor:
+    """The exact fp16 values (same shape) of FP8 E4M3 codes."""
+    _need(codes, torch.uint8, "codes")
+    out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device)
+    st = _lib.load().aq_codebooks_from_e4m3(codes.numel(), _ptr(codes), _ptr(out), _stream())
+    _lib.check(st, "aq_codebooks_from_e4m3")
+    return out
+
+
 def kmeans_step(samples: torch.Tensor, centroids: torch.Tensor):
     """One Lloyd step from fp32 centroids [U][M][K][Dsub]: (centroids_out, assign)."""
     _need(samples, torch.float16, "samples", 3)
@@ -169,11 +188,13 @@ def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
                 status: torch.Tensor | None = None) -> torch.Tensor:
     """Fused decode step: append kv_new [B][Hkv][2][D] fp16 (the token at
     position seq_lens[b]-1) to code_pages, then PQ decode attention over all
-    seq_lens[b] tokens; returns out [B][Hq][D] fp32."""
+    seq_lens[b] tokens; returns out [B][Hq][D] fp32.  Codebooks are fp16, or
+    uint8 FP8 E4M3 codes (to_e4m3) for half the codebook bytes."""
     _need(q, torch.float32, "q", 3)
     _need(kv_new, torch.float16, "kv_new", 4)
     _need(code_pages, torch.uint8, "code_pages", 5)
-    _need(codebooks, torch.float16, "codebooks", 6)
+    e4m3 = codebooks.dtype == torch.uint8
+    _need(codebooks, torch.uint8 if e4m3 else torch.float16, "codebooks", 6)
     _need(req_set, torch.int32, "req_set", 1)
     _need(block_table, torch.int32, "block_table", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
@@ -189,7 +210,8 @@ def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
     st = _lib.load().aq_decode_step(
         ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_new), _ptr(code_pages), code_pages.shape[0],
         _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), max_seq_len, float(scale), num_splits, _lib.STEP_OVERLAP if overlap else 0,
+        _ptr(seq_lens), max_seq_len, float(scale), num_splits,
+        (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0),
         _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status),
         _stream())
     _lib.check(st, "aq_decode_step")

@@ -220,6 +220,22 @@ aq_status aq_refine_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_
     return e == cudaSuccess ? AQ_OK : cuda_fail(e);
 }
 
+aq_status aq_codebooks_to_e4m3(int64_t n, const void *src_f16, uint8_t *dst_e4m3, aq_stream_t stream) {
+    if (n < 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (n == 0) return AQ_OK;
+    if (!src_f16 || !dst_e4m3 || misaligned(src_f16) || misaligned(dst_e4m3)) return AQ_ERR_INVALID_ARGUMENT;
+    cudaError_t e = launch_to_e4m3(n, src_f16, dst_e4m3, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
+aq_status aq_codebooks_from_e4m3(int64_t n, const uint8_t *src_e4m3, void *dst_f16, aq_stream_t stream) {
+    if (n < 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (n == 0) return AQ_OK;
+    if (!src_e4m3 || !dst_f16 || misaligned(src_e4m3) || misaligned(dst_f16)) return AQ_ERR_INVALID_ARGUMENT;
+    cudaError_t e = launch_from_e4m3(n, src_e4m3, dst_f16, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
 aq_status aq_kmeans_step(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
                          const void *samples_f16, const float *centroids_in, float *centroids_out,
                          int32_t *assign_out, aq_stream_t stream) {
@@ -326,7 +342,8 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     if (misaligned(q) || misaligned(out) || misaligned(code_pages) || misaligned(kv_pages) ||
         misaligned(kv_new) || misaligned(code_pages_w) || misaligned(codebooks) || misaligned(ws))
         return AQ_ERR_INVALID_ARGUMENT;
-    if (flags & ~AQ_STEP_OVERLAP) return AQ_ERR_INVALID_ARGUMENT;
+    if (flags & ~(AQ_STEP_OVERLAP | AQ_STEP_E4M3)) return AQ_ERR_INVALID_ARGUMENT;
+    if ((flags & AQ_STEP_E4M3) && (fp16 || !kv_new)) return AQ_ERR_INVALID_ARGUMENT;
     if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
     Plan pl{};
     st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl);
@@ -360,6 +377,7 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.kv_new = kv_new;
     p.code_pages_w = code_pages_w;
     p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
+    p.codebook_e4m3 = (flags & AQ_STEP_E4M3) ? 1 : 0;
     p.head_split_log2 = 0;
     while ((1 << p.head_split_log2) < pl.head_split) ++p.head_split_log2;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -59,6 +59,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// Arrive once on `bar` (release: this thread's earlier shared-memory writes
+// are visible to whoever waits for the phase).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Test phase `parity` of `bar`; a thread whose phase is still open is
 // suspended (up to kSuspendHintNs) until it completes instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {

@@ -31,6 +31,8 @@
 // codebook rows it already holds in registers), scores it from its fresh
 // codes, adds it to the value bins after the merge and writes its codes to
 // its page slot.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -134,6 +136,45 @@ __device__ __forceinline__ void copy_slice(__half *dst, const __half *src, uint6
     cp_async_mbar_arrive(bar);
 }
 
+// The same slice from FP8 E4M3 codebooks (one byte per element, same element
+// order): 8-byte loads widened exactly to fp16 and stored in the same layout,
+// then one plain arrival per thread on `bar`.
+template <int DSUB, int CHUNKS>
+__device__ __forceinline__ void copy_slice_e4m3(__half *dst, const uint8_t *src, uint64_t *bar) {
+    constexpr int NCH = DSUB / 8, NI = CHUNKS / kThreads;
+    const int t = static_cast<int>(threadIdx.x);
+    const int r0 = t / NCH, c = t % NCH;
+    const uint32_t d0 = smem_u32(dst) + static_cast<uint32_t>(r0 * NCH + chunk_pos<DSUB>(r0, c)) * 16u;
+    const uint8_t *s0 = src + static_cast<size_t>(t) * 8;
+    uint2 raw[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) raw[i] = ldg_stream_v2(s0 + static_cast<size_t>(i) * kThreads * 8);
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const uint32_t w[4] = {raw[i].x & 0xffffu, raw[i].x >> 16, raw[i].y & 0xffffu, raw[i].y >> 16};
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[j]), __NV_E4M3);
+            h[j] = static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d0 + static_cast<uint32_t>(i * kThreads * 16)),
+                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                     : "memory");
+    }
+    mbar_arrive(bar);
+}
+
+// A codebook slice of `elems` elements from offset `off` of the codebook array
+// (fp16 or, with E4M3, FP8 codes) into the swizzled fp16 layout.
+template <int DSUB, int CHUNKS, bool E4M3>
+__device__ __forceinline__ void copy_codebook_slice(__half *dst, const void *codebooks, size_t off, uint64_t *bar) {
+    if constexpr (E4M3)
+        copy_slice_e4m3<DSUB, CHUNKS>(dst, static_cast<const uint8_t *>(codebooks) + off, bar);
+    else
+        copy_slice<DSUB, CHUNKS>(dst, static_cast<const __half *>(codebooks) + off, bar);
+}
+
 template <int N>
 __device__ __forceinline__ void store_vec(float *dst, const float (&v)[N]) {
     if constexpr (N % 4 == 0) {
@@ -228,7 +269,7 @@ __device__ __forceinline__ void warp_argmin_into(float d, unsigned long long *sl
         atomicMin(slot, (static_cast<unsigned long long>(mn) << 32) | threadIdx.x);
 }
 
-template <int M, int G, int C, bool APPEND>
+template <int M, int G, int C, bool APPEND, bool E4M3>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
     constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT, NCH = S::NCH;
@@ -296,12 +337,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     }
     const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
     const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
-    const __half *gK = reinterpret_cast<const __half *>(p.codebooks) +
-                       ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
-                       static_cast<size_t>(rank) * S::CB_HALVES;
+    // element offset of this CTA's K slice (the V slice is cb_unit further)
+    const size_t gK = ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
+                      static_cast<size_t>(rank) * S::CB_HALVES;
     // the K slice now; the V slice, needed only after the scores, once the K
     // slice has landed (own buffer) or is no longer read (shared buffer)
-    if (set_ok) copy_slice<DSUB, S::CB_CHUNKS>(cbk, gK, &bar[0]);
+    if (set_ok) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, gK, &bar[0]);
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -391,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
     // new token's K and V codes from the same rows --------------------------
     bool tmo = !mbar_wait_bounded(&bar[0], 0);
-    if constexpr (!S::SHARED_CB) copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
+    if constexpr (!S::SHARED_CB) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
     tmo |= !mbar_wait_bounded(&bar[4], 0);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
@@ -441,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
     __syncthreads();                                   // every read of the K slice is done
-    if constexpr (S::SHARED_CB) copy_slice<DSUB, S::CB_CHUNKS>(cbv, gK + cb_unit, &bar[1]);
+    if constexpr (S::SHARED_CB) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
     if constexpr (C > 1) {
         // this CTA's rows to every peer in one bulk copy each; the source is not
         // written again before every peer has received it (each peer scores,
@@ -808,10 +849,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     p.out[bh * kHeadDim + d] = nan ? __int_as_float(0x7fc00000) : (den > 0.f ? num / den : 0.f);
 }
 
-template <int M, int G, int C, bool APPEND>
+template <int M, int G, int C, bool APPEND, bool E4M3>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
-    auto kern = pq_decode_kernel<M, G, C, APPEND>;
+    auto kern = pq_decode_kernel<M, G, C, APPEND, E4M3>;
     if (plan.share > S::MAX_SHARE || plan.share % kPage) return cudaErrorInvalidValue;
     static size_t attr_bytes = 0;                  // opt-in dynamic shared memory set so far
     const size_t need = S::smem();
@@ -840,26 +881,26 @@ cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) 
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int M, int G, bool APPEND>
+template <int M, int G, bool APPEND, bool E4M3>
 cudaError_t dispatch_c(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     switch (plan.cluster) {
-        case 1: return launch_one<M, G, 1, APPEND>(p, plan, s);
-        case 2: return launch_one<M, G, 2, APPEND>(p, plan, s);
-        case 4: return launch_one<M, G, 4, APPEND>(p, plan, s);
+        case 1: return launch_one<M, G, 1, APPEND, E4M3>(p, plan, s);
+        case 2: return launch_one<M, G, 2, APPEND, E4M3>(p, plan, s);
+        case 4: return launch_one<M, G, 4, APPEND, E4M3>(p, plan, s);
         case 8:                                    // one subspace per CTA
-            if constexpr (M == 8) return launch_one<M, G, 8, APPEND>(p, plan, s);
+            if constexpr (M == 8) return launch_one<M, G, 8, APPEND, E4M3>(p, plan, s);
             else return cudaErrorInvalidConfiguration;
         default: return cudaErrorInvalidConfiguration;
     }
 }
 
-template <int M, bool APPEND>
+template <int M, bool APPEND, bool E4M3>
 cudaError_t dispatch_g(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s) {
     switch (G) {
-        case 1: return dispatch_c<M, 1, APPEND>(p, plan, s);
-        case 2: return dispatch_c<M, 2, APPEND>(p, plan, s);
-        case 4: return dispatch_c<M, 4, APPEND>(p, plan, s);
-        case 8: return dispatch_c<M, 8, APPEND>(p, plan, s);
+        case 1: return dispatch_c<M, 1, APPEND, E4M3>(p, plan, s);
+        case 2: return dispatch_c<M, 2, APPEND, E4M3>(p, plan, s);
+        case 4: return dispatch_c<M, 4, APPEND, E4M3>(p, plan, s);
+        case 8: return dispatch_c<M, 8, APPEND, E4M3>(p, plan, s);
         default: return cudaErrorInvalidConfiguration;
     }
 }
@@ -902,8 +943,9 @@ int pq_decode_max_share(int M, int G) {
 cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
     G /= plan.head_split;                          // query heads per cluster
-    if (M == 4) e = dispatch_g<4, false>(p, G, plan, s);
-    else if (M == 8) e = dispatch_g<8, false>(p, G, plan, s);
+    if (p.codebook_e4m3) return cudaErrorInvalidValue;          // E4M3 codebooks: the fused step only
+    if (M == 4) e = dispatch_g<4, false, false>(p, G, plan, s);
+    else if (M == 8) e = dispatch_g<8, false, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     if (plan.num_splits > 1) return launch_combine(p, s);
@@ -913,8 +955,8 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
 cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
     G /= plan.head_split;
-    if (M == 4) e = dispatch_g<4, true>(p, G, plan, s);
-    else if (M == 8) e = dispatch_g<8, true>(p, G, plan, s);
+    if (M == 4) e = p.codebook_e4m3 ? dispatch_g<4, true, true>(p, G, plan, s) : dispatch_g<4, true, false>(p, G, plan, s);
+    else if (M == 8) e = p.codebook_e4m3 ? dispatch_g<8, true, true>(p, G, plan, s) : dispatch_g<8, true, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     if (plan.num_splits > 1) return launch_combine(p, s);

@@ -28,6 +28,7 @@ struct DecodeParams {
     uint8_t *code_pages_w;  // writable alias of code_pages (fused decode step)
     int32_t overlap;        // launched as a programmatic dependent of the previous kernel
     int32_t head_split_log2;  // PQ: 2^this clusters per kv head, each for Hq/Hkv >> this query heads
+    int32_t codebook_e4m3;    // PQ step: codebooks are FP8 E4M3 codes, same layout
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -73,6 +74,8 @@ cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Pla
 cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
+cudaError_t launch_to_e4m3(int64_t n, const void *src_f16, uint8_t *dst, cudaStream_t s);
+cudaError_t launch_from_e4m3(int64_t n, const uint8_t *src, void *dst_f16, cudaStream_t s);
 cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s);
 
 // Shared-memory bytes a PQ decode CTA needs for (M, G, cluster).

@@ -70,6 +70,17 @@ def pq_decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int, num_subspaces
             "code_stream": codes + books + pages * INT32, "total": total}
 
 
+def pq_step_bytes_e4m3(seq_lens, num_q_heads: int, num_kv_heads: int, num_subspaces: int,
+                       head_dim: int = 128, num_codewords: int = 256, page_size: int = 16) -> dict:
+    """Bytes of one fused decode step whose codebooks are stored as FP8 E4M3
+    (one byte per element instead of two)."""
+    d = pq_step_bytes(seq_lens, num_q_heads, num_kv_heads, num_subspaces, head_dim, num_codewords,
+                      page_size)
+    half = d["codebooks"] // 2
+    return dict(d, codebooks=d["codebooks"] - half, code_stream=d["code_stream"] - half,
+                total=d["total"] - half)
+
+
 def fp16_decode_bytes(seq_lens, num_q_heads: int, num_kv_heads: int,
                       head_dim: int = 128, page_size: int = 16) -> dict:
     """Bytes one fp16 decode-attention call must move (the uncompressed cache)."""

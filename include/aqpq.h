@@ -139,6 +139,25 @@ aq_status aq_refine_codebooks(const aq_pq_config *cfg, int64_t num_units,
                               const void *samples_f16, void *codebooks_f16,
                               int32_t *assign_out, aq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * FP8 E4M3 codebook storage (AQPIM blog §4.2: codebooks kept in a
+ * low-precision float such as FP8).  E4M3 (OCP): sign, 4 exponent bits with
+ * bias 7, 3 fraction bits, subnormals m * 2^-9, no infinities, S.1111.111 =
+ * NaN, largest magnitude 448.
+ *
+ * aq_codebooks_to_e4m3: n fp16 values -> n E4M3 codes, nearest with ties to
+ *   the even fraction; magnitudes beyond 448 and infinities become +-448; NaN
+ *   stays NaN.
+ * aq_codebooks_from_e4m3: n E4M3 codes -> their exact fp16 values.  Encoding
+ *   (aq_encode_append) against the widened codebook decides exactly as against
+ *   the E4M3 one.
+ * Both arrays are device memory, 16-byte aligned; n = 0 does nothing.
+ * ------------------------------------------------------------------------- */
+aq_status aq_codebooks_to_e4m3(int64_t n, const void *src_f16, uint8_t *dst_e4m3,
+                               aq_stream_t stream);
+aq_status aq_codebooks_from_e4m3(int64_t n, const uint8_t *src_e4m3, void *dst_f16,
+                                 aq_stream_t stream);
+
 /* One Lloyd step from given fp32 centroids (the step of aq_fit_codebooks,
  * exposed for step-by-step checking).
  *   centroids_in   in  fp32 [U][M][K][Dsub]
@@ -255,9 +274,16 @@ aq_status aq_decode_attention(const aq_pq_config *cfg, int32_t batch,
  *                 inputs read early -- not, for example, right after another
  *                 aq_decode_step on the same code_pages.  0: plain stream
  *                 order.
+ *                 AQ_STEP_E4M3: codebooks_f16 holds FP8 E4M3 codes (uint8,
+ *                 same [S][Hkv][2][M][K][Dsub] layout, from
+ *                 aq_codebooks_to_e4m3) instead of fp16 values: half the
+ *                 codebook bytes.  The kernel widens them exactly to fp16, so
+ *                 the step equals the fp16 step on the widened codebooks (and
+ *                 the new token's codes equal aq_encode_append's on them).
  *   other arguments as aq_decode_attention.
  * ------------------------------------------------------------------------- */
 #define AQ_STEP_OVERLAP 1
+#define AQ_STEP_E4M3    2
 aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch,
                          int32_t num_q_heads, int32_t num_kv_heads,
                          const float *q, const void *kv_new_f16,

@@ -118,6 +118,24 @@ def test_encode_and_fit_argument_checks(lib):
     assert lib.aq_refine_codebooks(ctypes.byref(cfg), 0, 64, 3, None, None, None, None) == 0
 
 
+def test_decode_step_flags_checked(lib):
+    cfg = _cfg()
+    def step(flags, kv_new=FAKE):
+        return lib.aq_decode_step(ctypes.byref(cfg), 2, 4, 4, FAKE, kv_new, FAKE, 64, FAKE, 4, FAKE, FAKE,
+                                  8, FAKE, 100, 0.1, 0, flags, FAKE, None, 0, None, None)
+    assert step(4) == 1                                 # unknown flag
+    assert step(2, kv_new=None) == 1                    # a step needs its new token
+
+
+def test_e4m3_conversion_argument_checks(lib):
+    assert lib.aq_codebooks_to_e4m3(-1, FAKE, FAKE, None) == 1
+    assert lib.aq_codebooks_to_e4m3(0, None, None, None) == 0
+    assert lib.aq_codebooks_to_e4m3(8, None, FAKE, None) == 1
+    assert lib.aq_codebooks_to_e4m3(8, FAKE, ctypes.c_void_p(0x10004), None) == 1
+    assert lib.aq_codebooks_from_e4m3(8, FAKE, None, None) == 1
+    assert lib.aq_codebooks_from_e4m3(8, ctypes.c_void_p(0x10001), FAKE, None) == 1
+
+
 def _plan(lib, B, Hq, Hkv, L, M=4, splits=0, fp16=0):
     cfg = _cfg(M=M)
     s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()

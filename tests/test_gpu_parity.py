@@ -358,6 +358,25 @@ def test_refine_matches_oracle(A, orc, name):
     _encode_direct(A, orc, kv, tset, slots, cbs, (B * 64) // 16)
 
 
+@pytest.mark.parametrize("n", [65536, 65536 - 3, 13])
+def test_e4m3_conversion_matches_oracle(A, orc, n):
+    """Every fp16 bit pattern to E4M3 and every code back to fp16, against the
+    oracle's definition (NaN compared by class: its sign is unspecified)."""
+    h = np.arange(65536, dtype=np.uint16)[:n].view(np.float16)
+    got = A.to_e4m3(dev(h)).cpu().numpy()
+    with np.errstate(invalid="ignore"):                  # NaN patterns cast to NaN
+        want = orc.e4m3_from_float(h.astype(np.float32))
+    nan = np.isnan(h)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.all((got[nan] & 0x7F) == 0x7F)
+    codes = np.arange(256, dtype=np.uint8)
+    back = A.from_e4m3(dev(codes)).cpu().numpy()
+    ref = orc.e4m3_to_float(codes).astype(np.float16)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(back[fin].view(np.uint16), ref[fin].view(np.uint16))
+    assert np.all(np.isnan(back[~fin]))
+
+
 # --------------------------------------------------------------------------
 # fused decode step (append the token at position seq_len-1, then attend)
 # --------------------------------------------------------------------------
@@ -398,6 +417,36 @@ def test_decode_step_matches_oracle(A, orc, case, splits, overlap):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert np.array_equal(pages.cpu().numpy(), want_pages)    # the new codes, nothing else
+    close(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("case", STEP_CASES + [(MANY[0][0], MANY[0][1], MANY[0][2], MANY[0][3], None)],
+                         ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}M{c[3]}" for c in STEP_CASES] + ["many_cluster2"])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_decode_step_e4m3_codebooks(A, orc, case, splits):
+    """FP8 E4M3 codebooks (AQPIM blog §4.2): the step on the codes equals the
+    oracle's step on their exact values (new codes bit-exact, outputs within
+    tolerance)."""
+    B, Hq, Hkv, M, lens = case
+    if lens is None:
+        lens = _many_lens(B, M + 1)
+    p = W.paged_codes_problem(hash((B, Hq, M, tuple(lens), 8)) % 10000, B, Hq, Hkv, M, lens, num_sets=B + 1)
+    cb8 = orc.e4m3_from_float(p["codebooks"].astype(np.float32))
+    cbw = orc.e4m3_to_float(cb8).astype(np.float16)
+    assert not np.array_equal(cbw, p["codebooks"])                 # the rounding is visible
+    kv_new = np.random.default_rng(len(lens) * 37 + M).standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+    want_pages = p["code_pages"].copy()
+    slots = np.array([p["block_table"][b, (L - 1) // 16] * 16 + (L - 1) % 16 for b, L in enumerate(lens)],
+                     np.int64)
+    orc.encode_append(kv_new, p["req_set"], slots, cbw, want_pages, 16)
+    want = oracle_pq(orc, dict(p, code_pages=want_pages, codebooks=cbw))
+    pages = dev(p["code_pages"])
+    st = A.new_status()
+    out = A.decode_step(dev(p["q"]), dev(kv_new), pages, dev(cb8), dev(p["req_set"]), dev(p["block_table"]),
+                        dev(p["seq_lens"]), int(max(lens)), 1.0 / np.sqrt(128), num_splits=splits, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(pages.cpu().numpy(), want_pages)
     close(out.cpu().numpy(), want)
 
 
