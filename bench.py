@@ -475,6 +475,8 @@ def run_ours(args, w, rank, world, local_rank):
     # fp16 comparison kernel on the same shape (cache of the same raw vectors)
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
     e4m3 = None if args.two_call else measure_e4m3(args, w, api, torch, base, Lmax, units, T)
+    sweep = (measure_layer_sweep(args, w, api, torch, base, Lmax, T)
+             if w.layers > 1 and not args.two_call else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -505,6 +507,8 @@ def run_ours(args, w, rank, world, local_rank):
         line["fp16_comparison"] = fp16
     if e4m3:
         line["e4m3_codebooks"] = e4m3
+    if sweep:
+        line["layer_sweep"] = sweep
     if rank == 0 and not args.no_cpu:
         ost = OracleStep(w)
         units_c, secs_c, n_c = ost.run(args.cpu_budget)
@@ -597,6 +601,66 @@ def measure_fp16(args, w, api, torch, base, Lmax, units, T):
     return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_call": ms,
             "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
             "splits": splits}
+
+
+def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
+    """A multi-layer stack (the 80-layer GQA workload): one fused decode step
+    per layer, each on that layer's own cache (its codebooks fitted and its
+    tokens encoded from that layer's vectors), run back to back as one sweep.
+    Timed eagerly (one launch per layer from Python) and as one captured CUDA
+    graph; the caches of all layers together exceed L2, so each step reads
+    cold codebooks and codes."""
+    Hq, Hkv, M = w.num_q_heads, w.num_kv_heads, w.num_subspaces
+    keep = ("q", "new_kv", "pages", "codebooks", "req_set", "bt", "seq_lens")
+    layers = [{k: base0[k] for k in keep}]
+    for layer in range(1, w.layers):
+        c = build_cache(w, api, torch, layer=layer)
+        layers.append({k: c[k] for k in keep})
+        del c
+    splits, cluster, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
+    st = api.new_status()
+
+    def sweep():
+        # consecutive steps touch different layers' caches: overlapped launches
+        # keep the early-read contract
+        for c in layers:
+            api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                            c["seq_lens"], Lmax, w.scale, overlap=True, out=out, workspace=ws, status=st)
+
+    for _ in range(3):
+        sweep()
+    torch.cuda.synchronize()
+    n = 5
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        sweep()
+    e1.record()
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sweep()
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / n
+    assert int(st.item()) == 0
+    byt = T.pq_step_bytes(w.seq_lens, Hq, Hkv, M)["total"] * w.layers
+    units = T.kv_tokens_heads(w.seq_lens, Hkv) * w.layers
+    peak, _ = measured_peaks()
+    del layers
+    return {"layers": w.layers, "eager_ms_per_sweep": eager_ms, "graph_ms_per_sweep": graph_ms,
+            "us_per_layer": graph_ms * 1e3 / w.layers, "value": units / (graph_ms / 1e3), "unit": UNIT,
+            "gbs": byt / (graph_ms / 1e3) / 1e9, "frac_of_peak": byt / (graph_ms / 1e3) / 1e9 / peak,
+            "plan": {"splits": splits, "cluster": cluster}}
 
 
 def measure_e4m3(args, w, api, torch, base, Lmax, units, T):
