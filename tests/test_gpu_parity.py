@@ -219,7 +219,7 @@ def test_encode_small_batch_append(A, orc):
 
 
 def test_encode_prefill_tiles(A, orc):
-    # many tokens (token-parallel kernel), ragged requests sharing tiles
+    # 767 and 829 tokens x 8 / 4 heads: still the codeword-parallel kernel; ragged requests
     w = W.make("ragged", seq_lens=[300, 70, 333, 64], num_q_heads=8, num_kv_heads=8)
     _encode_case(A, orc, w, 0, 10**9)
     w = W.make("long", seq_lens=[700, 129], num_q_heads=4, num_kv_heads=4)

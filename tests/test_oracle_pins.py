@@ -96,6 +96,10 @@ def test_byte_arithmetic_matches_pages():
 def test_pq_call_bytes_page1_shape():
     """B4 H32 L2048 M4: codes 2*4*32*2048*4 B, codebooks 4*32*2*64 KiB."""
     from decode_attention_product_gb300 import traffic as T
+    e = T.pq_step_bytes_e4m3([2048] * 4, 32, 32, 4)
+    f = T.pq_step_bytes([2048] * 4, 32, 32, 4)
+    assert e["codebooks"] == 4 * 32 * 2 * 4 * 256 * 32          # one byte per E4M3 entry
+    assert f["total"] - e["total"] == e["codebooks"]
     b = T.pq_decode_bytes([2048] * 4, 32, 32, 4)
     assert b["codes"] == 2 * 4 * 32 * 2048 * 4 == 2_097_152
     assert b["codebooks"] == 4 * 32 * 2 * 65536 == 16_777_216
