@@ -509,6 +509,11 @@ def run_ours(args, w, rank, world, local_rank):
         line["e4m3_codebooks"] = e4m3
     if sweep:
         line["layer_sweep"] = sweep
+    if args.two_call:
+        # the step's append (aq_encode_append of one token per request) is the
+        # step time less the decode launch time
+        line["append"] = {"us_per_step": (total_ms / args.steps - dec_avg_ms) * 1e3,
+                          "how": "step time minus the decode launch's event time"}
     if rank == 0 and not args.no_cpu:
         ost = OracleStep(w)
         units_c, secs_c, n_c = ost.run(args.cpu_budget)
