@@ -328,6 +328,129 @@ def build_cache(w, api, torch, layer=0):
             "kvs": kvs}
 
 
+MIN_REGION_MS = 200.0     # every timed region lasts at least this long
+
+
+def time_steps(torch, step, R, steps, dist=False, min_region_ms=MIN_REGION_MS, clocks=None):
+    """Device time per step of a rotation of steps, replayed from CUDA graphs.
+
+    `step(i)` launches step i, which uses input copy i % R.  One graph holds R
+    consecutive steps (copies 0..R-1) and one the tail of the timed count, so
+    consecutive steps always use different copies.  The timed region runs
+    `reps` x `steps` steps, reps chosen so that the region lasts at least
+    `min_region_ms`; a lead-in replay is enqueued before the start event, so
+    the GPU is already busy when the region starts and the host's graph-launch
+    latency stays outside it.  CUDA events on the launching stream; barrier and
+    synchronize on both sides.  Returns (ms per step, steps timed, region ms).
+    """
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                step(i)
+        return g
+
+    g_cycle = capture(R)
+    g_cycle.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    g_cycle.replay()
+    e0.record()
+    g_cycle.replay()
+    g_cycle.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    est = e0.elapsed_time(e1) / (2 * R)
+    reps = max(1, math.ceil(min_region_ms / max(steps * est, 1e-6)))
+    total = steps * reps
+    n_cyc, tail = divmod(total, R)
+    g_tail = capture(tail) if tail else None
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    if clocks is not None:
+        clocks.start()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    g_cycle.replay()                                   # lead-in, not timed
+    e0.record()
+    for _ in range(n_cyc):
+        g_cycle.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks is not None else None
+    region = e0.elapsed_time(e1)
+    return region / total, total, region, clk
+
+
+def rotation(base, torch, l2, keys=("codebooks", "pages", "q", "new_kv")):
+    """Input copies for rotation: enough that R consecutive steps read more than
+    2 x L2, so every timed step reads cold codebooks and codes."""
+    per_copy = sum(base[k].numel() * base[k].element_size() for k in keys)
+    R = max(2, min(64, math.ceil(2.2 * l2 / per_copy)))
+    copies = [base] + [{k: (v.clone() if torch.is_tensor(v) and k in keys else v)
+                        for k, v in base.items()} for _ in range(R - 1)]
+    return copies, R, per_copy
+
+
+def measure_fused_step(args, w, api, torch, T, base, local_rank, dist, world, e4m3=True):
+    """The fused decode step of workload w (aq_decode_step, launched as a
+    programmatic dependent of the previous step, which wrote another copy):
+    device time per step, roofline of the step kernel, clocks during the
+    timed region; plus the same step with E4M3 codebooks."""
+    M, Hq, Hkv = w.num_subspaces, w.num_q_heads, w.num_kv_heads
+    Lmax = int(w.seq_lens.max())
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    copies, R, per_copy = rotation(base, torch, l2)
+    splits, cluster, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda") for _ in range(R)]
+    status = api.new_status()
+
+    def step(i):
+        c = copies[i % R]
+        api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                        c["seq_lens"], Lmax, w.scale, overlap=True, out=outs[i % R], workspace=ws,
+                        status=status)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ms, n_timed, region, clk = time_steps(torch, step, R, args.steps, dist, clocks=ClockSampler(local_rank))
+    ms = max_over_ranks(ms)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    units = T.kv_tokens_heads(w.seq_lens, Hkv)
+    byt = T.pq_step_bytes(w.seq_lens, Hq, Hkv, M)
+    peak, peak_kind = measured_peaks()
+    achieved = byt["total"] / (ms / 1e3) / 1e9
+    out = {
+        "workload": workload_desc(w), "ms_per_step": ms, "steps_timed": n_timed, "region_ms": region,
+        "value": job_value(units, 1, ms / 1e3, world), "unit": UNIT,
+        "plan": {"splits": splits, "cluster": cluster},
+        "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB "
+              f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": measured_traffic(w.name, "step"),
+                     "kernel": "pq_decode_kernel (fused step)", "bytes_per_launch": byt["total"],
+                     "launch_ms": ms, "peak_kind": peak_kind},
+        "code_stream": {"gbs": byt["code_stream"] / (ms / 1e3) / 1e9,
+                        "codes_only_gbs": byt["codes"] / (ms / 1e3) / 1e9,
+                        "frac_of_peak": byt["code_stream"] / (ms / 1e3) / 1e9 / peak},
+        "clocks": clk,
+        "launches_per_step": 1 + (1 if splits > 1 else 0),
+    }
+    del copies, outs
+    if e4m3:
+        out["e4m3_codebooks"] = measure_e4m3(args, w, api, torch, base, Lmax, units, T, local_rank)
+    return out
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     torch.cuda.set_device(local_rank)
@@ -341,163 +464,84 @@ def run_ours(args, w, rank, world, local_rank):
     Lmax = int(w.seq_lens.max())
     base = build_cache(w, api, torch)
     M, Hq, Hkv = w.num_subspaces, w.num_q_heads, w.num_kv_heads
-    # rotation copies so that every timed step reads cold inputs (> 2 x L2)
-    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
-    per_copy = (base["codebooks"].numel() * 2 + base["pages"].numel() + base["q"].numel() * 4
-                + base["new_kv"].numel() * 2)
-    R = max(2, min(64, math.ceil(2.2 * l2 / per_copy))) if not args.no_rotate else 1
-    copies = [base] + [{k: (v.clone() if torch.is_tensor(v) and k in
-                            ("codebooks", "pages", "q", "new_kv") else v)
-                        for k, v in base.items()} for _ in range(R - 1)]
-    splits, cluster, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
-    outs = [torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda") for _ in range(R)]
-    status = api.new_status()
-
-    def step(i, ev0=None, ev1=None):
-        c = copies[i % R]
-        if not args.two_call:
-            # one fused launch: append the new token + attention, overlapping the
-            # previous step's tail, which wrote another copy's pages (with a
-            # single copy the previous step wrote these pages: no overlap)
-            api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
-                            c["seq_lens"], Lmax, w.scale, overlap=R > 1, out=outs[i % R], workspace=ws,
-                            status=status)
-            return
-        api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)
-        if ev0 is not None:
-            ev0.record()
-        api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
-                             c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws,
-                             status=status)
-        if ev1 is not None:
-            ev1.record()
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    # The timed steps are replayed from CUDA graphs (launch overhead of the
-    # Python binding off the critical path): one graph of R steps (one per input
-    # copy) and one of the K mod R remaining steps, so exactly K steps run.
-    evpairs = []
-
-    def capture(n, with_events):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(n):
-                e0 = e1 = None
-                if with_events:
-                    e0 = torch.cuda.Event(enable_timing=True, external=True)
-                    e1 = torch.cuda.Event(enable_timing=True, external=True)
-                    evpairs.append((e0, e1))
-                step(i, e0, e1)
-        return g
-
-    events_in_graph = False
-    if args.two_call:
-        try:
-            g_full = capture(R, True)
-            events_in_graph = True
-        except Exception:                               # torch without external events
-            torch.cuda.synchronize()
-            evpairs.clear()
-            g_full = capture(R, False)
-    else:
-        g_full = capture(R, False)
-    n_full, n_tail = divmod(args.steps, R)
-    g_tail = capture(n_tail, False) if n_tail else None
-    for _ in range(2):
-        g_full.replay()
-    torch.cuda.synchronize()
-    if dist:
-        torch.distributed.barrier()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    torch.cuda.synchronize()
-    if dist:
-        torch.distributed.barrier()
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_begin.record()
-    for _ in range(n_full):
-        g_full.replay()
-    if g_tail is not None:
-        g_tail.replay()
-    t_end.record()
-    torch.cuda.synchronize()
-    if dist:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    total_ms = t_begin.elapsed_time(t_end)
-    if not args.two_call:
-        dec_ms = [total_ms / args.steps]
-        dec_how = ("one fused kernel per step: timed region / K launches (CUDA events around "
-                   "the graph replays)")
-    elif events_in_graph and n_full > 0:
-        dec_ms = [e0.elapsed_time(e1) for e0, e1 in evpairs]
-        dec_how = "events around each decode launch inside the replayed step graph (last replay)"
-    else:
-        # decode-only graph of R back-to-back launches, timed with events
-        g_dec = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_dec):
-            for i in range(R):
-                c = copies[i % R]
-                api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
-                                     c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws,
-                                     status=status)
-        g_dec.replay()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        reps = max(1, args.steps // R)
-        e0.record()
-        for _ in range(reps):
-            g_dec.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        dec_ms = [e0.elapsed_time(e1) / (reps * R)]
-        dec_how = "decode-only graph of back-to-back launches (events around the replays)"
-    total_ms = max_over_ranks(total_ms)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
     units = T.kv_tokens_heads(w.seq_lens, Hkv)
-    value = job_value(units, args.steps, total_ms / 1e3, world)
-    # roofline of the decode kernel (algorithmic bytes per launch / event time)
-    byt = (T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M) if args.two_call
-           else T.pq_step_bytes(w.seq_lens, Hq, Hkv, M))
-    dec_avg_ms = float(np.mean(dec_ms))
     peak, peak_kind = measured_peaks()
-    achieved = byt["total"] / (dec_avg_ms / 1e3) / 1e9
-    traffic = measured_traffic(w.name, "two_call" if args.two_call else "step")
+    splits, cluster, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
+    if not args.two_call:
+        main = measure_fused_step(args, w, api, torch, T, base, local_rank, dist, world)
+        ms, n_timed = main["ms_per_step"], main["steps_timed"]
+        roof = dict(main["roofline"], timing=(
+            f"one fused kernel per step: CUDA events around graph replays of {n_timed} steps "
+            f"({args.steps} x {n_timed // args.steps}, region {main['region_ms']:.0f} ms, lead-in "
+            f"replay enqueued first), divided by the steps run"))
+        launches = n_timed * main["launches_per_step"]
+        clk = main["clocks"]
+    else:
+        # two launches per step (append, then decode attention): the step is
+        # timed as a whole, the decode launch alone from a decode-only rotation
+        l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+        copies, R, per_copy = rotation(base, torch, l2)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+        outs = [torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda") for _ in range(R)]
+        status = api.new_status()
+
+        def step(i):
+            c = copies[i % R]
+            api.encode_append(c["new_kv"], c["new_set"], c["new_slot"], c["codebooks"], c["pages"], status)
+            api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                                 c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws, status=status)
+
+        def dec(i):
+            c = copies[i % R]
+            api.decode_attention(c["q"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                                 c["seq_lens"], Lmax, w.scale, out=outs[i % R], workspace=ws, status=status)
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        ms, n_timed, region, clk = time_steps(torch, step, R, args.steps, dist,
+                                              clocks=ClockSampler(local_rank))
+        ms = max_over_ranks(ms)
+        dec_ms, _, _, _ = time_steps(torch, dec, R, args.steps, dist)
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        byt = T.pq_decode_bytes(w.seq_lens, Hq, Hkv, M)
+        achieved = byt["total"] / (dec_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": measured_traffic(w.name, "two_call"), "kernel": "pq_decode_kernel",
+                "bytes_per_launch": byt["total"], "launch_ms": dec_ms, "peak_kind": peak_kind,
+                "timing": "decode-only rotation of graph replays (CUDA events, lead-in replay first)"}
+        main = {"code_stream": {"gbs": byt["code_stream"] / (dec_ms / 1e3) / 1e9,
+                                "codes_only_gbs": byt["codes"] / (dec_ms / 1e3) / 1e9,
+                                "frac_of_peak": byt["code_stream"] / (dec_ms / 1e3) / 1e9 / peak},
+                "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB"}
+        launches = n_timed * (2 + (1 if splits > 1 else 0))
+        del copies, outs
+    value = job_value(units, 1, ms / 1e3, world)
     # e2e through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
         e2e = measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist)
     prefill = measure_prefill(w, api, torch, base, peak)
     # fp16 comparison kernel on the same shape (cache of the same raw vectors)
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
-    e4m3 = None if args.two_call else measure_e4m3(args, w, api, torch, base, Lmax, units, T)
     sweep = (measure_layer_sweep(args, w, api, torch, base, Lmax, T)
              if w.layers > 1 and not args.two_call else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "steps_timed": n_timed, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(w), "batch": w.batch, "seq_len": Lmax,
                    "num_q_heads": Hq, "num_kv_heads": Hkv, "num_subspaces": M,
                    "num_codewords": w.num_codewords, "plan": {"splits": splits, "cluster": cluster},
-                   "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB "
-                         f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)" if R > 1 else "none",
+                   "l2": main["l2"],
                    "step": ("append 1 token/request (encode) + PQ decode attention, two launches"
                             if args.two_call else
                             "fused launch: append 1 token/request + PQ decode attention "
                             "(aq_decode_step, programmatic dependent launch)")},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "kernel": "pq_decode_kernel" + ("" if args.two_call else " (fused step)"),
-                     "bytes_per_launch": byt["total"], "launch_ms": dec_avg_ms,
-                     "peak_kind": peak_kind, "timing": dec_how},
-        "code_stream": {"gbs": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9,
-                        "codes_only_gbs": byt["codes"] / (dec_avg_ms / 1e3) / 1e9,
-                        "frac_of_peak": byt["code_stream"] / (dec_avg_ms / 1e3) / 1e9 / peak},
-        "gpu_launches": args.steps * ((2 if args.two_call else 1) + (1 if splits > 1 else 0)),
+        "roofline": roof,
+        "code_stream": main["code_stream"],
+        "gpu_launches": launches,
         "clocks": clk,
         "prefill": prefill,
     }
@@ -505,15 +549,29 @@ def run_ours(args, w, rank, world, local_rank):
         line["e2e"] = e2e
     if fp16:
         line["fp16_comparison"] = fp16
-    if e4m3:
-        line["e4m3_codebooks"] = e4m3
+    if "e4m3_codebooks" in main:
+        line["e4m3_codebooks"] = main["e4m3_codebooks"]
     if sweep:
         line["layer_sweep"] = sweep
     if args.two_call:
-        # the step's append (aq_encode_append of one token per request) is the
-        # step time less the decode launch time
-        line["append"] = {"us_per_step": (total_ms / args.steps - dec_avg_ms) * 1e3,
-                          "how": "step time minus the decode launch's event time"}
+        line["append"] = {"us_per_step": (ms - roof["launch_ms"]) * 1e3,
+                          "how": "step time minus the decode launch's time"}
+    del base
+    torch.cuda.empty_cache()
+    # the other workloads' fused steps, each timed the same way
+    if not args.two_call and not args.no_extras and w.name == "page1":
+        extra = {}
+        for name in ("ragged", "long", "qwen_gqa"):
+            wx = W.make(name)
+            bx = build_cache(wx, api, torch)
+            ex = measure_fused_step(args, wx, api, torch, T, bx, local_rank, dist, world)
+            ex.pop("launches_per_step")
+            if wx.layers > 1:
+                ex["layer_sweep"] = measure_layer_sweep(args, wx, api, torch, bx, int(wx.seq_lens.max()), T)
+            extra[name] = ex
+            del bx
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
     if rank == 0 and not args.no_cpu:
         ost = OracleStep(w)
         units_c, secs_c, n_c = ost.run(args.cpu_budget)
@@ -560,7 +618,8 @@ def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
 
 
 def measure_fp16(args, w, api, torch, base, Lmax, units, T):
-    """The uncompressed comparison: fp16 pages of the same raw vectors."""
+    """The uncompressed comparison: fp16 pages of the same raw vectors, timed
+    like the PQ step (graph replays over rotated copies larger than 2 x L2)."""
     Hq, Hkv = w.num_q_heads, w.num_kv_heads
     kvs = base["kvs"]
     bt = base["bt_np"]
@@ -575,35 +634,24 @@ def measure_fp16(args, w, api, torch, base, Lmax, units, T):
         pages[idx] = torch.from_numpy(np.ascontiguousarray(blk)).cuda()
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     per = pages.numel() * 2
-    R = max(1, min(8, math.ceil(2.2 * l2 / per)))
+    R = max(2, min(8, math.ceil(2.2 * l2 / per)))
     pcs = [pages] + [pages.clone() for _ in range(R - 1)]
     splits, _, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, fp16=True)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
-    for i in range(3):
+
+    def step(i):
         api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax, w.scale,
                                   out=out, workspace=ws)
+
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(R):
-            api.decode_attention_fp16(base["q"], pcs[i % R], base["bt"], base["seq_lens"], Lmax,
-                                      w.scale, out=out, workspace=ws)
-    g.replay()
-    torch.cuda.synchronize()
-    reps = max(2, -(-max(10, args.steps) // R))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (reps * R)
+    ms, n_timed, _, _ = time_steps(torch, step, R, args.steps)
     byt = T.fp16_decode_bytes(w.seq_lens, Hq, Hkv)
     peak, _ = measured_peaks()
     del pcs, pages
-    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_call": ms,
+    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_call": ms, "steps_timed": n_timed,
             "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
             "splits": splits}
 
@@ -637,7 +685,7 @@ def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
     for _ in range(3):
         sweep()
     torch.cuda.synchronize()
-    n = 5
+    n = 20
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -651,6 +699,9 @@ def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
         sweep()
     g.replay()
     torch.cuda.synchronize()
+    # graph replays over a region of >= MIN_REGION_MS, a lead-in replay first
+    n = max(5, math.ceil(MIN_REGION_MS / max(eager_ms, 1e-3)))
+    g.replay()
     e0.record()
     for _ in range(n):
         g.replay()
@@ -668,49 +719,36 @@ def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
             "plan": {"splits": splits, "cluster": cluster}}
 
 
-def measure_e4m3(args, w, api, torch, base, Lmax, units, T):
+def measure_e4m3(args, w, api, torch, base, Lmax, units, T, local_rank=0):
     """The fused step with the same codebooks stored as FP8 E4M3 codes (half
     the codebook bytes; AQPIM blog §4.2), timed like the main step: graph
     replays over rotated copies of codebooks and pages larger than 2 x L2."""
     Hq, Hkv, M = w.num_q_heads, w.num_kv_heads, w.num_subspaces
-    cb8 = api.to_e4m3(base["codebooks"])
-    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-    per = cb8.numel() + base["pages"].numel()
-    R = max(1, min(16, math.ceil(2.2 * l2 / per)))
-    books = [cb8] + [cb8.clone() for _ in range(R - 1)]
-    pages = [base["pages"].clone() for _ in range(R)]
+    # its own pages too: the steps write the new tokens' codes, which differ
+    # from the fp16 codebooks' codes where rounding moved a codeword
+    b8 = dict(base, codebooks=api.to_e4m3(base["codebooks"]), pages=base["pages"].clone())
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    copies, R, _ = rotation(b8, torch, l2)
     splits, _, wsb = api.decode_plan(w.batch, Hq, Hkv, Lmax, M)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
     st = api.new_status()
 
     def step(i):
-        api.decode_step(base["q"], base["new_kv"], pages[i % R], books[i % R], base["req_set"], base["bt"],
-                        base["seq_lens"], Lmax, w.scale, overlap=R > 1, out=out, workspace=ws, status=st)
+        c = copies[i % R]
+        api.decode_step(c["q"], c["new_kv"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                        c["seq_lens"], Lmax, w.scale, overlap=True, out=out, workspace=ws, status=st)
 
     for i in range(3):
         step(i)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(R):
-            step(i)
-    g.replay()
-    torch.cuda.synchronize()
-    reps = max(2, -(-max(10, args.steps) // R))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
+    ms, n_timed, _, _ = time_steps(torch, step, R, args.steps)
     assert int(st.item()) == 0
-    ms = e0.elapsed_time(e1) / (reps * R)
     byt = T.pq_step_bytes_e4m3(w.seq_lens, Hq, Hkv, M)
     peak, _ = measured_peaks()
-    del books, pages
-    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "bytes_per_step": byt["total"],
+    del copies, b8
+    return {"value": units / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps_timed": n_timed,
+            "bytes_per_step": byt["total"],
             "gbs": byt["total"] / (ms / 1e3) / 1e9, "frac_of_peak": byt["total"] / (ms / 1e3) / 1e9 / peak,
             "codebooks": "FP8 E4M3 (same codebooks, rounded to nearest even)"}
 
@@ -725,7 +763,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="page1 only: skip the ragged, long and qwen_gqa step objects")
     ap.add_argument("--two-call", action="store_true",
                     help="time aq_encode_append + aq_decode_attention instead of the fused step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -64,12 +64,13 @@ _lock = threading.Lock()
 
 
 def load(path: str | None = None):
-    """Load libaqpq.so (once).  Raises if it is missing."""
+    """Load libaqpq.so (once).  Raises if it is missing.  The environment
+    variable AQPQ_LIB names another build of the library to load instead."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIB_PATH
+        p = path or os.environ.get("AQPQ_LIB") or LIB_PATH
         if not os.path.exists(p):
             raise RuntimeError(
                 f"libaqpq.so not found at {p}; build it with "

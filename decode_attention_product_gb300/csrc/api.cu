@@ -1,8 +1,11 @@
 // api.cu -- the extern "C" boundary of libaqpq (declared in include/aqpq.h):
 // host-side argument checks (before any CUDA call), work planning, dispatch to
 // the kernel launchers and mapping of CUDA errors to AQ_ERR_CUDA.
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "aqpq.h"
@@ -46,6 +49,19 @@ void record_cuda_error(cudaError_t e) {
     cudaGetLastError();
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
                   cudaGetErrorString(e));
+}
+
+cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(need));
+    std::lock_guard<std::mutex> lock(a.mu);
+    if (a.bytes[dev] >= need) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(need));
+    if (e == cudaSuccess) a.bytes[dev] = need;
+    return e;
 }
 
 // The plan is a pure function of the arguments (no device query), so that
@@ -109,11 +125,99 @@ static void split_plan(int C, int share_max, bool fp16, int64_t units, int max_s
     pl->share = ((pl->split_len + C - 1) / C + P - 1) / P * P;
 }
 
+// Which PQ kernel: AQPQ_DECODE_KERNEL=1 or 2 in the environment forces one
+// (for comparing them); otherwise the planner chooses.
+static int forced_kernel() {
+    const char *e = std::getenv("AQPQ_DECODE_KERNEL");
+    if (!e) return 0;
+    return (e[0] == '1' || e[0] == '2') && e[1] == 0 ? e[0] - '0' : 0;
+}
+
+// Whole-split plan (pq_attend_kernel): clusters of C CTAs, one subspace each
+// (M = 4: C = 4; M = 8: C = 8), every CTA holding the codes of the whole
+// split.  Splits only as many as the split capacity requires, more when the
+// clusters would not give about one CTA per SM; each split keeps >= 512
+// tokens, since every split reads the codebooks again.
+static bool attend_plan(int M, int G, int64_t units, int max_seq_len, int req, int sms, int P,
+                        size_t smem_cap, Plan *pl) {
+    const int C = M;                                   // one subspace per CTA
+    const int cap = pq_attend_max_split(M, G);
+    if (cap <= 0) return false;
+    const int pages = (max_seq_len + P - 1) / P;
+    int S = req;
+    if (S <= 0) {
+        S = (max_seq_len + cap - 1) / cap;
+        if (S < 1) S = 1;
+        const int64_t ctas = units * C * S;
+        if (ctas < sms && max_seq_len >= 1024) {
+            int want = static_cast<int>((sms + units * C - 1) / (units * C));
+            const int most = max_seq_len / 512;
+            if (want > most) want = most;
+            if (want > S) S = want;
+        }
+    }
+    if (S > 4096) S = 4096;
+    if (pages == 0) S = 1;
+    int split_pages = (pages + S - 1) / S;
+    if (split_pages < 1) split_pages = 1;
+    if (split_pages * P > cap) return false;
+    S = (pages + split_pages - 1) / split_pages;
+    if (S < 1) S = 1;
+    const size_t smem = pq_attend_smem_bytes(M, G, C, split_pages * P);
+    if (smem == 0 || smem > smem_cap) return false;
+    pl->kernel = 2;
+    pl->num_splits = S;
+    pl->cluster = C;
+    pl->split_len = split_pages * P;
+    pl->share = pl->split_len;
+    pl->head_split = 1;
+    pl->smem = smem;
+    return true;
+}
+
+static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
+                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl);
+
+// The plan of a decode call.  PQ: the whole-split kernel for GQA groups of 4
+// or more query heads per kv head when a split of at most two fits its
+// capacity (and the codebooks are fp16) -- there the table and value product
+// per query head dominate and scoring every token in each CTA is cheap
+// (measured: B8 Hq64 Hkv8 L1000 13.3 -> 12.9 us) -- else the token-share
+// kernel, whose split of the token work across the cluster is cheaper when
+// each kv head serves one or two query heads (B4 H32 L2048: 7.9 us against
+// 9.3 us).  The workspace reported covers both, so a caller that
+// sizes it with aq_decode_plan (which does not know the codebook format) has
+// enough for either.
 static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
-                           int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
+                           int req, bool fp16, int sms, size_t smem_cap, Plan *pl, bool e4m3 = false,
+                           bool allow_attend = true) {
+    Plan p1{};
+    aq_status st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1);
+    if (st != AQ_OK) return st;
+    Plan p2{};
+    const int64_t units = static_cast<int64_t>(batch) * Hkv;
+    const int forced = forced_kernel();
+    if (!fp16 && allow_attend && forced != 1 && (forced == 2 || Hq / Hkv >= 4) &&
+        attend_plan(cfg->num_subspaces, Hq / Hkv, units, max_seq_len, req, sms, cfg->page_size, smem_cap, &p2) &&
+        (forced == 2 || p2.num_splits <= 2)) {
+        p2.workspace = p2.num_splits > 1
+                           ? static_cast<size_t>(batch) * Hq * p2.num_splits * (kHeadDim + 2) * sizeof(float)
+                           : 0;
+        const size_t ws = p2.workspace > p1.workspace ? p2.workspace : p1.workspace;
+        *pl = e4m3 ? p1 : p2;
+        pl->workspace = ws;
+        return AQ_OK;
+    }
+    *pl = p1;
+    return AQ_OK;
+}
+
+static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
+                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
     const int P = cfg->page_size;
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
+    pl->kernel = 1;
     if (fp16) {
         split_plan(1, 0, true, units, max_seq_len, req, sms, P, pl);
         pl->head_split = 1;
@@ -289,6 +393,35 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens, int32_t 
     return e == cudaSuccess ? AQ_OK : cuda_fail(e);
 }
 
+// TMA view of the codebooks [S][Hkv][2][M][K][Dsub] fp16 as rows of Dsub
+// elements, one 256-row box per subspace, with the 64-byte (Dsub 32) or
+// 32-byte (Dsub 16) swizzle that places 16-byte chunk c of row k at
+// c ^ ((k / (128 / row bytes)) mod chunks per row) -- the kernels' layout.
+static cudaError_t codebook_tensor_map(CUtensorMap *map, const void *codebooks, int64_t num_sets, int Hkv, int M) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    if (!encode) return cudaErrorNotSupported;
+    const int dsub = kHeadDim / M;
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_sets > 0 ? num_sets : 1) * Hkv * 2 * M * kCodewords;
+    if (rows >= (1ull << 31)) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dsub), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(dsub) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(dsub), static_cast<cuuint32_t>(kCodewords)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(codebooks), dims, strides,
+                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              dsub == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static aq_status check_decode_common(const aq_pq_config *cfg, bool need_pq, int32_t batch, int32_t Hq,
                                      int32_t Hkv, int32_t max_pages, int32_t max_seq_len,
                                      int32_t num_splits) {
@@ -346,10 +479,21 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     if ((flags & AQ_STEP_E4M3) && (fp16 || !kv_new)) return AQ_ERR_INVALID_ARGUMENT;
     if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
     Plan pl{};
-    st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl);
+    st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl,
+                   (flags & AQ_STEP_E4M3) != 0);
     if (st != AQ_OK) return st;
     if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return AQ_ERR_WORKSPACE_TOO_SMALL;
     DecodeParams p{};
+    // a TMA view of fp16 codebooks for the kernels' slice copies
+    p.cb_map_ok = !fp16 && !(flags & AQ_STEP_E4M3) &&
+                  codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv, cfg->num_subspaces) == cudaSuccess;
+    if (pl.kernel == 2 && !p.cb_map_ok) {
+        // no TMA view of these codebooks (too many rows): the token-share kernel
+        const size_t ws_need = pl.workspace;
+        st = make_plan(cfg, batch, Hq, Hkv, max_seq_len, num_splits, fp16, kPlanSMs, kPlanSmemCap, &pl, true, false);
+        if (st != AQ_OK) return st;
+        pl.workspace = ws_need > pl.workspace ? ws_need : pl.workspace;
+    }
     p.q = q;
     p.code_pages = code_pages;
     p.codebooks = codebooks;

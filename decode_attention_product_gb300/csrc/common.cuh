@@ -101,6 +101,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
+// TMA tensor copy of one box of a 2-D tensor map (x = innermost element
+// coordinate, y = row) to this CTA's shared memory; completion is counted in
+// bytes on `bar`.  `map` is the address of a __grid_constant__ kernel
+// parameter.  The destination is aligned to the map's swizzle period.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 16-byte global -> shared copy through L2 (cp.async.cg): the destination is
 // any 16-byte aligned shared address, so a copy can lay rows out in its own
 // (swizzled) order.  Completion is tracked per thread.

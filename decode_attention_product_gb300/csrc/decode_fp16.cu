@@ -178,14 +178,10 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
 template <int G>
 cudaError_t launch_g(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     const size_t smem = (2 * kWarps * G + kWarps * G * kHeadDim) * sizeof(float) + 16;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(fp16_decode_kernel<G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static SmemAttr attr_state;                    // opt-in dynamic shared memory, per device
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(fp16_decode_kernel<G>), smem);
+        e != cudaSuccess)
+        return e;
     dim3 grid(static_cast<unsigned>(plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
               static_cast<unsigned>(p.batch));
     fp16_decode_kernel<G><<<grid, kThreads, smem, s>>>(p);

@@ -59,24 +59,23 @@ struct PqCfg {
     // tokens per thread, held in registers (codes and scores)
     static constexpr int TPT = (M == 8 && G <= 2) ? 4 : 8;
     static constexpr int MAX_SHARE = TPT * TOK_PER_PASS;    // tokens per CTA
-    // statistics pushed with the bins: m[G], l[G], new-token score[G], bad flag,
-    // the scale of the (integer) bins
-    static constexpr int STAT_FLOATS = 3 * G + 2;
+    // statistics pushed with the bins: m[G], l[G], new-token score[G], the
+    // scale of the (integer) bins of each head [G], bad flag
+    static constexpr int STAT_FLOATS = 4 * G + 1;
     static constexpr int INC_STRIDE = ROW_FLOATS + (STAT_FLOATS + 3) / 4 * 4;
     static constexpr int NKEY = 2 * MC;
     // value product: the k-slice order of subspace mi is XOR-ed with mi * VP_XOR,
     // so that the rows one half-warp reads (several subspaces, neighbouring
     // k-slices) fall in distinct 32- or 64-byte parts of their lines
     static constexpr int VP_XOR = (M == 8 && C == 4) ? 2 : 1;                     // new-token argmins: K then V, owned subspaces
-    // shared-memory layout (bytes)
-    static constexpr int OFF_BAR = 0;                       // 5 mbarriers
-    static constexpr int OFF_MISC = 64;                     // int flags
-    // codebook slices: with clusters of 4 (4 resident CTAs per SM either way)
-    // one buffer each, the V slice issued as soon as the K slice has landed;
-    // with fewer CTAs per cluster (larger slices) one buffer holds the K slice
-    // until the table build and the new key's encode are done, then the V slice
+    // shared-memory layout (bytes), the codebook slices first: TMA copies them
+    // with the hardware swizzle when the dynamic shared memory starts on a
+    // 1024-byte boundary.  With clusters of 4 (4 resident CTAs per SM either
+    // way) one buffer each, both slices issued at the start; with fewer CTAs
+    // per cluster (larger slices) one buffer holds the K slice until the table
+    // build and the new key's encode are done, then the V slice
     static constexpr bool SHARED_CB = C < 4;
-    static constexpr int OFF_CB = 128;
+    static constexpr int OFF_CB = 0;
     static constexpr int OFF_CBV = OFF_CB + (SHARED_CB ? 0 : CB_BYTES);
     static constexpr int OFF_LUT = OFF_CBV + CB_BYTES;
     static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
@@ -88,8 +87,11 @@ struct PqCfg {
     // new token: owned sub-vectors [2][MC][DSUB] f32, codes [2][M] int, score [G]
     static constexpr int OFF_NEW = (OFF_STAT + 2 * G * 4 + 15) / 16 * 16;
     static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8;
-    static constexpr int END = OFF_KEYS + NKEY * 8;
+    static constexpr int OFF_BAR = OFF_KEYS + NKEY * 8;     // 5 mbarriers
+    static constexpr int OFF_MISC = OFF_BAR + 5 * 8;        // int flags
+    static constexpr int END = OFF_MISC + 16;
     static size_t smem() { return END; }
+    static_assert(CB_BYTES % 1024 == 0, "slices keep the swizzle alignment");
     static_assert(K == kThreads, "one thread per codeword in the table build");
     static_assert(CB_CHUNKS % kThreads == 0, "whole slice chunks per thread");
     static_assert((NCH & (NCH - 1)) == 0 && NCH <= 8, "XOR swizzle over a power-of-two chunk count");
@@ -206,6 +208,23 @@ __device__ __forceinline__ void load_vec(float (&v)[N], const float *src) {
     }
 }
 
+template <int N>
+__device__ __forceinline__ void load_vec_u(unsigned (&v)[N], const unsigned *src) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            uint4 t = *reinterpret_cast<const uint4 *>(src + i);
+            v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        }
+    } else if constexpr (N == 2) {
+        uint2 t = *reinterpret_cast<const uint2 *>(src);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = src[i];
+    }
+}
+
 // Code bytes of one token: M key codes then M value codes.
 template <int M>
 struct Codes;
@@ -213,6 +232,7 @@ template <>
 struct Codes<4> {
     uint2 v;
     __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v2(p); }
+    __device__ __forceinline__ void load_shared(const unsigned char *p) { v = *reinterpret_cast<const uint2 *>(p); }
     __device__ __forceinline__ int k(int m) const { return static_cast<int>(__byte_perm(v.x, 0u, 0x4440u | m)); }
     __device__ __forceinline__ int vv(int m) const { return static_cast<int>(__byte_perm(v.y, 0u, 0x4440u | m)); }
 };
@@ -220,6 +240,7 @@ template <>
 struct Codes<8> {
     uint4 v;
     __device__ __forceinline__ void load_global(const uint8_t *p) { v = ld_global_na_v4(p); }
+    __device__ __forceinline__ void load_shared(const unsigned char *p) { v = *reinterpret_cast<const uint4 *>(p); }
     __device__ __forceinline__ int k(int m) const {
         return static_cast<int>(__byte_perm(m < 4 ? v.x : v.y, 0u, 0x4440u | (m & 3)));
     }
@@ -269,6 +290,29 @@ __device__ __forceinline__ void warp_argmin_into(float d, unsigned long long *sl
         atomicMin(slot, (static_cast<unsigned long long>(mn) << 32) | threadIdx.x);
 }
 
+// The new token's value codes of the owned subspaces (thread = codeword):
+// exact distances to its value sub-vectors xv [MC][DSUB], argmin into
+// keys[0..MC) (visible to all threads after the next barrier).
+template <int DSUB, int MC, int K, int NCH>
+__device__ __forceinline__ void encode_new_value(const __half *cbv, const float *xv, unsigned long long *keys) {
+    const int tid = threadIdx.x;
+    float dv[MC];
+#pragma unroll
+    for (int mi = 0; mi < MC; ++mi) {
+        const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
+        float d = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            unsigned long long f[4];
+            to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
+            d = sqdist8(d, xv + mi * DSUB + c * 8, f);
+        }
+        dv[mi] = d;
+    }
+#pragma unroll
+    for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[mi]);
+}
+
 template <int M, int G, int C, bool APPEND, bool E4M3>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
@@ -302,9 +346,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
+    // slices by TMA (one elected thread, hardware swizzle) when the base is
+    // 1024-byte aligned and a tensor map was made; else by per-thread 16-byte
+    // copies into the same layout (one arrival per thread)
+    const bool use_tma = !E4M3 && p.cb_map_ok && (smem_u32(smem) & 1023u) == 0;
     if (tid == 0) {
-        mbar_init(&bar[0], kThreads);                  // one cp.async arrival per thread
-        mbar_init(&bar[1], kThreads);
+        mbar_init(&bar[0], use_tma ? 1 : kThreads);
+        mbar_init(&bar[1], use_tma ? 1 : kThreads);
         mbar_init(&bar[2], 1);
         mbar_init(&bar[3], 1);
         mbar_init(&bar[4], 1);
@@ -340,9 +388,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // element offset of this CTA's K slice (the V slice is cb_unit further)
     const size_t gK = ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
                       static_cast<size_t>(rank) * S::CB_HALVES;
-    // the K slice now; the V slice, needed only after the scores, once the K
-    // slice has landed (own buffer) or is no longer read (shared buffer)
-    if (set_ok) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, gK, &bar[0]);
+    // TMA rows of the K slice (the V slice is M*K rows further)
+    const int rowK = ((set_ok ? set : 0) * Hkv + kvh) * 2 * M * K + rank * MC * K;
+    // the K slice now; the V slice too with its own buffer and TMA, else once
+    // the K slice has landed (own buffer) or is no longer read (shared buffer)
+    if (set_ok) {
+        if (use_tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, rowK + mi * K, &bar[0]);
+            }
+        } else {
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, gK, &bar[0]);
+        }
+    }
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -365,7 +425,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 }
             }
         }
-        if (set_ok) cp_async_wait_all();               // this thread's slice copies land first
+        if (set_ok) {
+            if (!use_tma) cp_async_wait_all();         // this thread's slice copies land first
+            else mbar_wait_bounded(&bar[0], 0);        // and the TMA copy
+        }
         return;
     }
     const int e0 = min(te, a0 + share);
@@ -432,7 +495,20 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
     // new token's K and V codes from the same rows --------------------------
     bool tmo = !mbar_wait_bounded(&bar[0], 0);
-    if constexpr (!S::SHARED_CB) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+    // the V slice into its own buffer once the K slice has landed, so that
+    // the K slice, which the table build waits for, has the bandwidth first
+    if constexpr (!S::SHARED_CB) {
+        if (use_tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi)
+                    tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
+            }
+        } else {
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+        }
+    }
     tmo |= !mbar_wait_bounded(&bar[4], 0);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
@@ -482,7 +558,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
     __syncthreads();                                   // every read of the K slice is done
-    if constexpr (S::SHARED_CB) copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+    if constexpr (S::SHARED_CB) {
+        if (use_tma) {
+            if (tid == 0) {
+                fence_proxy_async_shared();            // the K slice's reads precede the overwrite
+                mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi)
+                    tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
+            }
+        } else {
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+        }
+    }
     if constexpr (C > 1) {
         // this CTA's rows to every peer in one bulk copy each; the source is not
         // written again before every peer has received it (each peer scores,
@@ -510,22 +598,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             }
         }
     }
+    // with its own V buffer, the new value's codes while the peers' rows land
+    if constexpr (APPEND && !S::SHARED_CB) {
+        if (cl_new) {
+            tmo |= !mbar_wait_bounded(&bar[1], 0);
+            encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+        }
+    }
     if constexpr (C > 1) tmo |= !mbar_wait_bounded(&bar[2], 0);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     __syncthreads();
 
     // ---- scores, softmax statistics, value bins --------------------------------
-    // Scores by M table gathers stay in registers; the block's per-head max
-    // comes first, then each weight p = exp2(s - max) is added to the 256-bin
-    // value accumulators as the unsigned fixed-point integer
-    // round(p (2^32 - 2^12) / n), n = tokens this CTA streams (<= 2048): every
-    // p <= 1 to within the exp2 approximation, and the 2^12 margin covers that
-    // and the roundings, so no bin can overflow; integer shared-memory atomics
+    // Scores by M table gathers stay in registers.  The max of each warp's
+    // lanes of head g comes first, the weights relative to it and their sum
+    // next; the warps' (max, sum) pairs are merged with one barrier (PAM
+    // article §2.2.3 item 1: blockwise statistics merged by rescaling), so the
+    // block's max mx and weight sum lsum are known before any weight is
+    // binned.  Each weight
+    // p = 2^(s - mx) then enters the 256-bin value accumulators as the unsigned
+    // fixed-point integer round(p * 2^31 / lsum): the bins of one head sum to
+    // 2^31 (plus at most n/2 from rounding and a relative 2^-20 from the
+    // approximate exp2), so no bin can overflow 32 bits, and the weight lost to
+    // rounding is at most n/2 units of lsum/2^31, a relative n/2^32 of the
+    // block's weight (5e-7 at n = 2048 tokens).  Integer shared-memory atomics
     // are exact and fast, and the result does not depend on their order.  The
-    // per-head sum of the
-    // weights is reduced alongside.  The fused step's new token enters the
-    // max and the sum from its fresh codes; its value bin is added after the
-    // merge.
+    // fused step's new token enters the statistics from its fresh codes; its
+    // value bin is added after the merge.
     unsigned *ibins = reinterpret_cast<unsigned *>(bins);
     float s_new = -INFINITY;
     if constexpr (APPEND) {
@@ -537,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         }
     }
     float sc[TPT];
-    float mt = s_new;
+    float mloc = s_new;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
         if (i >= nslot) break;
@@ -546,56 +645,62 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
 #pragma unroll
             for (int m = 0; m < M; ++m) s += lut[(m * K + cc[i].k(m)) * G + g];
             sc[i] = s;
-            mt = fmaxf(mt, s);
+            mloc = fmaxf(mloc, s);
         }
     }
+    // the max over the lanes of head g (one redux for G = 1), this thread's
+    // weights relative to it (kept in sc) and their sum over the same lanes
+    float mg;
     if constexpr (G == 1) {
-        mt = warp_max_f32(mt);
+        mg = warp_max_f32(mloc);
     } else {
+        mg = mloc;
 #pragma unroll
-        for (int off = G; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+        for (int off = G; off < 32; off <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, off));
     }
-    if (lane < G) red_m[warp * G + lane] = mt;
-    __syncthreads();
-    float mx = red_m[g];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
-    const float qscale = __fdividef(4294963200.0f, static_cast<float>(max(eS - a0, 1)));
-    float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mx) : 0.f;
-    unsigned lq = 0;                                   // G == 1: the weights' fixed-point sum
+    float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mg) : 0.f;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
         if (i >= nslot) break;
         if (valid & (1u << i)) {
-            const float w = fast_exp2(sc[i] - mx);
-            const unsigned q = __float2uint_rn(w * qscale);
-            if constexpr (G == 1) lq += q;
-            else lt += w;
+            sc[i] = fast_exp2(sc[i] - mg);
+            lt += sc[i];
+        }
+    }
 #pragma unroll
-            for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
+    for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+    if (lane < G) {
+        red_m[warp * G + lane] = mg;
+        red_l[warp * G + lane] = lt;
+    }
+    __syncthreads();
+    float mx = red_m[g];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float mw = red_m[w * G + g];
+        if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+    }
+    // lsum >= 1 whenever this CTA holds a token of head g (its max weighs 1)
+    const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+    const float cfac = lsum * (1.0f / 2147483648.0f);  // integer bin -> weight
+    {
+        // weight relative to mx, in bin units: sc[i] * 2^(mg - mx) * qscale
+        const float rq = (mg == -INFINITY) ? 0.f : (mg == mx ? qscale : fast_exp2(mg - mx) * qscale);
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            if (i >= nslot) break;
+            if (valid & (1u << i)) {
+                const unsigned q = __float2uint_rn(sc[i] * rq);
+#pragma unroll
+                for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
+            }
         }
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the bins, for the bulk copies below
-    const float cfac = __fdividef(1.0f, qscale);       // integer bin -> weight
-    float lsum = 0.f;
-    if constexpr (G == 1) {
-        // the sum of the fixed-point weights, exact, then the new token's
-        lq = __reduce_add_sync(0xffffffffu, lq);
-        if (lane == 0) reinterpret_cast<unsigned *>(red_l)[warp] = lq;
-        __syncthreads();
-        unsigned qsum = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) qsum += reinterpret_cast<const unsigned *>(red_l)[w];
-        const float sn0 = snew[0];                     // this CTA's new token, if it holds it
-        lsum = static_cast<float>(qsum) * cfac + (sn0 != -INFINITY ? fast_exp2(sn0 - mx) : 0.f);
-    } else {
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-        if (lane < G) red_l[warp * G + lane] = lt;
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) lsum += red_l[w * G + g];
-    }
+    __syncthreads();                                   // every atomic of this CTA is done
 
     // ---- bins rows (integers, one bulk copy per peer) and statistics to the
     // peers that own them; sender rank lands in slot (rank - pr - 1) mod C ----
@@ -613,33 +718,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             st_async_f32(st + 4 * lane, mx, rbar);
             st_async_f32(st + 4 * (G + lane), lsum, rbar);
             st_async_f32(st + 4 * (2 * G + lane), snew[lane], rbar);
-            if (lane == 0) {
-                st_async_f32(st + 4 * (3 * G), __int_as_float(sflag[0]), rbar);
-                st_async_f32(st + 4 * (3 * G + 1), cfac, rbar);
-            }
+            st_async_f32(st + 4 * (3 * G + lane), cfac, rbar);
+            if (lane == 0) st_async_f32(st + 4 * (4 * G), __int_as_float(sflag[0]), rbar);
         }
     }
     // the new token's V codes (the peers' bins are landing meanwhile), then
     // its codes into its page slot, its page id checked here
     if constexpr (APPEND) {
         if (cl_new) {
-            if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-            float dv[MC];
-#pragma unroll
-            for (int mi = 0; mi < MC; ++mi) {
-                const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
-                float d = 0.f;
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    unsigned long long f[4];
-                    to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
-                    d = sqdist8(d, xnew + (MC + mi) * DSUB + c * 8, f);
-                }
-                dv[mi] = d;
+            if constexpr (S::SHARED_CB) {
+                if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+                encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+                __syncthreads();
             }
-#pragma unroll
-            for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[MC + mi]);
-            __syncthreads();
 #pragma unroll
             for (int mi = 0; mi < MC; ++mi) vcode[mi] = static_cast<int>(keys[MC + mi] & 0xffu);
             if (tid == 0) {
@@ -681,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             md[d] = sl[g];
             ld[d] = sl[G + g];
             sn = fmaxf(sn, sl[2 * G + g]);
-            pscale[d] = sl[3 * G + 1];
+            pscale[d] = sl[3 * G + g];
         }
 #pragma unroll
         for (int d = 0; d < C; ++d)
@@ -700,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     if (tid == 0) {
         int bb = sflag[0];
 #pragma unroll
-        for (int d = 1; d < C; ++d) bb |= __float_as_int(inc[(d - 1) * S::INC_STRIDE + S::ROW_FLOATS + 3 * G]);
+        for (int d = 1; d < C; ++d) bb |= __float_as_int(inc[(d - 1) * S::INC_STRIDE + S::ROW_FLOATS + 4 * G]);
         sflag[1] = bb;
         if (sflag[0]) flag_status(p.status, sflag[0]);
     }
@@ -849,19 +940,569 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ De
     p.out[bh * kHeadDim + d] = nan ? __int_as_float(0x7fc00000) : (den > 0.f ? num / den : 0.f);
 }
 
+// ============================================================================
+// Whole-split kernel.  One cluster of C CTAs per (request, kv head [, query-
+// head sub-group], split); CTA `rank` owns subspaces [rank*M/C, (rank+1)*M/C)
+// of both codebooks.  Unlike pq_decode_kernel, every CTA reads the codes of
+// all tokens of the split (whole 16-token pages, copied into shared memory;
+// the pages come from L2 after the first CTA's read) and scores all of
+// them, so every CTA holds the split's softmax statistics itself: only the
+// lookup-table rows cross the cluster.  Each CTA then bins the weights by its
+// own subspaces' value codes and applies its own value-codebook slice, which
+// gives its own output dimensions directly -- no exchange of value bins, no
+// merge.  The codebook slices arrive by TMA tensor copies whose hardware
+// swizzle places chunk c of row k where chunk_pos() expects it.
+//
+//  1. TMA: K and V codebook slices; cp.async: the split's code pages; the
+//     query group (after the dependency wait);
+//  2. LUT rows of the owned subspaces (AQPIM blog §4.1, §5.1 item 3), pushed
+//     to the peers; the fused step's new key encoded from the same rows;
+//  3. scores of every token of the split, s = sum_m LUT[m][kcode_m]; the
+//     split's (max, sum) per head (PAM article §2.2.3 item 1) by an online
+//     merge of per-thread pairs and one barrier;
+//  4. 256-bin value accumulators of the owned subspaces, fixed point relative
+//     to the split's weight sum; o = sum_k W[k] * C^V[k] for the owned dims;
+//  5. normalise and store, or store (max, sum, o) partials for the combine.
+// ============================================================================
+template <int M, int G, int C>
+struct AtCfg {
+    static constexpr int D = kHeadDim, K = kCodewords, P = kPage;
+    static constexpr int DSUB = D / M;
+    static constexpr int NCH = DSUB / 8;
+    static constexpr int MC = M / C;
+    static constexpr int SLICE_BYTES = MC * K * DSUB * 2;   // owned part of one codebook
+    static constexpr int LUT_FLOATS = M * K * G;
+    static constexpr int ROW_FLOATS = MC * K * G;           // this CTA's LUT rows
+    static constexpr int BIN_WORDS = MC * K * G;            // u32 value bins [MC][K][G]
+    static constexpr int TOK_PER_PASS = kThreads / G;
+    static constexpr int TPT = G == 8 ? 32 : 16;            // scores per thread, in registers
+    static constexpr int PAGE_BYTES = P * 2 * M;
+    static constexpr int CODE_CAP = 32768;                  // code bytes of one split
+    static constexpr int MAX_SPLIT = (TPT * TOK_PER_PASS < CODE_CAP / (2 * M) ? TPT * TOK_PER_PASS
+                                                                               : CODE_CAP / (2 * M)) / P * P;
+    static constexpr int NOUT = MC * DSUB * G;              // output elements of this CTA
+    // layout from the 1024-aligned base
+    static constexpr int OFF_CBK = 0;
+    static constexpr int OFF_CBV = SLICE_BYTES;
+    static constexpr int OFF_LUT = 2 * SLICE_BYTES;
+    static constexpr int OFF_BINS = OFF_LUT + LUT_FLOATS * 4;
+    static constexpr int OFF_Q = OFF_BINS + BIN_WORDS * 4;
+    static constexpr int OFF_PART = OFF_Q + G * D * 4;      // V-product partials [kWarps][NOUT]
+    static constexpr int OFF_RED = OFF_PART + kWarps * NOUT * 4;   // red_m, red_l [kWarps][G]
+    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mx, lsum, cfac, s_new [G]
+    static constexpr int OFF_NEW = OFF_STAT + 4 * G * 4;    // xnew [2][MC][DSUB] f32, newc [M]
+    static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + M * 4 + 7) / 8 * 8;  // [2][MC] u64
+    static constexpr int OFF_BAR = OFF_KEYS + 2 * MC * 8;   // K, V, codes, q, rows
+    static constexpr int OFF_FLAG = OFF_BAR + 5 * 8;
+    static constexpr int OFF_CODES = (OFF_FLAG + 16 + 15) / 16 * 16;
+    static size_t smem(int split_len) { return 1024 + OFF_CODES + static_cast<size_t>(split_len) * 2 * M; }
+    static_assert(K == kThreads, "one thread per codeword in the table build");
+    static_assert(SLICE_BYTES % 1024 == 0, "slices keep the swizzle alignment");
+    static_assert(OFF_LUT % 16 == 0 && OFF_Q % 16 == 0 && OFF_PART % 16 == 0, "alignment");
+    static_assert((MC * DSUB / 4) <= 32 && 32 % (MC * DSUB / 4) == 0, "V-product quads within a warp");
+    static_assert(ROW_FLOATS % 4 == 0, "bulk copies of whole rows");
+};
+
+template <int G>
+constexpr int kAtMinBlocks = G == 1 ? 4 : (G == 2 ? 3 : 2);
+
+template <int M, int G, int C, bool APPEND>
+__global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(const __grid_constant__ DecodeParams p) {
+    using S = AtCfg<M, G, C>;
+    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT, NCH = S::NCH;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
+    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
+    float *lut = reinterpret_cast<float *>(smem + S::OFF_LUT);
+    unsigned *bins = reinterpret_cast<unsigned *>(smem + S::OFF_BINS);
+    float *qs = reinterpret_cast<float *>(smem + S::OFF_Q);
+    float *part = reinterpret_cast<float *>(smem + S::OFF_PART);
+    float *red_m = reinterpret_cast<float *>(smem + S::OFF_RED);
+    float *red_l = red_m + kWarps * G;
+    float *st_mx = reinterpret_cast<float *>(smem + S::OFF_STAT);
+    float *st_l = st_mx + G, *st_c = st_l + G, *st_sn = st_c + G;
+    float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);      // [2][MC][DSUB]
+    int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);        // [M] key codes of the new token
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);  // K, V, codes, q, rows
+    int *sflag = reinterpret_cast<int *>(smem + S::OFF_FLAG);
+    const unsigned char *codes = smem + S::OFF_CODES;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int rank = 0;
+    if constexpr (C > 1) rank = static_cast<int>(cluster_ctarank());
+    const int split = blockIdx.x / C;
+    const int kvh = static_cast<int>(blockIdx.y >> p.head_split_log2), b = blockIdx.z;
+    const int hq0 = static_cast<int>(blockIdx.y) * G;
+    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+    const int S_ = p.num_splits;
+
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], i == 2 ? kThreads : 1);   // codes: one arrival per thread
+        fence_mbar_init();
+        sflag[0] = 0;
+    }
+    __syncthreads();
+    // ---- reads allowed before the preceding kernel completes: req_set,
+    // seq_lens, the block table, the codebooks and the code pages ------------
+    const int set = __ldg(p.req_set + b);
+    const int L_raw = __ldg(p.seq_lens + b);
+    const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
+    int bad0 = 0;
+    if (L_raw < 0 || L_raw > p.max_pages * P || L_raw > p.max_seq_len) bad0 |= AQ_DEV_BAD_LENGTH;
+    if (!set_ok) bad0 |= AQ_DEV_BAD_SET;
+    const int ts = split * p.split_len;
+    const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
+    if (bad0 || ts >= te) {
+        // nothing to read: NaN for a bad request, zeros / empty partials otherwise
+        grid_dependency_wait();
+        if (rank == 0) {
+            if (bad0 && tid == 0) flag_status(p.status, bad0);
+            const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
+            for (int i = tid; i < G * D; i += kThreads) {
+                const int gg = i / D, d = i % D;
+                const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
+                if (S_ == 1) p.out[bh * D + d] = v;
+                else if (d == 0) {
+                    p.part_ml[(bh * S_ + split) * 2 + 0] = bad0 ? v : -INFINITY;
+                    p.part_ml[(bh * S_ + split) * 2 + 1] = bad0 ? v : 0.0f;
+                }
+            }
+        }
+        return;
+    }
+    // the fused step's new token (position L-1, the last one) is scored from
+    // its fresh codes by every CTA of its split and streamed by none
+    const int new_pos = APPEND ? L_raw - 1 : -1;
+    const bool cl_new = APPEND && new_pos >= ts && new_pos < te;
+    const int ntok = (cl_new ? new_pos : te) - ts;   // streamed tokens [ts, ts + ntok)
+    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    if (tid == 0) {
+        // the two codebook slices: one 256-row TMA box per owned subspace
+        const int row0 = ((set * Hkv + kvh) * 2) * M * K + rank * MC * K;
+        mbar_arrive_expect_tx(&bar[0], S::SLICE_BYTES);
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, row0 + mi * K, &bar[0]);
+        mbar_arrive_expect_tx(&bar[1], S::SLICE_BYTES);
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, row0 + M * K + mi * K, &bar[1]);
+        if constexpr (C > 1) mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
+    }
+    {
+        // the split's code pages, whole pages (16 tokens x 2M codes of this kv
+        // head, one line each) into shared memory in token order: 16-byte
+        // cp.async chunks, consecutive threads along a page's line, page ids
+        // from the block table row (one line per page, so the reads are whole
+        // lines even under a shuffled table); one arrival per thread on bar[2]
+        constexpr int CPP = S::PAGE_BYTES / 16;          // chunks per page
+        const int npg = (ntok + P - 1) / P, pg0 = ts / P;
+        const size_t page_stride = static_cast<size_t>(Hkv) * S::PAGE_BYTES;
+        const unsigned char *src0 = p.code_pages + static_cast<size_t>(kvh) * S::PAGE_BYTES;
+        const uint32_t dst0 = smem_u32(codes);
+        bool bad = false;
+        for (int q = tid; q < npg * CPP; q += kThreads) {
+            const int j = q / CPP, c = q % CPP;
+            const int pg = __ldg(bt + pg0 + j);
+            if (pg >= 0 && static_cast<int64_t>(pg) < p.num_pages)
+                cp_async_16(dst0 + static_cast<uint32_t>(q) * 16u, src0 + static_cast<size_t>(pg) * page_stride + c * 16);
+            else
+                bad = true;
+        }
+        cp_async_mbar_arrive(&bar[2]);
+        if (bad) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+    }
+    // ---- the query and the new token come from the preceding kernel ----------
+    grid_dependency_wait();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[3], G * D * 4);
+        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + hq0) * D, G * D * 4, &bar[3]);
+    }
+    if constexpr (APPEND) {
+        if (cl_new && tid < 2 * MC * DSUB) {
+            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
+            xnew[tid] = __half2float(__ldg(reinterpret_cast<const __half *>(p.kv_new) +
+                                           ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D +
+                                           rank * MC * DSUB + r));
+        }
+    }
+    for (int i = tid; i < S::BIN_WORDS / 4; i += kThreads)
+        reinterpret_cast<uint4 *>(bins)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 2 * MC) keys[tid] = ~0ull;
+    grid_launch_dependents();                          // every read of this CTA is issued
+    __syncthreads();
+    if constexpr (C > 1) cluster_arrive_relaxed();     // this CTA's barriers are ready for pushes
+
+    // ---- lookup-table rows of the owned subspaces; the new key's codes -------
+    bool tmo = !mbar_wait_bounded(&bar[0], 0);
+    tmo |= !mbar_wait_bounded(&bar[3], 0);
+    if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
+    {
+        float dkv[MC];
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) {
+            const int m = rank * MC + mi;
+            const float *qm = qs + m * DSUB;
+            const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
+            unsigned long long acc2[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) acc2[gg] = 0ull;
+            float dk = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                unsigned long long f[4];
+                to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qm + gg * D + c * 8);
+                    const ulonglong2 qa = qv[0], qb = qv[1];
+                    unsigned long long a = acc2[gg];
+                    a = f2_fma(qa.x, f[0], a);
+                    a = f2_fma(qa.y, f[1], a);
+                    a = f2_fma(qb.x, f[2], a);
+                    a = f2_fma(qb.y, f[3], a);
+                    acc2[gg] = a;
+                }
+                if (APPEND && cl_new) dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
+            }
+            float acc[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                const float2 a = f2_unpack(acc2[gg]);
+                acc[gg] = (a.x + a.y) * p.scale_log2;
+            }
+            store_vec<G>(lut + (static_cast<size_t>(m) * K + tid) * G, acc);
+            dkv[mi] = dk;
+        }
+        if constexpr (APPEND) {
+            if (cl_new) {
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dkv[mi], &keys[mi]);
+            }
+        }
+    }
+    if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
+    __syncthreads();
+    if constexpr (C > 1) {
+        // this CTA's rows to every peer, one bulk copy each; the rows are not
+        // written again in this launch
+        if (tid < C - 1) {
+            const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) % C;
+            const uint32_t rows = smem_u32(lut + rank * S::ROW_FLOATS);
+            bulk_s2cluster(mapa_u32(rows, pr), rows, S::ROW_FLOATS * 4, mapa_u32(smem_u32(&bar[4]), pr));
+        }
+    }
+    if constexpr (APPEND) {
+        if (cl_new && tid < MC) {                      // the new key's code of subspace rank*MC + tid
+            const int m = rank * MC + tid;
+            const int code = static_cast<int>(keys[tid] & 0xffu);
+            newc[m] = code;
+            if constexpr (C > 1) {
+                const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[4]);
+#pragma unroll
+                for (int r = 1; r < C; ++r) {
+                    const uint32_t pr = static_cast<uint32_t>(rank + r) % C;
+                    st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
+                }
+            }
+        }
+    }
+    if constexpr (C > 1) tmo |= !mbar_wait_bounded(&bar[4], 0);
+    tmo |= !mbar_wait_bounded(&bar[2], 0);
+    if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    __syncthreads();                                   // the full table, the new key's codes
+    if constexpr (C > 1) cluster_arrive_relaxed();     // everything sent to this CTA has landed
+
+    // ---- scores and the split's softmax statistics ---------------------------
+    // Every thread keeps the (max, sum) pair of its tokens online; the pairs
+    // are merged over the lanes of head g and then over the warps (PAM article
+    // §2.2.3 item 1), so mx and lsum -- the same in every CTA of the cluster --
+    // are known before any weight is binned.
+    const int g = tid % G, jslot = tid / G;
+    float s_new = -INFINITY;
+    if constexpr (APPEND) {
+        if (cl_new && tid < G) {
+            s_new = 0.f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) s_new += lut[(m * K + newc[m]) * G + tid];
+        }
+    }
+    const int nslot = (ntok + S::TOK_PER_PASS - 1) / S::TOK_PER_PASS;
+    float sc[TPT];
+    float mloc = s_new;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+        if (i >= nslot) break;
+        const int r = jslot + i * S::TOK_PER_PASS;
+        if (r < ntok) {
+            Codes<M> cw;
+            cw.load_shared(codes + r * 2 * M);
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) s += lut[(m * K + cw.k(m)) * G + g];
+            sc[i] = s;
+            mloc = fmaxf(mloc, s);
+        }
+    }
+    float lloc = (s_new != -INFINITY) ? fast_exp2(s_new - mloc) : 0.f;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+        if (i >= nslot) break;
+        if (jslot + i * S::TOK_PER_PASS < ntok) {
+            sc[i] = fast_exp2(sc[i] - mloc);
+            lloc += sc[i];
+        }
+    }
+    {
+        float mt = mloc, lt = lloc;
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, mt, off);
+            const float l2 = __shfl_xor_sync(0xffffffffu, lt, off);
+            const float mn = fmaxf(mt, m2);
+            lt = (mt == mn ? lt : lt * fast_exp2(mt - mn)) + (m2 == mn ? l2 : l2 * fast_exp2(m2 - mn));
+            mt = mn;
+        }
+        if (lane < G) {
+            red_m[warp * G + lane] = mt;
+            red_l[warp * G + lane] = lt;
+        }
+    }
+    __syncthreads();
+    float mx = red_m[g];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float mw = red_m[w * G + g];
+        if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+    }
+    // value bins in fixed point: round(p * 2^31 / lsum) per token; the bins of
+    // one head sum to 2^31 (plus at most ntok/2 from rounding), and rounding
+    // loses at most a relative ntok/2^32 of the weight
+    const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+    const float cfac = lsum * (1.0f / 2147483648.0f);
+    if (tid < G) {
+        st_mx[tid] = mx;
+        st_l[tid] = lsum;
+        st_c[tid] = cfac;
+        st_sn[tid] = s_new;
+    }
+    // the new token's value codes of the owned subspaces
+    if constexpr (APPEND) {
+        if (cl_new) {
+            if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+            float dv[MC];
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) {
+                const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
+                float d = 0.f;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    unsigned long long f[4];
+                    to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
+                    d = sqdist8(d, xnew + (MC + mi) * DSUB + c * 8, f);
+                }
+                dv[mi] = d;
+            }
+#pragma unroll
+            for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[MC + mi]);
+        }
+    }
+    {
+        const float rq = (mloc == -INFINITY) ? 0.f : (mloc == mx ? qscale : fast_exp2(mloc - mx) * qscale);
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            if (i >= nslot) break;
+            const int r = jslot + i * S::TOK_PER_PASS;
+            if (r < ntok) {
+                Codes<M> cw;
+                cw.load_shared(codes + r * 2 * M);
+                const unsigned qv = __float2uint_rn(sc[i] * rq);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) atomicAdd(&bins[(mi * K + cw.vv(rank * MC + mi)) * G + g], qv);
+            }
+        }
+    }
+    __syncthreads();                                   // bins, statistics, the new value codes
+    int bad_all = sflag[0];
+    if constexpr (APPEND) {
+        if (cl_new && tid == 0) {
+            // this CTA's codes of the new token into its page slot
+            const int pg_new = __ldg(bt + new_pos / P);
+            if (pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages) {
+                uint8_t *dst = p.code_pages_w + ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) {
+                    dst[rank * MC + mi] = static_cast<uint8_t>(newc[rank * MC + mi]);
+                    dst[M + rank * MC + mi] = static_cast<uint8_t>(keys[MC + mi] & 0xffu);
+                }
+            } else {
+                atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+                bad_all |= AQ_DEV_BAD_PAGE;
+            }
+        }
+    }
+    if (!mbar_wait_bounded(&bar[1], 0)) {
+        atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+        bad_all |= AQ_DEV_TIMEOUT;
+    }
+
+    // ---- value codebook product for the owned dims -------------------------------
+    {
+        constexpr int NQ = MC * DSUB / 4, KSQ = kThreads / NQ, KSLQ = K / KSQ;
+        constexpr int ROWS128 = 128 / (DSUB * 2);
+        static_assert(KSQ % (ROWS128 * NCH) == 0, "row step keeps the swizzle position");
+        const int qd = tid % NQ, ks = tid / NQ;
+        const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
+        const int cj = j4 / 8, hj = j4 % 8;
+        constexpr int VPX = (M == 8 && C == 4) ? 2 : 1;
+        const int kx = ks ^ ((mi * VPX) & (KSQ - 1));
+        const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
+        const unsigned *wrow = bins + (static_cast<size_t>(mi) * K + kx) * G;
+        unsigned long long acc[G][2];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
+#pragma unroll 8
+        for (int i = 0; i < KSLQ; ++i) {
+            const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
+            const unsigned long long c01 = h2_to_f2p(cv2.x), c23 = h2_to_f2p(cv2.y);
+            unsigned wu[G];
+            load_vec_u<G>(wu, wrow + i * KSQ * G);
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                const float wf = static_cast<float>(wu[gg]);
+                const unsigned long long ww = f2_pack(wf, wf);
+                acc[gg][0] = f2_fma(ww, c01, acc[gg][0]);
+                acc[gg][1] = f2_fma(ww, c23, acc[gg][1]);
+            }
+        }
+        float accf[G][4];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const float2 a01 = f2_unpack(acc[gg][0]), a23 = f2_unpack(acc[gg][1]);
+            accf[gg][0] = a01.x; accf[gg][1] = a01.y; accf[gg][2] = a23.x; accf[gg][3] = a23.y;
+        }
+#pragma unroll
+        for (int off = NQ; off < 32; off <<= 1) {
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accf[gg][e] += __shfl_xor_sync(0xffffffffu, accf[gg][e], off);
+        }
+        if (lane < NQ) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v[G];
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) v[gg] = accf[gg][e];
+                store_vec<G>(part + (static_cast<size_t>(warp) * MC * DSUB + mi * DSUB + j4 + e) * G, v);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < S::NOUT; i += kThreads) {
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) o += part[static_cast<size_t>(w) * S::NOUT + i];
+        const int gg = i % G, dl = i / G;                 // dl in [0, MC*DSUB)
+        o *= st_c[gg];
+        if constexpr (APPEND) {
+            if (cl_new) {
+                // the new token: its weight times its value codeword
+                const int mi = dl / DSUB, j = dl % DSUB;
+                const int vc = static_cast<int>(keys[MC + mi] & 0xffu);
+                const float wn = fast_exp2(st_sn[gg] - st_mx[gg]);
+                o += wn * __half2float(cbv[((mi * K + vc) * NCH + chunk_pos<DSUB>(vc, j / 8)) * 8 + j % 8]);
+            }
+        }
+        const int d = rank * MC * DSUB + dl;
+        const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
+        const float nan = __int_as_float(0x7fc00000);
+        if (S_ == 1) {
+            const float l = st_l[gg];
+            p.out[bh * D + d] = bad_all ? nan : (l > 0.f ? __fdividef(o, l) : 0.f);
+        } else {
+            p.part_o[(bh * S_ + split) * D + d] = o;
+            if (rank == 0 && dl == 0) {
+                p.part_ml[(bh * S_ + split) * 2 + 0] = bad_all ? nan : st_mx[gg];
+                p.part_ml[(bh * S_ + split) * 2 + 1] = bad_all ? nan : st_l[gg];
+            }
+        }
+    }
+    if (tid == 0 && sflag[0]) flag_status(p.status, sflag[0]);
+    // A wait that ran out may leave a copy still landing: wait again (bounded)
+    // before the shared memory is released.
+    if (sflag[0] & AQ_DEV_TIMEOUT) {
+        cp_async_wait_all();
+        for (int i = 0; i < 4; ++i) mbar_wait_bounded(&bar[i], 0);
+        if constexpr (C > 1) mbar_wait_bounded(&bar[4], 0);
+    }
+    if constexpr (C > 1) cluster_wait_acquire();      // no CTA leaves while a peer may still read its rows
+}
+
+template <int M, int G, int C, bool APPEND>
+cudaError_t launch_attend(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
+    using S = AtCfg<M, G, C>;
+    auto kern = pq_attend_kernel<M, G, C, APPEND>;
+    if (plan.split_len > S::MAX_SPLIT || plan.split_len % kPage) return cudaErrorInvalidValue;
+    static SmemAttr attr_state;
+    const size_t need = S::smem(plan.split_len);
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), S::smem(S::MAX_SPLIT));
+        e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits),
+                       static_cast<unsigned>(p.num_kv_heads) << p.head_split_log2,
+                       static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = need;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.overlap ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int M, int G, bool APPEND>
+cudaError_t attend_c(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
+    switch (plan.cluster) {
+        case 2: return launch_attend<M, G, 2, APPEND>(p, plan, s);
+        case 4: return launch_attend<M, G, 4, APPEND>(p, plan, s);
+        case 8:
+            if constexpr (M == 8) return launch_attend<M, G, 8, APPEND>(p, plan, s);
+            else return cudaErrorInvalidConfiguration;
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+template <int M, bool APPEND>
+cudaError_t attend_g(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s) {
+    switch (G) {
+        case 1: return attend_c<M, 1, APPEND>(p, plan, s);
+        case 2: return attend_c<M, 2, APPEND>(p, plan, s);
+        case 4: return attend_c<M, 4, APPEND>(p, plan, s);
+        case 8: return attend_c<M, 8, APPEND>(p, plan, s);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
 template <int M, int G, int C, bool APPEND, bool E4M3>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
     auto kern = pq_decode_kernel<M, G, C, APPEND, E4M3>;
     if (plan.share > S::MAX_SHARE || plan.share % kPage) return cudaErrorInvalidValue;
-    static size_t attr_bytes = 0;                  // opt-in dynamic shared memory set so far
+    static SmemAttr attr_state;                    // opt-in dynamic shared memory, per device
     const size_t need = S::smem();
-    if (need > attr_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(need));
-        if (e != cudaSuccess) return e;
-        attr_bytes = need;
-    }
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), need); e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits),
                        static_cast<unsigned>(p.num_kv_heads) << p.head_split_log2,
@@ -931,6 +1572,24 @@ size_t pq_decode_smem_bytes(int M, int G, int cluster) {
     return 0;
 }
 
+size_t pq_attend_smem_bytes(int M, int G, int cluster, int split_len) {
+#define AQ_AS(MM, GG, CC) \
+    if (M == MM && G == GG && cluster == CC) return AtCfg<MM, GG, CC>::smem(split_len);
+    AQ_AS(4, 1, 2) AQ_AS(4, 1, 4) AQ_AS(4, 2, 2) AQ_AS(4, 2, 4) AQ_AS(4, 4, 2) AQ_AS(4, 4, 4) AQ_AS(4, 8, 2) AQ_AS(4, 8, 4)
+    AQ_AS(8, 1, 2) AQ_AS(8, 1, 4) AQ_AS(8, 1, 8) AQ_AS(8, 2, 2) AQ_AS(8, 2, 4) AQ_AS(8, 2, 8)
+    AQ_AS(8, 4, 2) AQ_AS(8, 4, 4) AQ_AS(8, 4, 8) AQ_AS(8, 8, 2) AQ_AS(8, 8, 4) AQ_AS(8, 8, 8)
+#undef AQ_AS
+    return 0;
+}
+
+int pq_attend_max_split(int M, int G) {
+#define AQ_AM(MM, GG) \
+    if (M == MM && G == GG) return AtCfg<MM, GG, 2>::MAX_SPLIT;
+    AQ_AM(4, 1) AQ_AM(4, 2) AQ_AM(4, 4) AQ_AM(4, 8) AQ_AM(8, 1) AQ_AM(8, 2) AQ_AM(8, 4) AQ_AM(8, 8)
+#undef AQ_AM
+    return 0;
+}
+
 int pq_decode_max_share(int M, int G) {
 #define AQ_MS(MM, GG) \
     if (M == MM && G == GG) return PqCfg<MM, GG, 1>::MAX_SHARE;
@@ -944,7 +1603,8 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
     cudaError_t e;
     G /= plan.head_split;                          // query heads per cluster
     if (p.codebook_e4m3) return cudaErrorInvalidValue;          // E4M3 codebooks: the fused step only
-    if (M == 4) e = dispatch_g<4, false, false>(p, G, plan, s);
+    if (plan.kernel == 2) e = M == 4 ? attend_g<4, false>(p, G, plan, s) : attend_g<8, false>(p, G, plan, s);
+    else if (M == 4) e = dispatch_g<4, false, false>(p, G, plan, s);
     else if (M == 8) e = dispatch_g<8, false, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
@@ -955,7 +1615,9 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
 cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
     G /= plan.head_split;
-    if (M == 4) e = p.codebook_e4m3 ? dispatch_g<4, true, true>(p, G, plan, s) : dispatch_g<4, true, false>(p, G, plan, s);
+    if (plan.kernel == 2 && !p.codebook_e4m3)
+        e = M == 4 ? attend_g<4, true>(p, G, plan, s) : attend_g<8, true>(p, G, plan, s);
+    else if (M == 4) e = p.codebook_e4m3 ? dispatch_g<4, true, true>(p, G, plan, s) : dispatch_g<4, true, false>(p, G, plan, s);
     else if (M == 8) e = p.codebook_e4m3 ? dispatch_g<8, true, true>(p, G, plan, s) : dispatch_g<8, true, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;

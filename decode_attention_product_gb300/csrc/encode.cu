@@ -480,13 +480,11 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_mma_kernel(const __grid
 
 template <int M>
 static cudaError_t launch_encode_mma(const EncodeParams &p, cudaStream_t s) {
-    static bool configured = false;                       // attribute set once per process
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(encode_mma_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             EncMma<M>::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static SmemAttr attr_state;                           // opt-in dynamic shared memory, per device
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(encode_mma_kernel<M>),
+                                         EncMma<M>::SMEM);
+        e != cudaSuccess)
+        return e;
     dim3 grid(static_cast<unsigned>((p.num_tokens + kTile - 1) / kTile), static_cast<unsigned>(p.num_kv_heads), 2u);
     encode_mma_kernel<M><<<grid, kEncThreads, EncMma<M>::SMEM, s>>>(p);
     return cudaGetLastError();

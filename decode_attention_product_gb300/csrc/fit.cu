@@ -178,13 +178,11 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
 template <int M>
 cudaError_t launch_m(const FitParams &p, cudaStream_t s) {
     const size_t smem = FitCfg<M>::smem(p.n_samples);
-    static size_t attr_bytes = 0;
-    if (smem > attr_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(fit_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(FitCfg<M>::smem(kMaxSamples)));
-        if (e != cudaSuccess) return e;
-        attr_bytes = FitCfg<M>::smem(kMaxSamples);
-    }
+    static SmemAttr attr_state;                    // opt-in dynamic shared memory, per device
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(fit_kernel<M>),
+                                         FitCfg<M>::smem(kMaxSamples));
+        e != cudaSuccess)
+        return e;
     dim3 grid(static_cast<unsigned>(p.num_units), static_cast<unsigned>(M));
     fit_kernel<M><<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();

@@ -2,13 +2,20 @@
 // C-ABI layer (api.cu) and the kernel translation units.  Not installed.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace aq {
 
 struct DecodeParams {
+    // TMA view of the codebooks as rows of Dsub fp16 elements
+    // ([S * Hkv * 2 * M * K] rows), swizzled like the shared-memory slices
+    // (PQ kernel with whole-split scoring)
+    CUtensorMap cb_map;
     const float *q;             // [B][Hq][D]
     const uint8_t *code_pages;  // [NP][Hkv][P][2][M]
     const void *codebooks;      // fp16 [S][Hkv][2][M][K][Dsub]
@@ -29,6 +36,7 @@ struct DecodeParams {
     int32_t overlap;        // launched as a programmatic dependent of the previous kernel
     int32_t head_split_log2;  // PQ: 2^this clusters per kv head, each for Hq/Hkv >> this query heads
     int32_t codebook_e4m3;    // PQ step: codebooks are FP8 E4M3 codes, same layout
+    int32_t cb_map_ok;        // cb_map describes the codebooks (fp16, TMA-addressable)
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -55,6 +63,7 @@ struct FitParams {
 };
 
 struct Plan {
+    int32_t kernel;       // PQ: 1 = per-CTA token shares with merged bins, 2 = whole-split scoring
     int32_t num_splits;
     int32_t cluster;      // CTAs per split
     int32_t split_len;    // tokens per split (multiple of the page size)
@@ -80,6 +89,11 @@ cudaError_t launch_fit(const FitParams &p, int M, cudaStream_t s);
 
 // Shared-memory bytes a PQ decode CTA needs for (M, G, cluster).
 size_t pq_decode_smem_bytes(int M, int G, int cluster);
+// Whole-split kernel: shared-memory bytes for a split of `split_len` tokens
+// (0 for an unsupported (M, G, cluster)), and the most tokens one split may
+// hold (its codes in shared memory, its scores in registers).
+size_t pq_attend_smem_bytes(int M, int G, int cluster, int split_len);
+int pq_attend_max_split(int M, int G);
 // Largest token share one cluster CTA handles (its tokens' codes live in
 // registers, a fixed number per thread); 0 for an unsupported (M, G).
 int pq_decode_max_share(int M, int G);
@@ -87,5 +101,18 @@ size_t fit_smem_bytes(int M, int n_samples);
 // Record a CUDA error for aq_last_error_message() and clear the runtime's
 // last-error state.
 void record_cuda_error(cudaError_t e);
+
+// Opt-in dynamic shared memory already granted to one kernel, per device
+// ordinal: cudaFuncSetAttribute acts on the current device's context only, so
+// a size set while device 0 was current says nothing about device 1.
+constexpr int kMaxDevices = 64;
+struct SmemAttr {
+    std::mutex mu;
+    size_t bytes[kMaxDevices] = {};
+};
+// Make sure `func` may launch with `need` bytes of dynamic shared memory on the
+// current device (sets the attribute the first time a larger size is asked
+// for on that device; thread-safe).
+cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need);
 
 }  // namespace aq

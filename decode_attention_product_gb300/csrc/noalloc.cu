@@ -15,7 +15,9 @@
 // In host code its name is only a stand-in, so its device address is looked up
 // with cudaGetSymbolAddress, once per device, on the first call made while that
 // device is current; that first call should therefore come before any stream
-// capture.  All calls share the one array and nothing in it is kept for the
+// capture.  The address is kept until the process exits: a cudaDeviceReset of
+// the device invalidates it, and the entry point is not to be called on that
+// device afterwards.  All calls share the one array and nothing in it is kept for the
 // caller: every partial is written by the split kernel before the combine
 // kernel reads it, so it needs no clearing, but two calls whose kernels overlap
 // on the GPU (different streams or host threads) race on it.

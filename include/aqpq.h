@@ -333,9 +333,11 @@ aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch,
  * (D + 2) * 4 bytes) returns AQ_ERR_WORKSPACE_TOO_SMALL before any launch; no
  * call allocates or frees memory.  The array's device address is looked up
  * once per device by the first call made with that device current, so make
- * that first call before any stream capture.  All calls share the array: two
- * calls whose kernels overlap on the GPU (other streams, other host threads)
- * race on it.  Nothing in it needs clearing between calls.
+ * that first call before any stream capture.  The address is kept for the
+ * life of the process: after cudaDeviceReset on a device it is stale, and this
+ * entry point must not be called on that device again.  All calls share the
+ * array: two calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on it.  Nothing in it needs clearing between calls.
  * ------------------------------------------------------------------------- */
 aq_status aq_decode_attention_noalloc(const aq_pq_config *cfg, int32_t batch,
                                       int32_t num_q_heads, int32_t num_kv_heads,

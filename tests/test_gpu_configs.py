@@ -1,0 +1,197 @@
+"""GPU parity on the benchmark workloads themselves, built the way a serving
+system (and bench.py) builds them: codebooks fitted on the GPU on each
+request's first 64 tokens, every cached token but the last encoded by the GPU
+prefill path, then one fused decode step (aq_decode_step) that appends the
+last token and attends over all of them.
+
+The GPU runs each workload at full size, so the decode launch has the plan
+bench.py times (page1: the token-share kernel in clusters of 4; ragged: the
+token-share kernel in clusters of 2, 2048 tokens per CTA for the 4096-token
+requests; long: the token-share kernel, 16 splits of clusters of 8 with the
+outlier channels; qwen_gqa: the whole-split kernel, clusters of 4 CTAs each
+scoring all 1000 tokens for 8 query heads).  The oracle repeats fit, encode and decode from the same raw
+vectors for a stated subset of (request, kv head) pairs -- every pair for page1
+and qwen_gqa -- and the GPU results are compared on that subset:
+
+  * codebooks bit-exact (the fit's arithmetic is exact on both sides);
+  * codes bit-exact where the oracle's relative runner-up gap exceeds 1e-4, and
+    (same fp32 decision arithmetic) everywhere;
+  * outputs within |o - o*| <= 2e-3 + 2e-3 |o*|.
+
+Every case runs again with the codebooks stored as FP8 E4M3 (AQPIM blog §4.2):
+the prefill encodes against their exact fp16 widening, the step reads the codes.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 2e-3
+GAP = 1e-4
+
+
+@pytest.fixture(scope="module")
+def A():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_attention_product_gb300 import build
+    build.build()
+    from decode_attention_product_gb300 import api
+    return api
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def close(got, want):
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    err = np.abs(got - want)
+    bad = err > ATOL + RTOL * np.abs(want)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tol; max err {err.max():.3e}"
+    return float(err.max())
+
+
+def gpu_pipeline(A, w, kvs, e4m3):
+    """Fit, prefill-encode tokens [0, L-1) and run one fused step on the GPU
+    for every request and head of workload w.  Returns host copies of the
+    fp16 codebooks, the code pages after the step and the step's output."""
+    B, Hkv, M = w.batch, w.num_kv_heads, w.num_subspaces
+    samples = np.stack([w.fit_samples(k) for k in kvs])              # [B][Hkv][2][N][D]
+    cb = A.fit_codebooks(dev(samples.reshape(-1, *samples.shape[3:])), M, w.fit_iters)
+    cb = cb.view(B, Hkv, 2, M, 256, w.dsub)
+    cb_step = cb
+    if e4m3:
+        cb_step = A.to_e4m3(cb)
+        cb = A.from_e4m3(cb_step)                                    # the exact widening
+    bt, npages = w.block_table()
+    kv = np.concatenate([k[:-1] for k in kvs])
+    tset = np.concatenate([np.full(len(k) - 1, b, np.int32) for b, k in enumerate(kvs)])
+    slots = np.concatenate([w.slot_mapping(bt, b, 0, len(k) - 1) for b, k in enumerate(kvs)])
+    pages = torch.zeros((npages, Hkv, 16, 2, M), dtype=torch.uint8, device="cuda")
+    st = A.new_status()
+    A.encode_append(dev(kv), dev(tset), dev(slots), cb, pages, st)
+    del kv
+    last = np.stack([k[-1] for k in kvs])                              # [B][Hkv][2][D]
+    Lmax = int(w.seq_lens.max())
+    q = w.queries()
+    out = A.decode_step(dev(q), dev(last), pages, cb_step, torch.arange(B, dtype=torch.int32, device="cuda"),
+                        dev(bt), dev(w.seq_lens), Lmax, w.scale, overlap=False, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return cb.cpu().numpy(), pages.cpu().numpy(), out.cpu().numpy(), q, bt
+
+
+def oracle_pipeline(orc, w, kvs, reqs, heads, e4m3):
+    """The oracle's fit, encode (all L tokens) and decode for requests `reqs`
+    and kv heads `heads` only (attention is independent per (request, kv
+    head)).  Returns (fp16 codebooks [R][H][2][M][K][Dsub], code pages
+    [NP][H][P][2][M], gaps per token list, output [R][H*G][D])."""
+    M, G = w.num_subspaces, w.group
+    R, H = len(reqs), len(heads)
+    samples = np.stack([w.fit_samples(kvs[b][:, heads]) for b in reqs])   # [R][H][2][N][D]
+    cb16, _, _, _ = orc.kmeans_fit(samples.reshape(-1, *samples.shape[3:]), M, 256, w.fit_iters)
+    cb16 = cb16.reshape(R, H, 2, M, 256, w.dsub)
+    cbw = cb16
+    if e4m3:
+        cbw = orc.e4m3_to_float(orc.e4m3_from_float(cb16.astype(np.float32))).astype(np.float16)
+    bt, npages = w.block_table()
+    kv = np.concatenate([kvs[b][:, heads] for b in reqs])
+    tset = np.concatenate([np.full(int(w.seq_lens[b]), i, np.int32) for i, b in enumerate(reqs)])
+    slots = np.concatenate([w.slot_mapping(bt, b, 0, int(w.seq_lens[b])) for b in reqs])
+    pages = np.zeros((npages, H, 16, 2, M), np.uint8)
+    gap = orc.encode_append(kv, tset, slots, cbw, pages, 16)
+    del kv
+    qh = np.concatenate([np.arange(h * G, (h + 1) * G) for h in heads])
+    q = w.queries()[np.asarray(reqs)][:, qh]
+    out = orc.decode_attention(q, pages, cbw, np.arange(R, dtype=np.int32), bt[np.asarray(reqs)],
+                               w.seq_lens[np.asarray(reqs)], w.scale, 16)
+    return cb16, cbw, pages, slots, gap, out, qh
+
+
+def check_config(A, orc, w, reqs, heads, e4m3):
+    kvs = w.kv_all(threads=16)
+    g_cb, g_pages, g_out, _, _ = gpu_pipeline(A, w, kvs, e4m3)
+    cb16, cbw, o_pages, slots, gap, o_out, qh = oracle_pipeline(orc, w, kvs, reqs, heads, e4m3)
+    r, h = np.asarray(reqs), np.asarray(heads)
+    # codebooks (the GPU's are the widened ones with e4m3)
+    want_cb = cbw if e4m3 else cb16
+    assert np.array_equal(g_cb[r][:, h].view(np.uint16), want_cb.view(np.uint16))
+    # codes of every token of the subset, the step's new token included
+    pg, sl = slots // 16, slots % 16
+    gc = g_pages[pg, :, sl][:, h]                                     # [T][H][2][M]
+    oc = o_pages[pg, :, sl]
+    clear = gap > GAP
+    assert np.array_equal(gc[clear], oc[clear])
+    assert np.array_equal(gc, oc)
+    # outputs of the subset's query heads
+    err = close(g_out[r][:, qh], o_out)
+    return err, clear.mean()
+
+
+# (workload, requests compared, kv heads compared)
+def _ragged_subset(w):
+    """32 requests: the first 12 of 4096 tokens (2048 tokens per CTA on the
+    clusters-of-2 plan) and the first 20 shorter ones, in batch order."""
+    lens = w.seq_lens
+    longs = [b for b in range(w.batch) if lens[b] == 4096][:12]
+    shorts = [b for b in range(w.batch) if lens[b] != 4096][:20]
+    return sorted(longs + shorts)
+
+
+CONFIGS = {
+    "page1": (lambda w: list(range(w.batch)), lambda w: list(range(w.num_kv_heads))),
+    "qwen_gqa": (lambda w: list(range(w.batch)), lambda w: list(range(w.num_kv_heads))),
+    "ragged": (_ragged_subset, lambda w: [0, 13, 31]),
+    "long": (lambda w: [0], lambda w: [0, 17]),
+}
+
+
+@pytest.mark.parametrize("e4m3", [False, True], ids=["fp16_codebooks", "e4m3_codebooks"])
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_workload_pipeline_matches_oracle(A, orc, name, e4m3):
+    w = W.make(name)
+    if name == "qwen_gqa":
+        w.layers = 1                                    # one layer of the stack
+    reqs_fn, heads_fn = CONFIGS[name]
+    reqs, heads = reqs_fn(w), heads_fn(w)
+    plan = A.decode_plan(w.batch, w.num_q_heads, w.num_kv_heads, int(w.seq_lens.max()), w.num_subspaces)
+    expect = {"page1": (1, 4), "ragged": (1, 2), "long": (16, 8), "qwen_gqa": (1, 4)}[name]
+    assert plan[:2] == expect, plan
+    err, clear = check_config(A, orc, w, reqs, heads, e4m3)
+    assert clear > 0.99
+
+
+# --------------------------------------------------------------------------
+# a peaked softmax with large values, 2048 tokens per CTA
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("kernel", ["1", "2"])
+@pytest.mark.parametrize("kscale", [1.0, 4.0, 8.0])
+def test_peaked_softmax_large_values(A, orc, kscale, kernel, monkeypatch):
+    """48 requests of 4096 tokens x 32 heads: on the token-share kernel the
+    clusters-of-2 plan, each CTA streaming 2048 tokens; on the whole-split
+    kernel every CTA scores all 4096.  Key codebooks scaled by `kscale` make the softmax
+    peaked (scores spread over tens of units: most weights are below 2^-20 of
+    the largest), value codebooks scaled to |v| ~ 50.  The value bins are fixed
+    point relative to each CTA's weight sum, so the tiny weights' share stays
+    within the tolerance."""
+    B, H, M, L = 48, 32, 4, 4096
+    p = W.paged_codes_problem(97 + int(kscale), B, H, H, M, [L] * B, num_sets=B)
+    cb = p["codebooks"].astype(np.float32)
+    cb[:, :, 0] *= kscale
+    cb[:, :, 1] *= 50.0
+    p["codebooks"] = cb.astype(np.float16)
+    monkeypatch.setenv("AQPQ_DECODE_KERNEL", kernel)
+    assert A.decode_plan(B, H, H, L, M)[:2] == ((1, 2) if kernel == "1" else (1, 4))
+    st = A.new_status()
+    out = A.decode_attention(dev(p["q"]), dev(p["code_pages"]), dev(p["codebooks"]), dev(p["req_set"]),
+                             dev(p["block_table"]), dev(p["seq_lens"]), L, 1.0 / np.sqrt(128), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = orc.decode_attention(p["q"], p["code_pages"], p["codebooks"], p["req_set"], p["block_table"],
+                                p["seq_lens"], 1.0 / np.sqrt(128), 16)
+    close(out.cpu().numpy(), want)

@@ -17,6 +17,22 @@ ATOL = RTOL = 2e-3
 GAP = 1e-4
 
 
+@pytest.fixture(params=["auto", "1", "2"])
+def kernel(request, monkeypatch):
+    """Which PQ decode kernel the planner may use: its own choice, the
+    token-share kernel, or the whole-split kernel (where a split fits)."""
+    if request.param == "auto":
+        monkeypatch.delenv("AQPQ_DECODE_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("AQPQ_DECODE_KERNEL", request.param)
+    return request.param
+
+
+@pytest.fixture
+def kernel1(monkeypatch):
+    monkeypatch.setenv("AQPQ_DECODE_KERNEL", "1")
+
+
 @pytest.fixture(scope="module")
 def A():
     if not torch.cuda.is_available():
@@ -79,7 +95,7 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}M{c[3]}" for c in CASES])
 @pytest.mark.parametrize("splits", [0, 1, 2, 7])
-def test_decode_matches_oracle(A, orc, case, splits):
+def test_decode_matches_oracle(A, orc, case, splits, kernel):
     B, Hq, Hkv, M, lens = case
     p = W.paged_codes_problem(hash((B, Hq, Hkv, M, tuple(lens))) % 10000, B, Hq, Hkv, M, lens,
                               num_sets=B + 1)
@@ -100,7 +116,7 @@ def _many_lens(n, seed):
 
 
 @pytest.mark.parametrize("case", MANY, ids=[f"B{c[0]}H{c[1]}M{c[3]}" for c in MANY])
-def test_decode_many_units_cluster2(A, orc, case):
+def test_decode_many_units_cluster2(A, orc, case, kernel1):
     B, Hq, Hkv, M = case
     lens = _many_lens(B, M)
     assert A.decode_plan(B, Hq, Hkv, max(lens), M)[1] == 2
@@ -110,7 +126,7 @@ def test_decode_many_units_cluster2(A, orc, case):
     close(got, oracle_pq(orc, p))
 
 
-def test_decode_plan_variants_agree(A, orc):
+def test_decode_plan_variants_agree(A, orc, kernel):
     """Cluster sizes 4 and the split counts the planner picks for the long shape
     give the same answer as the oracle."""
     p = W.paged_codes_problem(5, 1, 4, 4, 8, [20000], num_sets=1)
@@ -121,7 +137,7 @@ def test_decode_plan_variants_agree(A, orc):
         close(got, want)
 
 
-def test_decode_repeated_calls_agree(A):
+def test_decode_repeated_calls_agree(A, kernel):
     """The value bins accumulate as unsigned fixed-point integers, so the order
     of the shared-memory atomics cannot change them, and every other reduction
     has a fixed order: repeated calls agree bit for bit."""
@@ -131,7 +147,7 @@ def test_decode_repeated_calls_agree(A):
     assert np.array_equal(a, b)
 
 
-def test_decode_data_errors_flag_and_nan(A):
+def test_decode_data_errors_flag_and_nan(A, kernel):
     p = W.paged_codes_problem(7, 3, 4, 4, 4, [40, 40, 40], num_sets=3)
     # request 0: block-table entry outside the pool; request 1: set outside the array
     p["block_table"][0, 1] = p["num_pages"] + 5
@@ -395,7 +411,7 @@ STEP_CASES = [
 @pytest.mark.parametrize("case", STEP_CASES, ids=[f"B{c[0]}Hq{c[1]}Hkv{c[2]}M{c[3]}" for c in STEP_CASES])
 @pytest.mark.parametrize("splits", [0, 1, 3])
 @pytest.mark.parametrize("overlap", [False, True])
-def test_decode_step_matches_oracle(A, orc, case, splits, overlap):
+def test_decode_step_matches_oracle(A, orc, case, splits, overlap, kernel):
     B, Hq, Hkv, M, lens = case
     p = W.paged_codes_problem(hash((B, Hq, M, tuple(lens), 7)) % 10000, B, Hq, Hkv, M, lens,
                               num_sets=B + 1)
@@ -452,7 +468,7 @@ def test_decode_step_e4m3_codebooks(A, orc, case, splits):
 
 @pytest.mark.parametrize("case", MANY, ids=[f"B{c[0]}H{c[1]}M{c[3]}" for c in MANY])
 @pytest.mark.parametrize("overlap", [False, True])
-def test_decode_step_many_units_cluster2(A, orc, case, overlap):
+def test_decode_step_many_units_cluster2(A, orc, case, overlap, kernel1):
     B, Hq, Hkv, M = case
     lens = _many_lens(B, M + 1)
     assert A.decode_plan(B, Hq, Hkv, max(lens), M)[1] == 2
@@ -474,7 +490,7 @@ def test_decode_step_many_units_cluster2(A, orc, case, overlap):
     close(out.cpu().numpy(), want)
 
 
-def test_decode_step_equals_append_then_decode(A):
+def test_decode_step_equals_append_then_decode(A, kernel):
     """The fused step gives the two-call sequence's codes and (to fp32
     rounding) its output."""
     p = W.paged_codes_problem(77, 4, 32, 32, 4, [2048] * 4)
@@ -492,7 +508,7 @@ def test_decode_step_equals_append_then_decode(A):
     assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-6)
 
 
-def test_decode_step_bad_new_page_flagged(A):
+def test_decode_step_bad_new_page_flagged(A, kernel):
     """The new token's page id outside the pool: bad-page status, NaN output for
     that request, no code written anywhere for it, the other request intact."""
     p = W.paged_codes_problem(9, 2, 4, 4, 4, [40, 40], num_sets=2)

@@ -64,6 +64,8 @@ def test_noalloc_matches_workspace_entry_point(splits):
         assert int(status.item()) == 0
         got = out.cpu().numpy().astype(np.float64)
         assert np.all(np.abs(got - ref) <= TOL + TOL * np.abs(ref))
+        # same plan, same kernels, only the scratch differs: bit-identical
+        assert np.array_equal(got, ref)
 
 
 def test_noalloc_rejects_scratch_beyond_its_array():
