@@ -527,6 +527,8 @@ def run_ours(args, w, rank, world, local_rank):
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
     sweep = (measure_layer_sweep(args, w, api, torch, base, Lmax, T)
              if w.layers > 1 and not args.two_call else None)
+    mixed = (measure_mixed(args, w, api, torch, T, base, max(1, w.num_kv_heads // 8), local_rank)
+             if not args.two_call else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "steps_timed": n_timed, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -553,6 +555,8 @@ def run_ours(args, w, rank, world, local_rank):
         line["e4m3_codebooks"] = main["e4m3_codebooks"]
     if sweep:
         line["layer_sweep"] = sweep
+    if mixed:
+        line["mixed_precision"] = mixed
     if args.two_call:
         line["append"] = {"us_per_step": (ms - roof["launch_ms"]) * 1e3,
                           "how": "step time minus the decode launch's time"}
@@ -717,6 +721,61 @@ def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
             "us_per_layer": graph_ms * 1e3 / w.layers, "value": units / (graph_ms / 1e3), "unit": UNIT,
             "gbs": byt / (graph_ms / 1e3) / 1e9, "frac_of_peak": byt / (graph_ms / 1e3) / 1e9 / peak,
             "plan": {"splits": splits, "cluster": cluster}}
+
+
+def measure_mixed(args, w, api, torch, T, base, n16, local_rank=0):
+    """The mixed-precision step (AQPIM blog §6.1 item 4): kv heads [0, n16)
+    keep fp16 pages of the same raw vectors, the others the PQ cache; one
+    aq_decode_step_mixed per step (PQ step, fp16 append, fp16 attention),
+    timed like the main step over rotated copies larger than 2 x L2."""
+    Hq, Hkv, M = w.num_q_heads, w.num_kv_heads, w.num_subspaces
+    G = Hq // Hkv
+    Lmax = int(w.seq_lens.max())
+    bt, npages = base["bt_np"], base["npages"]
+    kvp = np.zeros((npages, n16, 2, 16, 128), np.float16)
+    for b, k in enumerate(base["kvs"]):
+        t = np.arange(len(k))
+        kvp[bt[b, t // 16], :, :, t % 16] = k[:, :n16]
+    mb = dict(base, codebooks=base["codebooks"][:, n16:].contiguous(), pages=base["pages"][:, n16:].contiguous(),
+              kvp=torch.from_numpy(kvp).cuda())
+    l2 = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    copies, R, per_copy = rotation(mb, torch, l2, keys=("codebooks", "pages", "q", "new_kv", "kvp"))
+    out = torch.empty((w.batch, Hq, 128), dtype=torch.float32, device="cuda")
+    st = api.new_status()
+    w_b = ctypes_workspace(api, w, n16, Lmax, torch)
+
+    def step(i):
+        c = copies[i % R]
+        api.decode_step_mixed(c["q"], c["new_kv"], n16, c["kvp"], c["pages"], c["codebooks"], c["req_set"], c["bt"],
+                              c["seq_lens"], Lmax, num_subspaces=M, scale=w.scale, overlap=True, out=out,
+                              workspace=w_b, status=st)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    ms, n_timed, _, _ = time_steps(torch, step, R, args.steps)
+    assert int(st.item()) == 0
+    pq = T.pq_step_bytes(w.seq_lens, (Hkv - n16) * G, Hkv - n16, M)["total"]
+    f16 = T.fp16_decode_bytes(w.seq_lens, n16 * G, n16)
+    f16_total = f16["total"] - f16["q"] - f16["out"] + 2 * w.batch * n16 * 2 * 128 * 2   # q/out counted once; the append
+    byt = pq + f16_total
+    peak, _ = measured_peaks()
+    del copies, mb
+    return {"fp16_kv_heads": n16, "pq_kv_heads": Hkv - n16, "ms_per_step": ms, "steps_timed": n_timed,
+            "bytes_per_step": byt, "gbs": byt / (ms / 1e3) / 1e9, "frac_of_peak": byt / (ms / 1e3) / 1e9 / peak,
+            "value": T.kv_tokens_heads(w.seq_lens, Hkv) / (ms / 1e3), "unit": UNIT,
+            "launches_per_step": 3, "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB"}
+
+
+def ctypes_workspace(api, w, n16, Lmax, torch):
+    """The mixed step's workspace (None when it needs none)."""
+    import ctypes
+    from decode_attention_product_gb300 import _lib
+    cfg = _lib.config(w.num_subspaces)
+    n = ctypes.c_size_t()
+    _lib.check(_lib.load().aq_decode_step_mixed_workspace(ctypes.byref(cfg), w.batch, w.num_q_heads, w.num_kv_heads,
+                                                          n16, Lmax, ctypes.byref(n)), "workspace")
+    return torch.empty(n.value, dtype=torch.uint8, device="cuda") if n.value else None
 
 
 def measure_e4m3(args, w, api, torch, base, Lmax, units, T, local_rank=0):

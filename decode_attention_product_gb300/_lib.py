@@ -40,6 +40,9 @@ SIGNATURES = {
                                   P, P], i32),
     "aq_decode_step": ([P, i32, i32, i32, P, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32, i32,
                         P, P, sz, P, P], i32),
+    "aq_decode_step_mixed": ([P, i32, i32, i32, i32, P, P, P, i64, P, i64, P, i64, P, P, i32, P, i32, f32,
+                              i32, P, P, sz, P, P], i32),
+    "aq_decode_step_mixed_workspace": ([P, i32, i32, i32, i32, i32, P], i32),
     "aq_decode_attention_noalloc": ([P, i32, i32, i32, P, P, i64, P, i64, P, P, i32, P, i32, f32,
                                      i32, P, P, P], i32),
 }

@@ -218,6 +218,56 @@ def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
     return out
 
 
+def decode_step_mixed(q: torch.Tensor, kv_new: torch.Tensor, num_fp16_heads: int,
+                      kv_pages_f16: torch.Tensor | None, code_pages: torch.Tensor | None,
+                      codebooks: torch.Tensor | None, req_set: torch.Tensor | None,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                      num_subspaces: int = 4, scale: float | None = None, overlap: bool = False,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      status: torch.Tensor | None = None) -> torch.Tensor:
+    """Mixed-precision decode step: kv heads [0, num_fp16_heads) append their
+    new K/V to the fp16 cache kv_pages_f16 [NP16][n16][2][P][D] and attend over
+    it, the other kv heads take the fused PQ step over code_pages / codebooks
+    (pools of Hkv - n16 heads); returns out [B][Hq][D] fp32."""
+    _need(q, torch.float32, "q", 3)
+    _need(kv_new, torch.float16, "kv_new", 4)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    Hkv = kv_new.shape[1]
+    n16 = int(num_fp16_heads)
+    e4m3 = False
+    if n16 > 0:
+        _need(kv_pages_f16, torch.float16, "kv_pages_f16", 5)
+    if n16 < Hkv:
+        _need(code_pages, torch.uint8, "code_pages", 5)
+        e4m3 = codebooks is not None and codebooks.dtype == torch.uint8
+        _need(codebooks, torch.uint8 if e4m3 else torch.float16, "codebooks", 6)
+        _need(req_set, torch.int32, "req_set", 1)
+        num_subspaces = codebooks.shape[3]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    cfg = _lib.config(num_subspaces, head_dim=D)
+    if workspace is None:
+        w = ctypes.c_size_t()
+        st = _lib.load().aq_decode_step_mixed_workspace(ctypes.byref(cfg), B, Hq, Hkv, n16, max_seq_len,
+                                                        ctypes.byref(w))
+        _lib.check(st, "aq_decode_step_mixed_workspace")
+        workspace = torch.empty(w.value, dtype=torch.uint8, device=q.device) if w.value else None
+    st = _lib.load().aq_decode_step_mixed(
+        ctypes.byref(cfg), B, Hq, Hkv, n16, _ptr(q), _ptr(kv_new), _ptr(kv_pages_f16),
+        kv_pages_f16.shape[0] if kv_pages_f16 is not None else 0, _ptr(code_pages),
+        code_pages.shape[0] if code_pages is not None else 0, _ptr(codebooks),
+        codebooks.shape[0] if codebooks is not None else 0, _ptr(req_set), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
+        (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0), _ptr(out),
+        _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status), _stream())
+    _lib.check(st, "aq_decode_step_mixed")
+    return out
+
+
 def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
                           seq_lens: torch.Tensor, max_seq_len: int, scale: float | None = None,
                           num_splits: int = 0, out: torch.Tensor | None = None,

@@ -522,6 +522,9 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.code_pages_w = code_pages_w;
     p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
     p.codebook_e4m3 = (flags & AQ_STEP_E4M3) ? 1 : 0;
+    p.q_head_base = 0;
+    p.kv_head_base = 0;
+    p.qo_kv_heads = Hkv;
     p.head_split_log2 = 0;
     while ((1 << p.head_split_log2) < pl.head_split) ++p.head_split_log2;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -565,6 +568,153 @@ aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch, int32
     return decode_impl(cfg, true, batch, num_q_heads, num_kv_heads, q, nullptr, kv_pages_f16, nullptr, nullptr, 0,
                        num_pages, nullptr, 0, nullptr, block_table, max_pages, seq_lens, max_seq_len, scale,
                        num_splits, out, workspace, workspace_bytes, device_status, stream);
+}
+
+static size_t part_bytes(int32_t batch, int32_t Hq, int32_t splits) {
+    return splits > 1 ? static_cast<size_t>(batch) * Hq * splits * (kHeadDim + 2) * sizeof(float) : 0;
+}
+
+// Plans of the two parts of a mixed-precision step: the fp16 heads' attention
+// and the PQ heads' step, each over its own heads, with split partials in its
+// own part of the workspace (indexed by the full query-head numbering).
+static aq_status mixed_plans(const aq_pq_config *cfg, int32_t batch, int32_t Hq, int32_t Hkv, int32_t n16,
+                             int32_t max_seq_len, bool e4m3, Plan *p16, Plan *ppq, size_t *ws) {
+    const int G = Hq / Hkv;
+    *ws = 0;
+    if (n16 > 0) {
+        aq_status st = make_plan(cfg, batch, n16 * G, n16, max_seq_len, 0, true, kPlanSMs, kPlanSmemCap, p16);
+        if (st != AQ_OK) return st;
+        *ws += part_bytes(batch, Hq, p16->num_splits);
+    }
+    if (n16 < Hkv) {
+        aq_status st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs,
+                                 kPlanSmemCap, ppq, e4m3);
+        if (st != AQ_OK) return st;
+        // the workspace covers either PQ kernel (the format is not known to the size query)
+        Plan other{};
+        st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
+                       &other, !e4m3);
+        if (st != AQ_OK) return st;
+        const int s = ppq->num_splits > other.num_splits ? ppq->num_splits : other.num_splits;
+        *ws += part_bytes(batch, Hq, s);
+    }
+    return AQ_OK;
+}
+
+aq_status aq_decode_step_mixed_workspace(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t num_fp16_heads, int32_t max_seq_len,
+                                         size_t *workspace_bytes) {
+    const int P = cfg ? cfg->page_size : 1;
+    aq_status st = check_decode_common(cfg, true, batch, num_q_heads, num_kv_heads,
+                                       P > 0 ? (max_seq_len + P - 1) / P : 0, max_seq_len, 0);
+    if (st != AQ_OK) return st;
+    if (num_fp16_heads < 0 || num_fp16_heads > num_kv_heads) return AQ_ERR_INVALID_ARGUMENT;
+    Plan a{}, b{};
+    size_t ws = 0;
+    st = mixed_plans(cfg, batch, num_q_heads, num_kv_heads, num_fp16_heads, max_seq_len, false, &a, &b, &ws);
+    if (st != AQ_OK) return st;
+    if (workspace_bytes) *workspace_bytes = ws;
+    return AQ_OK;
+}
+
+aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t num_fp16_heads, const float *q, const void *kv_new_f16,
+                               void *kv_pages_f16, int64_t num_fp16_pages, uint8_t *code_pages, int64_t num_pages,
+                               const void *codebooks, int64_t num_sets, const int32_t *req_set,
+                               const int32_t *block_table, int32_t max_pages, const int32_t *seq_lens,
+                               int32_t max_seq_len, float scale, int32_t flags, float *out, void *workspace,
+                               size_t workspace_bytes, int32_t *device_status, aq_stream_t stream) {
+    aq_status st = check_decode_common(cfg, true, batch, num_q_heads, num_kv_heads, max_pages, max_seq_len, 0);
+    if (st != AQ_OK) return st;
+    const int Hkv = num_kv_heads, Hq = num_q_heads, G = Hq / Hkv, n16 = num_fp16_heads;
+    if (n16 < 0 || n16 > Hkv) return AQ_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(scale) || num_pages < 0 || num_fp16_pages < 0 || num_sets < 0) return AQ_ERR_INVALID_ARGUMENT;
+    if (flags & ~(AQ_STEP_OVERLAP | AQ_STEP_E4M3)) return AQ_ERR_INVALID_ARGUMENT;
+    if (batch == 0) return AQ_OK;
+    if (!q || !out || !kv_new_f16 || !block_table || !seq_lens) return AQ_ERR_INVALID_ARGUMENT;
+    if (n16 > 0 && !kv_pages_f16) return AQ_ERR_INVALID_ARGUMENT;
+    if (n16 < Hkv && (!code_pages || !codebooks || !req_set)) return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(q) || misaligned(out) || misaligned(kv_new_f16) || misaligned(kv_pages_f16) ||
+        misaligned(code_pages) || misaligned(codebooks) || misaligned(workspace))
+        return AQ_ERR_INVALID_ARGUMENT;
+    if (max_pages == 0 && max_seq_len > 0) return AQ_ERR_INVALID_ARGUMENT;
+    Plan p16{}, ppq{};
+    size_t ws = 0;
+    st = mixed_plans(cfg, batch, Hq, Hkv, n16, max_seq_len, (flags & AQ_STEP_E4M3) != 0, &p16, &ppq, &ws);
+    if (st != AQ_OK) return st;
+    if (ws > 0 && (!workspace || workspace_bytes < ws)) return AQ_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    float *wsp = static_cast<float *>(workspace);
+    DecodeParams base{};
+    base.q = q;
+    base.out = out;
+    base.block_table = block_table;
+    base.seq_lens = seq_lens;
+    base.kv_new = kv_new_f16;
+    base.status = device_status;
+    base.batch = batch;
+    base.num_q_heads = Hq;
+    base.max_pages = max_pages;
+    base.max_seq_len = max_seq_len;
+    base.scale_log2 = scale * 1.4426950408889634f;
+    base.qo_kv_heads = Hkv;
+    if (n16 < Hkv) {
+        // the PQ heads: one fused step over their pools
+        DecodeParams p = base;
+        p.code_pages = code_pages;
+        p.code_pages_w = code_pages;
+        p.codebooks = codebooks;
+        p.req_set = req_set;
+        p.num_pages = num_pages;
+        p.num_sets = num_sets;
+        p.num_kv_heads = Hkv - n16;
+        p.kv_head_base = n16;
+        p.q_head_base = n16 * G;
+        p.num_splits = ppq.num_splits;
+        p.split_len = ppq.split_len;
+        p.share = ppq.share;
+        p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
+        p.codebook_e4m3 = (flags & AQ_STEP_E4M3) ? 1 : 0;
+        p.cb_map_ok = !p.codebook_e4m3 &&
+                      codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv - n16, cfg->num_subspaces) == cudaSuccess;
+        if (ppq.kernel == 2 && !p.cb_map_ok) {
+            st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
+                           &ppq, true, false);
+            if (st != AQ_OK) return st;
+            p.num_splits = ppq.num_splits;
+            p.split_len = ppq.split_len;
+            p.share = ppq.share;
+        }
+        p.head_split_log2 = 0;
+        while ((1 << p.head_split_log2) < ppq.head_split) ++p.head_split_log2;
+        if (ppq.num_splits > 1) {
+            p.part_o = wsp;
+            p.part_ml = p.part_o + static_cast<size_t>(batch) * Hq * ppq.num_splits * kHeadDim;
+            wsp += static_cast<size_t>(batch) * Hq * ppq.num_splits * (kHeadDim + 2);
+        }
+        cudaError_t e = launch_pq_decode_step(p, cfg->num_subspaces, G, ppq, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (n16 > 0) {
+        // the fp16 heads: the new tokens into their pages, then the attention
+        DecodeParams p = base;
+        p.kv_pages = kv_pages_f16;
+        p.num_pages = num_fp16_pages;
+        p.num_kv_heads = n16;
+        p.kv_head_base = 0;
+        p.q_head_base = 0;
+        p.num_splits = p16.num_splits;
+        p.split_len = p16.split_len;
+        p.share = p16.share;
+        if (p16.num_splits > 1) {
+            p.part_o = wsp;
+            p.part_ml = p.part_o + static_cast<size_t>(batch) * Hq * p16.num_splits * kHeadDim;
+        }
+        cudaError_t e = launch_append_fp16(p, s);
+        if (e == cudaSuccess) e = launch_fp16_decode(p, G, p16, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return AQ_OK;
 }
 
 }  // extern "C"

@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
         const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
         for (int i = tid; i < G * D; i += kThreads) {
             const int g = i / D, d = i % D;
-            const size_t bh = static_cast<size_t>(b) * Hq + kvh * G + g;
+            const size_t bh = static_cast<size_t>(b) * Hq + p.q_head_base + kvh * G + g;
             if (S_ == 1) p.out[bh * D + d] = v;
             else if (d == 0) {
                 p.part_ml[(bh * S_ + split) * 2 + 0] = bad0 ? v : -INFINITY;
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         float4 t = *reinterpret_cast<const float4 *>(
-            p.q + (static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G + g) * D + 4 * lane);
+            p.q + (static_cast<size_t>(b) * Hq + p.q_head_base + static_cast<size_t>(kvh) * G + g) * D + 4 * lane);
         qv[g] = make_float4(t.x * p.scale_log2, t.y * p.scale_log2, t.z * p.scale_log2,
                             t.w * p.scale_log2);
     }
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
                 o += f * wacc[(w * G + g) * D + d];
             }
         }
-        const size_t bh = static_cast<size_t>(b) * Hq + static_cast<size_t>(kvh) * G + g;
+        const size_t bh = static_cast<size_t>(b) * Hq + p.q_head_base + static_cast<size_t>(kvh) * G + g;
         const float nan = __int_as_float(0x7fc00000);
         if (S_ == 1) {
             p.out[bh * D + d] = bad ? nan : (l > 0.f ? o / l : 0.f);
@@ -200,8 +200,38 @@ cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, c
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    if (plan.num_splits > 1) return launch_combine(p, s);
+    if (plan.num_splits > 1) return launch_combine(p, p.num_kv_heads * G, s);
     return cudaSuccess;
+}
+
+// One thread per 8 bytes of a new key or value: kv_new[b][kv_head_base + h]
+// into slot (seq_lens[b] - 1) % P of page block_table[b][(seq_lens[b] - 1) / P],
+// kv head h of the fp16 pool.  A length or page outside its range sets the
+// status bit and skips the copy (the attention of that request reports it
+// too).
+__global__ void __launch_bounds__(256) append_fp16_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int D = kHeadDim, P = kPage, PER = D * 2 * 2 / 8;   // 8-byte words per (K, V) pair
+    const int b = blockIdx.y, h = blockIdx.x;
+    const int L = p.seq_lens[b];
+    if (L < 1 || L > p.max_pages * P) return;                  // an empty or bad request: nothing to append
+    const int t = L - 1;
+    const int pg = p.block_table[static_cast<size_t>(b) * p.max_pages + t / P];
+    if (pg < 0 || static_cast<int64_t>(pg) >= p.num_pages) {
+        if (threadIdx.x == 0) flag_status(p.status, AQ_DEV_BAD_PAGE);
+        return;
+    }
+    for (int i = threadIdx.x; i < PER; i += blockDim.x) {
+        const int kv = i / (PER / 2), w = i % (PER / 2);          // K then V; 8-byte word within the vector
+        const uint2 v = reinterpret_cast<const uint2 *>(p.kv_new)
+            [((static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + h) * 2 + kv) * (D / 4) + w];
+        reinterpret_cast<uint2 *>(const_cast<void *>(p.kv_pages))
+            [(((static_cast<size_t>(pg) * p.num_kv_heads + h) * 2 + kv) * P + t % P) * (D / 4) + w] = v;
+    }
+}
+
+cudaError_t launch_append_fp16(const DecodeParams &p, cudaStream_t s) {
+    append_fp16_kernel<<<dim3(static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(p.batch)), 64, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace aq

@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // blockIdx.y = kv head * 2^head_split_log2 + sub-group: this cluster serves
     // query heads [blockIdx.y * G, +G) of kv head blockIdx.y >> head_split_log2
     const int kvh = static_cast<int>(blockIdx.y >> p.head_split_log2), b = blockIdx.z;
-    const int hq0 = static_cast<int>(blockIdx.y) * G;
+    const int hq0 = p.q_head_base + static_cast<int>(blockIdx.y) * G;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         if (cl_new && tid < 2 * MC * DSUB) {
             const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
             xnew[tid] = __half2float(__ldg(reinterpret_cast<const __half *>(p.kv_new) +
-                                           ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D +
+                                           ((static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + kvh) * 2 + w) * D +
                                            rank * MC * DSUB + r));
         }
     }
@@ -917,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ DecodeParams p) {
-    const size_t bh = blockIdx.x;
+    const size_t bh = static_cast<size_t>(blockIdx.y) * p.num_q_heads + p.q_head_base + blockIdx.x;
     const int d = threadIdx.x;
     const int S_ = p.num_splits;
     const float *ml = p.part_ml + bh * S_ * 2;
@@ -1034,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     if constexpr (C > 1) rank = static_cast<int>(cluster_ctarank());
     const int split = blockIdx.x / C;
     const int kvh = static_cast<int>(blockIdx.y >> p.head_split_log2), b = blockIdx.z;
-    const int hq0 = static_cast<int>(blockIdx.y) * G;
+    const int hq0 = p.q_head_base + static_cast<int>(blockIdx.y) * G;
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const int S_ = p.num_splits;
 
@@ -1122,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
         if (cl_new && tid < 2 * MC * DSUB) {
             const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
             xnew[tid] = __half2float(__ldg(reinterpret_cast<const __half *>(p.kv_new) +
-                                           ((static_cast<size_t>(b) * Hkv + kvh) * 2 + w) * D +
+                                           ((static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + kvh) * 2 + w) * D +
                                            rank * MC * DSUB + r));
         }
     }
@@ -1608,7 +1608,7 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
     else if (M == 8) e = dispatch_g<8, false, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
-    if (plan.num_splits > 1) return launch_combine(p, s);
+    if (plan.num_splits > 1) return launch_combine(p, p.num_kv_heads * G * plan.head_split, s);
     return cudaSuccess;
 }
 
@@ -1621,13 +1621,12 @@ cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Pla
     else if (M == 8) e = p.codebook_e4m3 ? dispatch_g<8, true, true>(p, G, plan, s) : dispatch_g<8, true, false>(p, G, plan, s);
     else return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
-    if (plan.num_splits > 1) return launch_combine(p, s);
+    if (plan.num_splits > 1) return launch_combine(p, p.num_kv_heads * G * plan.head_split, s);
     return cudaSuccess;
 }
 
-cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s) {
-    const unsigned n = static_cast<unsigned>(p.batch) * static_cast<unsigned>(p.num_q_heads);
-    combine_kernel<<<n, 128, 0, s>>>(p);
+cudaError_t launch_combine(const DecodeParams &p, int num_q_heads_launch, cudaStream_t s) {
+    combine_kernel<<<dim3(static_cast<unsigned>(num_q_heads_launch), static_cast<unsigned>(p.batch)), 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

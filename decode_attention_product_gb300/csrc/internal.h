@@ -37,6 +37,12 @@ struct DecodeParams {
     int32_t head_split_log2;  // PQ: 2^this clusters per kv head, each for Hq/Hkv >> this query heads
     int32_t codebook_e4m3;    // PQ step: codebooks are FP8 E4M3 codes, same layout
     int32_t cb_map_ok;        // cb_map describes the codebooks (fp16, TMA-addressable)
+    // Head numbering of q / out / kv_new when a launch covers only some kv
+    // heads (a mixed-precision step): launch kv head h is kv head
+    // kv_head_base + h of those arrays, which hold qo_kv_heads kv heads and
+    // num_q_heads query heads; its first query head is q_head_base + h * G.
+    // Pages, codebooks and the grid use num_kv_heads (this launch's heads).
+    int32_t q_head_base, kv_head_base, qo_kv_heads;
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -81,7 +87,12 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
 cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan,
                                   cudaStream_t s);
 cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s);
-cudaError_t launch_combine(const DecodeParams &p, cudaStream_t s);
+// Combine of split partials for this launch's query heads (num_q_heads_launch
+// of them, from q_head_base on).
+cudaError_t launch_combine(const DecodeParams &p, int num_q_heads_launch, cudaStream_t s);
+// Copy each request's new fp16 key and value (kv_new) into its page slot of an
+// fp16 cache, for this launch's kv heads.
+cudaError_t launch_append_fp16(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
 cudaError_t launch_to_e4m3(int64_t n, const void *src_f16, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_from_e4m3(int64_t n, const uint8_t *src, void *dst_f16, cudaStream_t s);

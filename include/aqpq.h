@@ -203,6 +203,12 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens,
  *   *cluster_size   out: CTAs cooperating on one split (may be NULL)
  *   *workspace_bytes out: bytes the call needs in `workspace` (may be NULL)
  * `fp16` selects the plan of aq_decode_attention_fp16.
+ * Two PQ kernels exist: one whose cluster CTAs split the tokens and merge
+ * their value bins, and one whose CTAs each score every token of their split
+ * (used for GQA groups of 4 or more query heads per kv head).  The
+ * environment variable AQPQ_DECODE_KERNEL=1 or =2 forces the first or, where
+ * its split fits, the second (read at every call; results agree within
+ * rounding).
  * ------------------------------------------------------------------------- */
 aq_status aq_decode_plan(const aq_pq_config *cfg, int32_t batch,
                          int32_t num_q_heads, int32_t num_kv_heads,
@@ -313,6 +319,54 @@ aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch,
                                    int32_t num_splits, float *out,
                                    void *workspace, size_t workspace_bytes,
                                    int32_t *device_status, aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * aq_decode_step_mixed -- one fused decode step over a cache kept at two
+ * precisions, by kv head (AQPIM blog §6.1 item 4: keep the full-precision
+ * cache for the most important heads, here kv heads [0, num_fp16_heads) and
+ * their query heads; every other kv head is product-quantised).
+ *
+ * For kv head h < num_fp16_heads: the new key and value kv_new_f16[b][h] are
+ * written into kv_pages_f16 at position seq_lens[b] - 1 and the attention is
+ * aq_decode_attention_fp16's over the fp16 cache.  For kv head h >=
+ * num_fp16_heads: aq_decode_step's over the PQ cache, whose pools hold only
+ * those heads (pool head h - num_fp16_heads).  Both caches are addressed by
+ * the same block table (a page id indexes either pool).  Query head j reads
+ * kv head j / (Hq / Hkv) as everywhere.
+ *
+ *   q             in      fp32 [B][Hq][D]
+ *   kv_new_f16    in      fp16 [B][Hkv][2][D]
+ *   kv_pages_f16  in/out  fp16 [num_fp16_pages][num_fp16_heads][2][P][D]
+ *   code_pages    in/out  uint8 [num_pages][Hkv - num_fp16_heads][P][2][M]
+ *   codebooks     in      fp16 (or E4M3 codes with AQ_STEP_E4M3)
+ *                         [num_sets][Hkv - num_fp16_heads][2][M][K][Dsub]
+ *   out           out     fp32 [B][Hq][D]
+ *   workspace     device scratch of >= aq_decode_step_mixed_workspace() bytes
+ *   flags         AQ_STEP_OVERLAP (applies to the PQ heads' launch, with
+ *                 aq_decode_step's contract), AQ_STEP_E4M3
+ *   other arguments as aq_decode_step.  0 <= num_fp16_heads <= Hkv; with 0 the
+ *   fp16 arguments may be NULL, with Hkv the PQ ones.  Up to four launches:
+ *   the PQ step (+ its combine), the fp16 append, the fp16 attention (+ its
+ *   combine).
+ * ------------------------------------------------------------------------- */
+aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t num_fp16_heads,
+                               const float *q, const void *kv_new_f16,
+                               void *kv_pages_f16, int64_t num_fp16_pages,
+                               uint8_t *code_pages, int64_t num_pages,
+                               const void *codebooks, int64_t num_sets,
+                               const int32_t *req_set, const int32_t *block_table,
+                               int32_t max_pages, const int32_t *seq_lens,
+                               int32_t max_seq_len, float scale, int32_t flags,
+                               float *out, void *workspace, size_t workspace_bytes,
+                               int32_t *device_status, aq_stream_t stream);
+
+/* Host-only: the workspace bytes aq_decode_step_mixed needs for these
+ * arguments (either codebook format). */
+aq_status aq_decode_step_mixed_workspace(const aq_pq_config *cfg, int32_t batch,
+                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t num_fp16_heads, int32_t max_seq_len,
+                                         size_t *workspace_bytes);
 
 /* ---------------------------------------------------------------------------
  * aq_decode_attention_noalloc -- aq_decode_attention for callers that cannot

@@ -17,6 +17,8 @@ What each function computes, and the passage it follows, is stated in
   attention and the blockwise (max, sum) merge (PAM article §2.2.3).
 * ``decode_attention`` / ``decode_attention_fp16``: paged PQ (resp. fp16)
   decode attention, decompress-then-compute (AQPIM blog §4).
+* ``decode_attention_mixed``: fp16 attention for the first kv heads, PQ for
+  the rest (AQPIM blog §6.1 item 4).
 * ``kmeans_fit`` / ``kmeans_step``: Lloyd k-means codebook fit (AQPIM blog
   §3.2 item 2, §5.2 item 1).
 
@@ -189,6 +191,31 @@ def decode_attention_fp16(q, kv_pages, block_table, seq_lens, scale):
     _load().oracle_decode_attention_fp16(
         B, Hq, Hkv, D, P, _p(q), _p(kvp), _p(bt), bt.shape[1],
         _p(_c(seq_lens, np.int32)), scale, _p(out))
+    return out
+
+
+def decode_attention_mixed(q, kv_pages_f16, code_pages, codebooks, req_set, block_table, seq_lens,
+                           scale, page_size, num_fp16_heads):
+    """Decode attention over a cache kept at two precisions by kv head (AQPIM
+    blog §6.1 item 4: the full-precision cache kept for the most important
+    heads): kv heads [0, num_fp16_heads) attend over their fp16 pages
+    kv_pages_f16 [NP][n16][2][P][D] exactly as decode_attention_fp16, the
+    others over their PQ cache (pools of Hkv - n16 heads) exactly as
+    decode_attention.  Query head j reads kv head j / G.  float64 [B][Hq][D].
+    """
+    q = np.asarray(q)
+    B, Hq, D = q.shape
+    n16 = int(num_fp16_heads)
+    Hpq = codebooks.shape[1] if codebooks is not None else 0
+    Hkv = n16 + Hpq
+    assert Hq % Hkv == 0
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D), np.float64)
+    if n16 > 0:
+        out[:, :n16 * G] = decode_attention_fp16(q[:, :n16 * G], kv_pages_f16, block_table, seq_lens, scale)
+    if Hpq > 0:
+        out[:, n16 * G:] = decode_attention(q[:, n16 * G:], code_pages, codebooks, req_set, block_table,
+                                            seq_lens, scale, page_size)
     return out
 
 

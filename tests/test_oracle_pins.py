@@ -397,6 +397,66 @@ def test_gqa_head_mapping(orc):
     assert np.allclose(out[0, 2], e1) and np.allclose(out[0, 3], e1)
 
 
+def _codeword_fp16_pages(cbs, pages, req_set, bt, lens):
+    """fp16 pages [NP][Hkv][2][P][D] holding, at every cached token's slot, the
+    vectors its codes reconstruct to (written by numpy from the codebooks)."""
+    B, Hkv, P = len(lens), cbs.shape[1], 16
+    kvp = np.zeros((pages.shape[0], Hkv, 2, P, D), np.float16)
+    for b in range(B):
+        for h in range(Hkv):
+            Kx, Vx = _decode_np(cbs, pages, req_set, bt, lens, b, h)
+            for t in range(int(lens[b])):
+                kvp[bt[b, t // P], h, 0, t % P] = Kx[t]
+                kvp[bt[b, t // P], h, 1, t % P] = Vx[t]
+    return kvp
+
+
+def test_mixed_precision_limits(orc):
+    """No fp16 head: the mixed step is PQ attention on every head; every head
+    fp16: fp16 attention on every head (AQPIM blog §6.1 item 4 at its two
+    ends), with a GQA group of 4 so that the query-head slicing is exercised."""
+    q, pages, cbs, req_set, bt, lens = _paged_problem(41, Hq=8, Hkv=2, M=4)
+    kvp = _rng(41).standard_normal((pages.shape[0], 2, 2, 16, D)).astype(np.float16)
+    pq = orc.decode_attention(q, pages, cbs, req_set, bt, lens, 0.09, 16)
+    f16 = orc.decode_attention_fp16(q, kvp, bt, lens, 0.09)
+    got0 = orc.decode_attention_mixed(q, None, pages, cbs, req_set, bt, lens, 0.09, 16, 0)
+    got2 = orc.decode_attention_mixed(q, kvp, None, None, req_set, bt, lens, 0.09, 16, 2)
+    assert np.array_equal(got0, pq) and np.array_equal(got2, f16)
+
+
+def test_mixed_precision_on_codeword_cache_is_fp16_attention(orc):
+    """When every cached vector is a codeword concatenation, fp16 and PQ
+    attention agree head by head, so any split of the kv heads into an fp16
+    prefix and a PQ rest gives fp16 attention on all heads -- which fails if
+    the query heads were sliced by kv head instead of group, the pools taken
+    from the wrong end, or the two parts swapped."""
+    q, pages, cbs, req_set, bt, lens = _paged_problem(42, Hq=12, Hkv=3, M=4)
+    kvp = _codeword_fp16_pages(cbs, pages, req_set, bt, lens)
+    want = orc.decode_attention_fp16(q, kvp, bt, lens, 0.08)
+    for n16 in range(4):
+        got = orc.decode_attention_mixed(q, np.ascontiguousarray(kvp[:, :n16]),
+                                         np.ascontiguousarray(pages[:, n16:]),
+                                         np.ascontiguousarray(cbs[:, n16:]), req_set, bt, lens, 0.08, 16, n16)
+        assert np.allclose(got, want, rtol=1e-13, atol=1e-14), n16
+
+
+def test_mixed_precision_head_mapping(orc):
+    """kv head 0 fp16 with every value e_0, kv head 1 PQ with every value
+    codeword e_1: query heads 0..G-1 return e_0, heads G..2G-1 return e_1."""
+    G, P, M, K = 3, 16, 4, 256
+    kvp = np.zeros((1, 1, 2, P, D), np.float16)
+    kvp[0, 0, 1, :, 0] = 1.0
+    cbs = np.zeros((1, 1, 2, M, K, D // M), np.float16)
+    cbs[0, 0, 1, 0, 0, 1] = 1.0
+    pages = np.zeros((1, 1, P, 2, M), np.uint8)
+    q = _rng(6).standard_normal((1, 2 * G, D)).astype(np.float32)
+    out = orc.decode_attention_mixed(q, kvp, pages, cbs, np.zeros(1, np.int32), np.zeros((1, 1), np.int32),
+                                     np.array([11], np.int32), 0.1, P, 1)
+    e0, e1 = np.eye(D)[0], np.eye(D)[1]
+    for h in range(G):
+        assert np.allclose(out[0, h], e0) and np.allclose(out[0, G + h], e1)
+
+
 def test_block_table_page_and_slot(orc):
     """A saturating score on token t* returns the value stored at page
     block_table[b][t*/P], slot t* % P (PAM article §2.2.2 block table)."""
