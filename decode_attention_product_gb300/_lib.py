@@ -27,6 +27,7 @@ SIGNATURES = {
     "aq_status_string": ([i32], ctypes.c_char_p),
     "aq_last_error_message": ([], ctypes.c_char_p),
     "aq_version": ([], ctypes.c_char_p),
+    "aq_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_uint64),
     "aq_fit_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),
     "aq_kmeans_step": ([P, i64, i32, P, P, P, P, P], i32),
     "aq_refine_codebooks": ([P, i64, i32, i32, P, P, P, P], i32),

@@ -3,6 +3,7 @@
 // the kernel launchers and mapping of CUDA errors to AQ_ERR_CUDA.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -50,6 +51,12 @@ void record_cuda_error(cudaError_t e) {
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
                   cudaGetErrorString(e));
 }
+
+namespace {
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+}  // namespace
+
+unsigned long long decode_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need) {
     int dev = 0;
@@ -277,7 +284,12 @@ const char *aq_status_string(aq_status s) {
 
 const char *aq_last_error_message(void) { return aq::g_last_error; }
 
-const char *aq_version(void) { return "aqpq 0.1 sm_103a"; }
+const char *aq_version(void) { return "aqpq 0.2 sm_103a"; }
+
+uint64_t aq_set_wait_limit_ns(uint64_t ns) {
+    constexpr uint64_t kMax = 1000000000ull;           // 1 s
+    return aq::g_wait_limit_ns.exchange(ns > kMax ? kMax : ns);
+}
 
 aq_status aq_fit_codebooks(const aq_pq_config *cfg, int64_t num_units, int32_t n_samples,
                            int32_t iters, const void *samples_f16, void *codebooks_f16,
@@ -525,6 +537,7 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     p.q_head_base = 0;
     p.kv_head_base = 0;
     p.qo_kv_heads = Hkv;
+    p.wait_limit_ns = decode_wait_limit_ns();
     p.head_split_log2 = 0;
     while ((1 << p.head_split_log2) < pl.head_split) ++p.head_split_log2;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -658,6 +671,7 @@ aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t n
     base.max_seq_len = max_seq_len;
     base.scale_log2 = scale * 1.4426950408889634f;
     base.qo_kv_heads = Hkv;
+    base.wait_limit_ns = decode_wait_limit_ns();
     if (n16 < Hkv) {
         // the PQ heads: one fused step over their pools
         DecodeParams p = base;

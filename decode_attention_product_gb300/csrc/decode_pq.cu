@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
 
     // ---- lookup-table rows of the owned subspaces, pushed to the peers; the
     // new token's K and V codes from the same rows --------------------------
-    bool tmo = !mbar_wait_bounded(&bar[0], 0);
+    bool tmo = !mbar_wait_limit(&bar[0], 0, p.wait_limit_ns);
     // the V slice into its own buffer once the K slice has landed, so that
     // the K slice, which the table build waits for, has the bandwidth first
     if constexpr (!S::SHARED_CB) {
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
         }
     }
-    tmo |= !mbar_wait_bounded(&bar[4], 0);
+    tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
     int vcode[MC];                                     // the new token's V codes, owned subspaces
@@ -601,11 +601,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // with its own V buffer, the new value's codes while the peers' rows land
     if constexpr (APPEND && !S::SHARED_CB) {
         if (cl_new) {
-            tmo |= !mbar_wait_bounded(&bar[1], 0);
+            tmo |= !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns);
             encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
         }
     }
-    if constexpr (C > 1) tmo |= !mbar_wait_bounded(&bar[2], 0);
+    if constexpr (C > 1) tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     __syncthreads();
 
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     if constexpr (APPEND) {
         if (cl_new) {
             if constexpr (S::SHARED_CB) {
-                if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+                if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
                 encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
                 __syncthreads();
             }
@@ -735,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             for (int mi = 0; mi < MC; ++mi) vcode[mi] = static_cast<int>(keys[MC + mi] & 0xffu);
             if (tid == 0) {
                 const bool pg_ok = pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages;
-                if (pg_ok) {
+                if (pg_ok && !(sflag[0] & AQ_DEV_TIMEOUT)) {   // no codes from data that may not have landed
                     uint8_t *dst = p.code_pages_w +
                                    ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
 #pragma unroll
@@ -750,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         }
     }
     if constexpr (C > 1) {
-        if (!mbar_wait_bounded(&bar[3], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+        if (!mbar_wait_limit(&bar[3], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         cluster_arrive_relaxed();                      // all traffic into this CTA has landed
     }
 
@@ -819,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     int bad_all = sflag[1];
 
     // ---- value codebook product for the owned subspaces -----------------------
-    if (!mbar_wait_bounded(&bar[1], 0)) {
+    if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) {
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
     }
@@ -994,7 +994,8 @@ struct AtCfg {
     static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + M * 4 + 7) / 8 * 8;  // [2][MC] u64
     static constexpr int OFF_BAR = OFF_KEYS + 2 * MC * 8;   // K, V, codes, q, rows
     static constexpr int OFF_FLAG = OFF_BAR + 5 * 8;
-    static constexpr int OFF_CODES = (OFF_FLAG + 16 + 15) / 16 * 16;
+    static constexpr int OFF_PBAD = OFF_FLAG + 16;          // [C] ints
+    static constexpr int OFF_CODES = (OFF_PBAD + 4 * C + 15) / 16 * 16;
     static size_t smem(int split_len) { return 1024 + OFF_CODES + static_cast<size_t>(split_len) * 2 * M; }
     static_assert(K == kThreads, "one thread per codeword in the table build");
     static_assert(SLICE_BYTES % 1024 == 0, "slices keep the swizzle alignment");
@@ -1027,6 +1028,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);  // K, V, codes, q, rows
     int *sflag = reinterpret_cast<int *>(smem + S::OFF_FLAG);
+    int *pbad = reinterpret_cast<int *>(smem + S::OFF_PBAD);          // [C] flags the peers sent with their rows
     const unsigned char *codes = smem + S::OFF_CODES;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1087,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
         mbar_arrive_expect_tx(&bar[1], S::SLICE_BYTES);
 #pragma unroll
         for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, row0 + M * K + mi * K, &bar[1]);
-        if constexpr (C > 1) mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0)) * 4);
+        if constexpr (C > 1) mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::ROW_FLOATS + (cl_new ? MC : 0) + 1) * 4);
     }
     {
         // the split's code pages, whole pages (16 tokens x 2M codes of this kv
@@ -1134,8 +1136,11 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     if constexpr (C > 1) cluster_arrive_relaxed();     // this CTA's barriers are ready for pushes
 
     // ---- lookup-table rows of the owned subspaces; the new key's codes -------
-    bool tmo = !mbar_wait_bounded(&bar[0], 0);
-    tmo |= !mbar_wait_bounded(&bar[3], 0);
+    bool tmo = !mbar_wait_limit(&bar[0], 0, p.wait_limit_ns);
+    tmo |= !mbar_wait_limit(&bar[3], 0, p.wait_limit_ns);
+    // a table built from a slice or query that had not landed reaches the
+    // peers too: the flag travels with the rows
+    if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     {
         float dkv[MC];
@@ -1189,7 +1194,9 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
         if (tid < C - 1) {
             const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) % C;
             const uint32_t rows = smem_u32(lut + rank * S::ROW_FLOATS);
-            bulk_s2cluster(mapa_u32(rows, pr), rows, S::ROW_FLOATS * 4, mapa_u32(smem_u32(&bar[4]), pr));
+            const uint32_t rbar = mapa_u32(smem_u32(&bar[4]), pr);
+            bulk_s2cluster(mapa_u32(rows, pr), rows, S::ROW_FLOATS * 4, rbar);
+            st_async_f32(mapa_u32(smem_u32(&pbad[rank]), pr), __int_as_float(sflag[0]), rbar);
         }
     }
     if constexpr (APPEND) {
@@ -1207,8 +1214,8 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
             }
         }
     }
-    if constexpr (C > 1) tmo |= !mbar_wait_bounded(&bar[4], 0);
-    tmo |= !mbar_wait_bounded(&bar[2], 0);
+    if constexpr (C > 1) tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
+    tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     __syncthreads();                                   // the full table, the new key's codes
     if constexpr (C > 1) cluster_arrive_relaxed();     // everything sent to this CTA has landed
@@ -1292,7 +1299,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     // the new token's value codes of the owned subspaces
     if constexpr (APPEND) {
         if (cl_new) {
-            if (!mbar_wait_bounded(&bar[1], 0)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+            if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
             float dv[MC];
 #pragma unroll
             for (int mi = 0; mi < MC; ++mi) {
@@ -1327,11 +1334,16 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     }
     __syncthreads();                                   // bins, statistics, the new value codes
     int bad_all = sflag[0];
+#pragma unroll
+    for (int r = 0; r < C; ++r)
+        if (r != rank) bad_all |= pbad[r];
     if constexpr (APPEND) {
         if (cl_new && tid == 0) {
             // this CTA's codes of the new token into its page slot
             const int pg_new = __ldg(bt + new_pos / P);
-            if (pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages) {
+            if (sflag[0] & AQ_DEV_TIMEOUT) {
+                // no codes from data that may not have landed
+            } else if (pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages) {
                 uint8_t *dst = p.code_pages_w + ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
 #pragma unroll
                 for (int mi = 0; mi < MC; ++mi) {
@@ -1344,7 +1356,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
             }
         }
     }
-    if (!mbar_wait_bounded(&bar[1], 0)) {
+    if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) {
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
     }

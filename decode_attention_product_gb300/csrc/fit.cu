@@ -46,7 +46,7 @@ struct FitCfg {
         b += static_cast<size_t>(n) * 4;                    // assign int  [N]
         b += static_cast<size_t>(K) * 4;                    // cnt   int   [K]
         b += static_cast<size_t>(K) * 4;                    // slot  int   [K]
-        return b + 64;
+        return b + 64;                                      // nused, chg
     }
 };
 
@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
     int *cnt = asg + N;
     int *slot = cnt + K;
     int *nused = slot + K;
+    int *chg = nused + 1;                                   // [2]: an assignment changed in step it (it & 1)
 
     const int64_t u = blockIdx.x;
     const int m = blockIdx.y, tid = threadIdx.x;
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
             c16[i] = h;
         }
     }
+    if (tid == 0) chg[0] = chg[1] = 0;
     __syncthreads();
 
     // assignment mapping: NCH threads per sample, each over K / NCH centroids
@@ -129,12 +131,21 @@ __global__ void __launch_bounds__(kThreads) fit_kernel(const __grid_constant__ F
                 const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
                 key = o < key ? o : key;
             }
-            if (n < N && ch == 0) asg[n] = static_cast<int>(key & 0xffffffffu);
+            if (n < N && ch == 0) {
+                const int a = static_cast<int>(key & 0xffffffffu);
+                if (it > 0 && asg[n] != a) chg[it & 1] = 1;
+                asg[n] = a;
+            }
         }
         for (int i = tid; i < nslot * DSUB; i += kThreads) isum[i] = 0;
         for (int i = tid; i < K; i += kThreads) cnt[i] = 0;
         if (tid == 0) *nused = 0;
         __syncthreads();
+        // Exact early exit: an assignment equal to the previous step's gives
+        // the same members, hence the same exact sums and centroids, so every
+        // later step would repeat it -- the result is the full fit's.
+        if (it > 0 && chg[it & 1] == 0) break;
+        if (tid == 0) chg[(it + 1) & 1] = 0;
         // member counts; the first member of a centroid claims its sum slot
         for (int n = tid; n < N; n += kThreads) {
             const int k = asg[n];

@@ -43,6 +43,9 @@ struct DecodeParams {
     // num_q_heads query heads; its first query head is q_head_base + h * G.
     // Pages, codebooks and the grid use num_kv_heads (this launch's heads).
     int32_t q_head_base, kv_head_base, qo_kv_heads;
+    // limit of the decode kernels' waits on their own copies before the
+    // drain (aq_set_wait_limit_ns); the drain before exit keeps the default
+    unsigned long long wait_limit_ns;
     float scale_log2;                            // scale * log2(e)
 };
 
@@ -109,6 +112,8 @@ int pq_attend_max_split(int M, int G);
 // registers, a fixed number per thread); 0 for an unsupported (M, G).
 int pq_decode_max_share(int M, int G);
 size_t fit_smem_bytes(int M, int n_samples);
+// The current limit of the decode kernels' waits (aq_set_wait_limit_ns).
+unsigned long long decode_wait_limit_ns();
 // Record a CUDA error for aq_last_error_message() and clear the runtime's
 // last-error state.
 void record_cuda_error(cudaError_t e);

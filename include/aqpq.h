@@ -37,8 +37,8 @@
  *     the caller-zeroed int32 `device_status` word and skip the offending
  *     element; attention outputs of an affected request are set to NaN.
  *   - Kernels never wait on another launch.  Their only waits are on their own
- *     asynchronous copies, bounded in time; a wait that runs out sets
- *     AQ_DEV_TIMEOUT, and the affected outputs become NaN.
+ *     asynchronous copies, bounded in time (aq_set_wait_limit_ns); a wait that
+ *     runs out sets AQ_DEV_TIMEOUT, and the affected outputs become NaN.
  *
  * Layouts (D = head_dim, M = num_subspaces, Dsub = D / M, K = num_codewords,
  * P = page_size, S = number of codebook sets, NP = number of pages):
@@ -90,8 +90,21 @@ const char *aq_status_string(aq_status s);
 /* Text of the last CUDA error seen by this thread's libaqpq call ("" if none). */
 const char *aq_last_error_message(void);
 
-/* Library version, e.g. "aqpq 0.1 sm_103a". */
+/* Library version, e.g. "aqpq 0.2 sm_103a". */
 const char *aq_version(void);
+
+/* Limit, in nanoseconds, of the decode kernels' waits on their own
+ * asynchronous copies (aq_decode_attention, aq_decode_step, the PQ part of
+ * aq_decode_step_mixed); default AQ_DEFAULT_WAIT_LIMIT_NS (200 ms), at most
+ * 1 s.  A wait that runs out sets AQ_DEV_TIMEOUT, the outputs it affects
+ * become NaN, and a fused step writes no new codes from that CTA.  Whatever
+ * the limit, a kernel waits (up to 200 ms) for every copy into its shared
+ * memory to land before it exits.  Meant for testing the timeout path; it
+ * applies to launches made after the call, from any thread, and returns the
+ * previous limit.  No pages describe this: it is a property of this
+ * library's kernels. */
+#define AQ_DEFAULT_WAIT_LIMIT_NS 200000000ull
+uint64_t aq_set_wait_limit_ns(uint64_t ns);
 
 /* ---------------------------------------------------------------------------
  * aq_fit_codebooks -- codebook fit by Lloyd k-means (AQPIM blog §3.2 item 2,

@@ -47,6 +47,15 @@ def test_status_strings(lib):
     assert lib.aq_version().startswith(b"aqpq")
 
 
+def test_wait_limit_setter(lib):
+    """Host state only: set, read back as the previous value, clamp at 1 s,
+    restore the default (no kernel runs)."""
+    prev = lib.aq_set_wait_limit_ns(12345)
+    assert prev == 200_000_000
+    assert lib.aq_set_wait_limit_ns(5 * 10**9) == 12345
+    assert lib.aq_set_wait_limit_ns(prev) == 10**9
+
+
 def _cfg(M=4, D=128, K=256, P=16):
     return _lib.PQConfig(D, M, K, P)
 
