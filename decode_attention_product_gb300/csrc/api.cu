@@ -183,7 +183,7 @@ static bool attend_plan(int M, int G, int64_t units, int max_seq_len, int req, i
 }
 
 static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
-                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl);
+                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl, bool stream);
 
 // The plan of a decode call.  PQ: the whole-split kernel for GQA groups of 4
 // or more query heads per kv head when a split of at most two fits its
@@ -198,9 +198,14 @@ static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv,
 static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl, bool e4m3 = false,
                            bool allow_attend = true) {
-    Plan p1{};
-    aq_status st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1);
+    // the token-share plan for this codebook format, and for the other one (an
+    // E4M3 call streams no multi-chunk shares, so it may split more)
+    Plan p1{}, p1x{};
+    aq_status st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1, !e4m3);
     if (st != AQ_OK) return st;
+    st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1x, e4m3);
+    if (st != AQ_OK) return st;
+    if (p1x.workspace > p1.workspace) p1.workspace = p1x.workspace;
     Plan p2{};
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
     const int forced = forced_kernel();
@@ -220,7 +225,7 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
 }
 
 static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, int max_seq_len,
-                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl) {
+                            int req, bool fp16, int sms, size_t smem_cap, Plan *pl, bool stream) {
     const int P = cfg->page_size;
     const int G = Hq / Hkv;
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
@@ -243,19 +248,21 @@ static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv,
         for (int c = 4; c >= 1; c /= 2)
             if (c <= M && pq_decode_smem_bytes(M, Gs, c) <= smem_cap) { C = c; break; }
         if (C == 0) return AQ_ERR_UNSUPPORTED;
-        const int share_max = pq_decode_max_share(M, Gs) / P * P;
-        if (share_max <= 0) return AQ_ERR_UNSUPPORTED;
+        const int chunk = pq_decode_max_share(M, Gs) / P * P;
+        if (chunk <= 0) return AQ_ERR_UNSUPPORTED;
+        // shares of several chunks (streamed in two passes) for clusters of 4 or 8
+        auto share_max = [&](int c) { return stream && c >= 4 ? chunk * kMaxStreamChunks : chunk; };
         const int64_t clusters = units * nsub;         // per split
-        split_plan(C, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+        split_plan(C, share_max(C), false, clusters, max_seq_len, req, sms, P, pl);
         const int64_t ctas = clusters * pl->num_splits * C;
         if (C == 4 && ctas >= static_cast<int64_t>(kManyWaves) * sms * 4 &&
             pq_decode_smem_bytes(M, Gs, 2) <= smem_cap)
-            split_plan(2, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+            split_plan(2, share_max(2), false, clusters, max_seq_len, req, sms, P, pl);
         else if (C == 4 && M == 8 && pl->num_splits >= 2 && pq_decode_smem_bytes(M, Gs, 8) > 0 &&
                  pq_decode_smem_bytes(M, Gs, 8) <= smem_cap)
             // a long request with 8 subspaces: clusters of 8, one subspace per
             // CTA, half the splits and so half the per-split fixed work
-            split_plan(8, share_max, false, clusters, max_seq_len, req, sms, P, pl);
+            split_plan(8, share_max(8), false, clusters, max_seq_len, req, sms, P, pl);
         pl->head_split = nsub;
         pl->smem = pq_decode_smem_bytes(M, Gs, pl->cluster);
     }

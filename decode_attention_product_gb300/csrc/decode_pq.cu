@@ -105,6 +105,8 @@ struct PqCfg {
     static_assert(ROW_FLOATS % 4 == 0 && INC_STRIDE % 4 == 0, "bulk copies of whole rows");
 };
 
+constexpr int kMaxChunks = kMaxStreamChunks;
+
 // CTAs per SM the register budget is sized for: shared memory (LUT, bins and
 // pushed rows all scale with G) allows about 4 / 2 / 1 resident CTAs.
 template <int G, int C>
@@ -225,6 +227,12 @@ __device__ __forceinline__ void load_vec_u(unsigned (&v)[N], const unsigned *src
     }
 }
 
+// A compile-time int as a value (slot index of a generic lambda).
+template <int N>
+struct IntC {
+    static constexpr int value = N;
+};
+
 // Code bytes of one token: M key codes then M value codes.
 template <int M>
 struct Codes;
@@ -313,7 +321,7 @@ __device__ __forceinline__ void encode_new_value(const __half *cbv, const float 
     for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[mi]);
 }
 
-template <int M, int G, int C, bool APPEND, bool E4M3>
+template <int M, int G, int C, bool APPEND, bool E4M3, bool STREAM>
 __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = PqCfg<M, G, C>;
     constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, TPT = S::TPT, NCH = S::NCH;
@@ -384,11 +392,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         }
     }
     const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
-    const size_t cb_unit = static_cast<size_t>(M) * K * DSUB;
-    // element offset of this CTA's K slice (the V slice is cb_unit further)
-    const size_t gK = ((static_cast<size_t>(set_ok ? set : 0) * Hkv + kvh) * 2) * cb_unit +
-                      static_cast<size_t>(rank) * S::CB_HALVES;
-    // TMA rows of the K slice (the V slice is M*K rows further)
+    // first codebook row of this CTA's K slice (rows of DSUB elements; the V
+    // slice is M*K rows further); element offsets are rows * DSUB
     const int rowK = ((set_ok ? set : 0) * Hkv + kvh) * 2 * M * K + rank * MC * K;
     // the K slice now; the V slice too with its own buffer and TMA, else once
     // the K slice has landed (own buffer) or is no longer read (shared buffer)
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, rowK + mi * K, &bar[0]);
             }
         } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, gK, &bar[0]);
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, static_cast<size_t>(rowK) * DSUB, &bar[0]);
         }
     }
 
@@ -506,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                     tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
             }
         } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, static_cast<size_t>(rowK + M * K) * DSUB,
+                                                          &bar[1]);
         }
     }
     tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
@@ -568,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                     tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
             }
         } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, gK + cb_unit, &bar[1]);
+            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, static_cast<size_t>(rowK + M * K) * DSUB,
+                                                          &bar[1]);
         }
     }
     if constexpr (C > 1) {
@@ -635,70 +642,198 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             snew[tid] = s_new;
         }
     }
-    float sc[TPT];
-    float mloc = s_new;
+    // A share of more than one chunk (TPT x TOK_PER_PASS tokens: the codes one
+    // thread holds) is streamed twice: pass 1 keeps each thread's (max, sum)
+    // online over the tokens, pass 2 re-reads the codes (from L2), recomputes
+    // the scores and bins the weights against the block's statistics.
+    constexpr int CHUNK = TPT * S::TOK_PER_PASS;
+    const int nch = (max(eS - a0, 0) + CHUNK - 1) / CHUNK;
+    float mx, lsum;
+    auto score = [&](const Codes<M> &cw) {
+        float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (i >= nslot) break;
-        if (valid & (1u << i)) {
-            float s = 0.f;
-#pragma unroll
-            for (int m = 0; m < M; ++m) s += lut[(m * K + cc[i].k(m)) * G + g];
-            sc[i] = s;
-            mloc = fmaxf(mloc, s);
-        }
-    }
-    // the max over the lanes of head g (one redux for G = 1), this thread's
-    // weights relative to it (kept in sc) and their sum over the same lanes
-    float mg;
-    if constexpr (G == 1) {
-        mg = warp_max_f32(mloc);
-    } else {
-        mg = mloc;
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, off));
-    }
-    float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mg) : 0.f;
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (i >= nslot) break;
-        if (valid & (1u << i)) {
-            sc[i] = fast_exp2(sc[i] - mg);
-            lt += sc[i];
-        }
-    }
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-    if (lane < G) {
-        red_m[warp * G + lane] = mg;
-        red_l[warp * G + lane] = lt;
-    }
-    __syncthreads();
-    float mx = red_m[g];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
-    float lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const float mw = red_m[w * G + g];
-        if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
-    }
-    // lsum >= 1 whenever this CTA holds a token of head g (its max weighs 1)
-    const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
-    const float cfac = lsum * (1.0f / 2147483648.0f);  // integer bin -> weight
-    {
-        // weight relative to mx, in bin units: sc[i] * 2^(mg - mx) * qscale
-        const float rq = (mg == -INFINITY) ? 0.f : (mg == mx ? qscale : fast_exp2(mg - mx) * qscale);
-#pragma unroll
+        for (int m = 0; m < M; ++m) s += lut[(m * K + cw.k(m)) * G + g];
+        return s;
+    };
+    if (!STREAM || nch <= 1) {
+        float sc[TPT];
+        float mloc = s_new;
+    #pragma unroll
         for (int i = 0; i < TPT; ++i) {
             if (i >= nslot) break;
             if (valid & (1u << i)) {
-                const unsigned q = __float2uint_rn(sc[i] * rq);
-#pragma unroll
-                for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
+                float s = 0.f;
+    #pragma unroll
+                for (int m = 0; m < M; ++m) s += lut[(m * K + cc[i].k(m)) * G + g];
+                sc[i] = s;
+                mloc = fmaxf(mloc, s);
             }
         }
+        // the max over the lanes of head g (one redux for G = 1), this thread's
+        // weights relative to it (kept in sc) and their sum over the same lanes
+        float mg;
+        if constexpr (G == 1) {
+            mg = warp_max_f32(mloc);
+        } else {
+            mg = mloc;
+    #pragma unroll
+            for (int off = G; off < 32; off <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, off));
+        }
+        float lt = (s_new != -INFINITY) ? fast_exp2(s_new - mg) : 0.f;
+    #pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            if (i >= nslot) break;
+            if (valid & (1u << i)) {
+                sc[i] = fast_exp2(sc[i] - mg);
+                lt += sc[i];
+            }
+        }
+    #pragma unroll
+        for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+        if (lane < G) {
+            red_m[warp * G + lane] = mg;
+            red_l[warp * G + lane] = lt;
+        }
+        __syncthreads();
+        mx = red_m[g];
+    #pragma unroll
+        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+        lsum = 0.f;
+    #pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = red_m[w * G + g];
+            if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+        }
+        // lsum >= 1 whenever this CTA holds a token of head g (its max weighs 1)
+        const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        {
+            // weight relative to mx, in bin units: sc[i] * 2^(mg - mx) * qscale
+            const float rq = (mg == -INFINITY) ? 0.f : (mg == mx ? qscale : fast_exp2(mg - mx) * qscale);
+    #pragma unroll
+            for (int i = 0; i < TPT; ++i) {
+                if (i >= nslot) break;
+                if (valid & (1u << i)) {
+                    const unsigned q = __float2uint_rn(sc[i] * rq);
+    #pragma unroll
+                    for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cc[i].vv(m)) * G + g], q);
+                }
+            }
+        }
+    } else if constexpr (STREAM) {
+        // This thread's tokens in halves of HT slots (half h: tokens
+        // a0 + (h*HT + i)*TOK_PER_PASS + jslot), software-pipelined: while
+        // half h is scored from one register slot, the codes of half h+1 are
+        // in flight into the other and the page ids of the next refill are
+        // loading, so neither the block-table nor the code latency is exposed.
+        constexpr int HT = TPT / 2;
+        const int NH = (max(eS - a0, 0) + HT * S::TOK_PER_PASS - 1) / (HT * S::TOK_PER_PASS);
+        int pidn[HT];
+        auto tok = [&](int h, int i) { return a0 + (h * HT + i) * S::TOK_PER_PASS + jslot; };
+        auto load_pids = [&](int h) {
+#pragma unroll
+            for (int i = 0; i < HT; ++i) {
+                const int t = tok(h, i);
+                pidn[i] = (h < NH && t < eS) ? __ldg(bt + static_cast<unsigned>(t) / P) : -2;
+            }
+        };
+        auto issue = [&](auto slot, int h) {                 // codes of half h into slot, from pidn
+            constexpr int sl = decltype(slot)::value;
+#pragma unroll
+            for (int i = 0; i < HT; ++i) {
+                valid &= ~(1u << (sl * HT + i));
+                const int t = tok(h, i);
+                if (h < NH && t < eS) {
+                    const int pg = pidn[i];
+                    if (pg >= 0 && static_cast<int64_t>(pg) < p.num_pages) {
+                        cc[sl * HT + i].load_global(codes_kvh + static_cast<size_t>(pg) * page_stride +
+                                                    (static_cast<unsigned>(t) % P) * (2 * M));
+                        valid |= 1u << (sl * HT + i);
+                    } else {
+                        bad_pg = true;
+                    }
+                }
+            }
+        };
+        // one pass: f(slot, h) consumes half h from its slot, which is then
+        // refilled with half h+2 (halves 0 and 1 are in their slots at entry)
+        auto pass = [&](auto f) {
+            load_pids(2);
+            for (int h0 = 0; h0 < NH; h0 += 2) {
+                f(IntC<0>{}, h0);
+                issue(IntC<0>{}, h0 + 2);
+                load_pids(h0 + 3);
+                if (h0 + 1 < NH) {
+                    f(IntC<1>{}, h0 + 1);
+                    issue(IntC<1>{}, h0 + 3);
+                    load_pids(h0 + 4);
+                }
+            }
+        };
+        // pass 1: (max, sum) online (chunk 0 = halves 0 and 1 came with the prologue)
+        float mrun = s_new, lrun = (s_new != -INFINITY) ? 1.0f : 0.f;
+        pass([&](auto slot, int) {
+            constexpr int sl = decltype(slot)::value;
+            float sc[HT];
+            float mc = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < HT; ++i)
+                if (valid & (1u << (sl * HT + i))) {
+                    sc[i] = score(cc[sl * HT + i]);
+                    mc = fmaxf(mc, sc[i]);
+                }
+            if (mc > mrun) {
+                lrun = (mrun == -INFINITY) ? 0.f : lrun * fast_exp2(mrun - mc);
+                mrun = mc;
+            }
+#pragma unroll
+            for (int i = 0; i < HT; ++i)
+                if (valid & (1u << (sl * HT + i))) lrun += fast_exp2(sc[i] - mrun);
+        });
+        if (bad_pg) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+        // (max, sum) pairs over the lanes of head g, then over the warps
+        float mt = mrun, lt = lrun;
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, mt, off);
+            const float l2 = __shfl_xor_sync(0xffffffffu, lt, off);
+            const float mn = fmaxf(mt, m2);
+            lt = (mt == mn ? lt : lt * fast_exp2(mt - mn)) + (m2 == mn ? l2 : l2 * fast_exp2(m2 - mn));
+            mt = mn;
+        }
+        if (lane < G) {
+            red_m[warp * G + lane] = mt;
+            red_l[warp * G + lane] = lt;
+        }
+        __syncthreads();
+        mx = red_m[g];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+        lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = red_m[w * G + g];
+            if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+        }
+        const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        // pass 2: the halves again from the start, weights binned against the
+        // block's statistics
+        load_pids(0);
+        issue(IntC<0>{}, 0);
+        load_pids(1);
+        issue(IntC<1>{}, 1);
+        pass([&](auto slot, int) {
+            constexpr int sl = decltype(slot)::value;
+#pragma unroll
+            for (int i = 0; i < HT; ++i)
+                if (valid & (1u << (sl * HT + i))) {
+                    const Codes<M> &cw = cc[sl * HT + i];
+                    const unsigned q = __float2uint_rn(fast_exp2(score(cw) - mx) * qscale);
+#pragma unroll
+                    for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cw.vv(m)) * G + g], q);
+                }
+        });
     }
+    const float cfac = lsum * (1.0f / 2147483648.0f);  // integer bin -> weight
     if constexpr (C > 1) fence_proxy_async_shared();  // the bins, for the bulk copies below
     __syncthreads();                                   // every atomic of this CTA is done
 
@@ -1506,11 +1641,34 @@ cudaError_t attend_g(const DecodeParams &p, int G, const Plan &plan, cudaStream_
     }
 }
 
+// Shares of several chunks stream in two passes; that instantiation exists
+// for fp16 codebooks and clusters of 4 or 8 (the planner keeps other shares to
+// one chunk).
+template <int C, bool E4M3>
+constexpr bool kStreams = !E4M3 && C >= 4;
+
+template <int M, int G, int C, bool APPEND, bool E4M3, bool STREAM>
+cudaError_t launch_kernel(const DecodeParams &p, const Plan &plan, cudaStream_t s);
+
 template <int M, int G, int C, bool APPEND, bool E4M3>
 cudaError_t launch_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     using S = PqCfg<M, G, C>;
-    auto kern = pq_decode_kernel<M, G, C, APPEND, E4M3>;
-    if (plan.share > S::MAX_SHARE || plan.share % kPage) return cudaErrorInvalidValue;
+    if (plan.share % kPage) return cudaErrorInvalidValue;
+    if (plan.share > S::MAX_SHARE) {
+        if constexpr (kStreams<C, E4M3>) {
+            if (plan.share > S::MAX_SHARE * kMaxChunks) return cudaErrorInvalidValue;
+            return launch_kernel<M, G, C, APPEND, E4M3, true>(p, plan, s);
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
+    return launch_kernel<M, G, C, APPEND, E4M3, false>(p, plan, s);
+}
+
+template <int M, int G, int C, bool APPEND, bool E4M3, bool STREAM>
+cudaError_t launch_kernel(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
+    using S = PqCfg<M, G, C>;
+    auto kern = pq_decode_kernel<M, G, C, APPEND, E4M3, STREAM>;
     static SmemAttr attr_state;                    // opt-in dynamic shared memory, per device
     const size_t need = S::smem();
     if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), need); e != cudaSuccess)

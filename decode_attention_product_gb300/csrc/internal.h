@@ -108,9 +108,12 @@ size_t pq_decode_smem_bytes(int M, int G, int cluster);
 // hold (its codes in shared memory, its scores in registers).
 size_t pq_attend_smem_bytes(int M, int G, int cluster, int split_len);
 int pq_attend_max_split(int M, int G);
-// Largest token share one cluster CTA handles (its tokens' codes live in
-// registers, a fixed number per thread); 0 for an unsupported (M, G).
+// Tokens of one chunk of a token-share CTA (its codes live in registers, a
+// fixed number per thread); 0 for an unsupported (M, G).  A CTA of a cluster
+// of 4 or 8 with fp16 codebooks streams up to kMaxStreamChunks chunks in two
+// passes; other CTAs hold one chunk.
 int pq_decode_max_share(int M, int G);
+constexpr int kMaxStreamChunks = 16;
 size_t fit_smem_bytes(int M, int n_samples);
 // The current limit of the decode kernels' waits (aq_set_wait_limit_ns).
 unsigned long long decode_wait_limit_ns();
