@@ -331,7 +331,7 @@ def build_cache(w, api, torch, layer=0):
 MIN_REGION_MS = 200.0     # every timed region lasts at least this long
 
 
-def time_steps(torch, step, R, steps, dist=False, min_region_ms=MIN_REGION_MS, clocks=None):
+def time_steps(torch, step, R, steps, dist=False, min_region_ms=None, clocks=None):
     """Device time per step of a rotation of steps, replayed from CUDA graphs.
 
     `step(i)` launches step i, which uses input copy i % R.  One graph holds R
@@ -350,6 +350,8 @@ def time_steps(torch, step, R, steps, dist=False, min_region_ms=MIN_REGION_MS, c
                 step(i)
         return g
 
+    if min_region_ms is None:
+        min_region_ms = MIN_REGION_MS
     g_cycle = capture(R)
     g_cycle.replay()
     torch.cuda.synchronize()
@@ -813,6 +815,7 @@ def measure_e4m3(args, w, api, torch, base, Lmax, units, T, local_rank=0):
 
 
 def main():
+    global MIN_REGION_MS
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -827,7 +830,10 @@ def main():
     ap.add_argument("--two-call", action="store_true",
                     help="time aq_encode_append + aq_decode_attention instead of the fused step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--min-region-ms", type=float, default=200.0,
+                    help="shortest timed region (repeats of the K steps); lower only for profiler runs")
     args = ap.parse_args()
+    MIN_REGION_MS = args.min_region_ms
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
