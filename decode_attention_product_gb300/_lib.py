@@ -41,6 +41,9 @@ SIGNATURES = {
                                   P, P], i32),
     "aq_decode_step": ([P, i32, i32, i32, P, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32, i32,
                         P, P, sz, P, P], i32),
+    "aq_decode_step_host_staging": ([i32, i32, i32], sz),
+    "aq_decode_step_host": ([P, i32, i32, i32, P, P, P, i64, P, i64, P, P, i32, P, i32, f32, i32, i32, P, P, sz, P,
+                             sz, P, P], i32),
     "aq_decode_step_mixed": ([P, i32, i32, i32, i32, P, P, P, i64, P, i64, P, i64, P, P, i32, P, i32, f32,
                               i32, P, P, sz, P, P], i32),
     "aq_decode_step_mixed_workspace": ([P, i32, i32, i32, i32, i32, P], i32),

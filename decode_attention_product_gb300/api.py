@@ -304,13 +304,18 @@ class DecodeStep:
     Holds the cache tensors, the workspace, the output and a device status
     word.  `run(q, new_kv)` launches the step on the current stream.
     `capture_host(q_host, kv_host, out_host)` records the whole step -- copies
-    of the pinned host inputs to the device, the two calls, the copy of the
-    output back to pinned host memory -- into a CUDA graph; `replay()` launches
-    it and, with wait=True, blocks until the output is on the host.
+    of the pinned host inputs to the device, the step, the copy of the output
+    back to pinned host memory -- into a CUDA graph; `replay()` launches it and,
+    with wait=True, blocks until the output is on the host.  `launch()` /
+    `wait()` split that in two, so that a caller keeping two sets of pinned
+    buffers can launch step i before it waits for step i-1's output (the copies
+    and the kernel of one step overlap the host's work on the other).
+    `overlap=True` launches the step as a programmatic dependent of the
+    preceding kernel (aq_decode_step's AQ_STEP_OVERLAP contract).
     """
 
     def __init__(self, code_pages, codebooks, req_set, block_table, seq_lens, max_seq_len,
-                 new_slot, new_set, num_q_heads, scale=None, num_splits=0):
+                 new_slot, new_set, num_q_heads, scale=None, num_splits=0, overlap=False):
         self.code_pages, self.codebooks = code_pages, codebooks
         self.req_set, self.block_table, self.seq_lens = req_set, block_table, seq_lens
         self.max_seq_len = int(max_seq_len)
@@ -326,30 +331,60 @@ class DecodeStep:
         self.out = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32, device=dev)
         self.graph = None
         self._host = None
+        self._done = None
+        self._io = None
+        self.overlap = overlap
 
     def run(self, q, new_kv, out=None):
         return decode_step(q, new_kv, self.code_pages, self.codebooks, self.req_set,
                            self.block_table, self.seq_lens, self.max_seq_len, self.scale,
-                           self.num_splits, out=self.out if out is None else out,
+                           self.num_splits, overlap=self.overlap, out=self.out if out is None else out,
                            workspace=self.workspace, status=self.status)
 
-    def capture_host(self, q_host, kv_host, out_host):
-        """Capture copy-in, step, copy-out into a CUDA graph (pinned host tensors)."""
-        for t, n in ((q_host, "q_host"), (kv_host, "kv_host"), (out_host, "out_host")):
-            if t.is_cuda or not t.is_pinned():
-                raise ValueError(f"{n} must be a pinned host tensor")
-        q_d = torch.empty(q_host.shape, dtype=q_host.dtype, device=self.out.device)
-        kv_d = torch.empty(kv_host.shape, dtype=kv_host.dtype, device=self.out.device)
-        self._host = (q_host, kv_host, out_host, q_d, kv_d)
+    def pinned_io(self):
+        """(q_host, kv_host, out_host): pinned host views of one input buffer
+        (q [B][Hq][D] fp32 then the new K/V [B][Hkv][2][D] fp16) and an output
+        buffer [B][Hq][D] fp32, for capture_host() without arguments: the inputs
+        then reach the device in one copy."""
+        if self._io is None:
+            nq = self.B * self.Hq * HEAD_DIM * 4
+            nkv = self.B * self.Hkv * 2 * HEAD_DIM * 2
+            buf = torch.empty(nq + nkv, dtype=torch.uint8).pin_memory()
+            q = buf[:nq].view(torch.float32).view(self.B, self.Hq, HEAD_DIM)
+            kv = buf[nq:].view(torch.float16).view(self.B, self.Hkv, 2, HEAD_DIM)
+            out = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32).pin_memory()
+            self._io = (buf, q, kv, out)
+        return self._io[1:]
+
+    def capture_host(self, q_host=None, kv_host=None, out_host=None):
+        """Capture copy-in, step, copy-out into a CUDA graph (pinned host
+        tensors; none given: this object's pinned_io(), copied in one piece)."""
+        dev = self.out.device
+        if q_host is None:
+            self.pinned_io()
+            buf, q_host, kv_host, out_host = self._io
+            buf_d = torch.empty(buf.shape, dtype=buf.dtype, device=dev)
+            nq = q_host.numel() * 4
+            q_d = buf_d[:nq].view(torch.float32).view(q_host.shape)
+            kv_d = buf_d[nq:].view(torch.float16).view(kv_host.shape)
+            copies = [(buf_d, buf)]
+        else:
+            for t, n in ((q_host, "q_host"), (kv_host, "kv_host"), (out_host, "out_host")):
+                if t.is_cuda or not t.is_pinned():
+                    raise ValueError(f"{n} must be a pinned host tensor")
+            q_d = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+            kv_d = torch.empty(kv_host.shape, dtype=kv_host.dtype, device=dev)
+            copies = [(q_d, q_host), (kv_d, kv_host)]
+        self._host = (q_host, kv_host, out_host, q_d, kv_d, copies)
         # one eager run sets kernel attributes outside the capture
-        q_d.copy_(q_host)
-        kv_d.copy_(kv_host)
+        for d, h in copies:
+            d.copy_(h)
         self.run(q_d, kv_d)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            q_d.copy_(q_host, non_blocking=True)
-            kv_d.copy_(kv_host, non_blocking=True)
+            for d, h in copies:
+                d.copy_(h, non_blocking=True)
             self.run(q_d, kv_d)
             out_host.copy_(self.out, non_blocking=True)
         self.graph = g
@@ -359,6 +394,80 @@ class DecodeStep:
         self.graph.replay()
         if wait:
             torch.cuda.current_stream().synchronize()
+
+    def launch(self):
+        """Replay the captured step on the current stream without waiting
+        (replays on different streams may overlap: use distinct caches)."""
+        self.graph.replay()
+        if self._done is None:
+            self._done = torch.cuda.Event()
+        self._done.record()
+
+    def wait(self):
+        """Block until the last launch()'s output is in pinned host memory."""
+        self._done.synchronize()
+
+    def check_status(self):
+        """Raise if a kernel flagged a data error (reads the status word)."""
+        st = int(self.status.item())
+        if st:
+            raise RuntimeError(f"device status {st:#x}")
+
+
+class HostDecodeStep:
+    """aq_decode_step_host for a fixed batch and cache: one C call per step
+    enqueues the copy of the query and the new K/V from pinned host memory, the
+    fused step and the copy of the output back to pinned host memory, on
+    `stream` (a torch.cuda.Stream; the current one if None).
+
+    `q_host`, `kv_host`, `out_host` are the pinned tensors (write the next
+    step's inputs into the first two, read the output from the last one after
+    `sync()`); `launch()` enqueues one step.  The call's arguments are
+    marshalled once, here.
+    """
+
+    def __init__(self, code_pages, codebooks, req_set, block_table, seq_lens, max_seq_len,
+                 num_q_heads, scale=None, num_splits=0, stream=None):
+        _need(code_pages, torch.uint8, "code_pages", 5)
+        e4m3 = codebooks.dtype == torch.uint8
+        _need(codebooks, torch.uint8 if e4m3 else torch.float16, "codebooks", 6)
+        for t, n in ((req_set, "req_set"), (seq_lens, "seq_lens")):
+            _need(t, torch.int32, n, 1)
+        _need(block_table, torch.int32, "block_table", 2)
+        self.B, self.Hq = int(seq_lens.shape[0]), int(num_q_heads)
+        self.Hkv, self.M = int(codebooks.shape[1]), int(codebooks.shape[3])
+        dev = code_pages.device
+        self.stream = stream or torch.cuda.current_stream()
+        self.q_host = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32).pin_memory()
+        self.kv_host = torch.empty((self.B, self.Hkv, 2, HEAD_DIM), dtype=torch.float16).pin_memory()
+        self.out_host = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32).pin_memory()
+        lib = _lib.load()
+        n = lib.aq_decode_step_host_staging(self.B, self.Hq, self.Hkv)
+        self.staging = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.workspace = workspace_for(self.B, self.Hq, self.Hkv, int(max_seq_len), self.M, num_splits,
+                                       device=dev)
+        self.status = new_status(dev)
+        self._keep = (code_pages, codebooks, req_set, block_table, seq_lens)
+        self._cfg = _lib.config(self.M, page_size=code_pages.shape[2])
+        scale = HEAD_DIM ** -0.5 if scale is None else scale
+        self._fn = lib.aq_decode_step_host
+        self._args = (ctypes.byref(self._cfg), self.B, self.Hq, self.Hkv, _ptr(self.q_host), _ptr(self.kv_host),
+                      _ptr(code_pages), code_pages.shape[0], _ptr(codebooks), codebooks.shape[0], _ptr(req_set),
+                      _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_seq_len), float(scale),
+                      num_splits, _lib.STEP_E4M3 if e4m3 else 0, _ptr(self.out_host), _ptr(self.staging),
+                      self.staging.numel(), _ptr(self.workspace),
+                      self.workspace.numel() if self.workspace is not None else 0, _ptr(self.status),
+                      ctypes.c_void_p(self.stream.cuda_stream))
+
+    def launch(self):
+        """Enqueue one step (copies in, step, copy out) on the stream."""
+        st = self._fn(*self._args)
+        if st != _lib.AQ_OK:
+            _lib.check(st, "aq_decode_step_host")
+
+    def sync(self):
+        """Wait until the last launched step's output is in out_host."""
+        self.stream.synchronize()
 
     def check_status(self):
         """Raise if a kernel flagged a data error (reads the status word)."""

@@ -579,6 +579,46 @@ aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch, int32_t num_q_h
                        device_status, stream);
 }
 
+size_t aq_decode_step_host_staging(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads) {
+    const size_t q = static_cast<size_t>(batch) * num_q_heads * kHeadDim * sizeof(float);
+    const size_t kv = static_cast<size_t>(batch) * num_kv_heads * 2 * kHeadDim * 2;
+    return (q + 255) / 256 * 256 + (kv + 255) / 256 * 256 + (q + 255) / 256 * 256;
+}
+
+aq_status aq_decode_step_host(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                              const float *q_host, const void *kv_new_host, uint8_t *code_pages, int64_t num_pages,
+                              const void *codebooks_f16, int64_t num_sets, const int32_t *req_set,
+                              const int32_t *block_table, int32_t max_pages, const int32_t *seq_lens,
+                              int32_t max_seq_len, float scale, int32_t num_splits, int32_t flags, float *out_host,
+                              void *staging, size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                              int32_t *device_status, aq_stream_t stream) {
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1) return AQ_ERR_INVALID_ARGUMENT;
+    if (batch == 0) return AQ_OK;
+    if (!q_host || !kv_new_host || !out_host || !staging) return AQ_ERR_INVALID_ARGUMENT;
+    if (misaligned(staging)) return AQ_ERR_INVALID_ARGUMENT;
+    if (staging_bytes < aq_decode_step_host_staging(batch, num_q_heads, num_kv_heads))
+        return AQ_ERR_WORKSPACE_TOO_SMALL;
+    const size_t qb = static_cast<size_t>(batch) * num_q_heads * kHeadDim * sizeof(float);
+    const size_t kvb = static_cast<size_t>(batch) * num_kv_heads * 2 * kHeadDim * 2;
+    unsigned char *st = static_cast<unsigned char *>(staging);
+    float *q_d = reinterpret_cast<float *>(st);
+    void *kv_d = st + (qb + 255) / 256 * 256;
+    float *out_d = reinterpret_cast<float *>(st + (qb + 255) / 256 * 256 + (kvb + 255) / 256 * 256);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the copies precede the step in stream order; no programmatic overlap
+    // with a preceding kernel (the step's inputs come from the copies)
+    cudaError_t e = cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(kv_d, kv_new_host, kvb, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    aq_status r = aq_decode_step(cfg, batch, num_q_heads, num_kv_heads, q_d, kv_d, code_pages, num_pages,
+                                 codebooks_f16, num_sets, req_set, block_table, max_pages, seq_lens, max_seq_len, scale,
+                                 num_splits, flags & ~AQ_STEP_OVERLAP, out_d, workspace, workspace_bytes,
+                                 device_status, stream);
+    if (r != AQ_OK) return r;
+    e = cudaMemcpyAsync(out_host, out_d, qb, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? AQ_OK : cuda_fail(e);
+}
+
 aq_status aq_decode_attention_fp16(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
                                    int32_t num_kv_heads, const float *q, const void *kv_pages_f16,
                                    int64_t num_pages, const int32_t *block_table, int32_t max_pages,

@@ -316,6 +316,36 @@ aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch,
                          aq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * aq_decode_step_host -- aq_decode_step with the query, the new K/V and the
+ * output in host memory (a serving loop's view: one call per step).  An
+ * interface convenience of this library; the pages describe the step itself.
+ *
+ * Enqueues on `stream`: the copy of q_host [B][Hq][D] fp32 and kv_new_host
+ * [B][Hkv][2][D] fp16 into the caller's device `staging`, the fused step, and
+ * the copy of the output into out_host [B][Hq][D] fp32.  Returns once they
+ * are enqueued; out_host holds the step's output when the stream has passed
+ * this point.  For asynchronous copies the host buffers are page-locked
+ * (pinned); pageable ones make the copies synchronous.
+ *   staging        device memory of >= aq_decode_step_host_staging() bytes,
+ *                  16-byte aligned, owned by the caller (no allocation here)
+ *   flags          AQ_STEP_E4M3 only (AQ_STEP_OVERLAP is ignored: the step's
+ *                  inputs come from the copies just before it)
+ *   other arguments as aq_decode_step.
+ * ------------------------------------------------------------------------- */
+size_t aq_decode_step_host_staging(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads);
+aq_status aq_decode_step_host(const aq_pq_config *cfg, int32_t batch, int32_t num_q_heads,
+                              int32_t num_kv_heads, const float *q_host,
+                              const void *kv_new_host, uint8_t *code_pages,
+                              int64_t num_pages, const void *codebooks_f16,
+                              int64_t num_sets, const int32_t *req_set,
+                              const int32_t *block_table, int32_t max_pages,
+                              const int32_t *seq_lens, int32_t max_seq_len, float scale,
+                              int32_t num_splits, int32_t flags, float *out_host,
+                              void *staging, size_t staging_bytes, void *workspace,
+                              size_t workspace_bytes, int32_t *device_status,
+                              aq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * aq_decode_attention_fp16 -- the uncompressed comparison point: the same
  * paged decode attention over an fp16 K/V cache (AQPIM blog §2.1 cache).
  * Only cfg->head_dim and cfg->page_size are used.

@@ -535,3 +535,78 @@ def test_decode_step_bad_new_page_flagged(A, kernel):
         pg = p["block_table"][0, j]
         if 0 <= pg < p["num_pages"]:
             assert np.array_equal(after[pg], before[pg])
+
+
+def test_decode_step_graphs_with_pinned_buffers(A, orc):
+    """api.DecodeStep: two captured graphs (copy in, fused step, copy out) with
+    their own pinned buffers and inputs, the second launched before the first
+    is waited for; each host output matches the oracle's step on its inputs."""
+    B, Hq, Hkv, M, lens = 2, 8, 8, 4, [700, 1300]
+    p = W.paged_codes_problem(55, B, Hq, Hkv, M, lens, num_sets=B)
+    rng = np.random.default_rng(55)
+    slots = np.array([p["block_table"][b, (L - 1) // 16] * 16 + (L - 1) % 16 for b, L in enumerate(lens)], np.int64)
+    pages = dev(p["code_pages"])
+    args = (pages, dev(p["codebooks"]), dev(p["req_set"]), dev(p["block_table"]), dev(p["seq_lens"]), max(lens),
+            dev(slots), dev(p["req_set"]), Hq, 1.0 / np.sqrt(128))
+    sets, steps = [], []
+    for i in range(2):
+        q = rng.standard_normal((B, Hq, 128)).astype(np.float32)
+        kv = rng.standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+        ds = A.DecodeStep(*args)
+        if i == 0:                                   # the caller's three pinned tensors
+            host = (torch.from_numpy(q).pin_memory(), torch.from_numpy(kv).pin_memory(),
+                    torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory())
+            ds.capture_host(*host)
+        else:                                        # the step's own packed pinned buffers
+            host = ds.pinned_io()
+            host[0].copy_(torch.from_numpy(q))
+            host[1].copy_(torch.from_numpy(kv))
+            ds.capture_host()
+        sets.append((q, kv, host))
+        steps.append(ds)
+    steps[0].launch()
+    steps[1].launch()
+    steps[0].wait()
+    got0 = sets[0][2][2].numpy().copy()
+    steps[1].wait()
+    got1 = sets[1][2][2].numpy().copy()
+    for ds in steps:
+        ds.check_status()
+    for (q, kv, _), got in zip(sets, (got0, got1)):
+        want_pages = p["code_pages"].copy()
+        orc.encode_append(kv, p["req_set"], slots, p["codebooks"], want_pages, 16)
+        want = orc.decode_attention(q, want_pages, p["codebooks"], p["req_set"], p["block_table"], p["seq_lens"],
+                                    1.0 / np.sqrt(128), 16)
+        close(got, want)
+
+
+def test_decode_step_host_buffers(A, orc):
+    """aq_decode_step_host (api.HostDecodeStep): inputs and output in pinned
+    host memory, copies and the step enqueued by one call; the output equals
+    aq_decode_step's on device copies of the same inputs bit for bit, and the
+    oracle's within tolerance; the new codes land in the cache."""
+    B, Hq, Hkv, M, lens = 3, 8, 4, 4, [333, 1024, 17]
+    p = W.paged_codes_problem(66, B, Hq, Hkv, M, lens, num_sets=B)
+    rng = np.random.default_rng(66)
+    q = rng.standard_normal((B, Hq, 128)).astype(np.float32)
+    kv = rng.standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+    pages_h, pages_d = dev(p["code_pages"]), dev(p["code_pages"])
+    args = (dev(p["codebooks"]), dev(p["req_set"]), dev(p["block_table"]), dev(p["seq_lens"]), max(lens))
+    hs = A.HostDecodeStep(pages_h, *args, Hq, 1.0 / np.sqrt(128))
+    hs.q_host.copy_(torch.from_numpy(q))
+    hs.kv_host.copy_(torch.from_numpy(kv))
+    hs.launch()
+    hs.sync()
+    hs.check_status()
+    got = hs.out_host.numpy().copy()
+    ref = A.decode_step(dev(q), dev(kv), pages_d, args[0], args[1], args[2], args[3], max(lens), 1.0 / np.sqrt(128))
+    torch.cuda.synchronize()
+    assert np.array_equal(got, ref.cpu().numpy())
+    assert torch.equal(pages_h, pages_d)
+    slots = np.array([p["block_table"][b, (L - 1) // 16] * 16 + (L - 1) % 16 for b, L in enumerate(lens)], np.int64)
+    want_pages = p["code_pages"].copy()
+    orc.encode_append(kv, p["req_set"], slots, p["codebooks"], want_pages, 16)
+    assert np.array_equal(pages_h.cpu().numpy(), want_pages)
+    want = orc.decode_attention(q, want_pages, p["codebooks"], p["req_set"], p["block_table"], p["seq_lens"],
+                                1.0 / np.sqrt(128), 16)
+    close(got, want)
