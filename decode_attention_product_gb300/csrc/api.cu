@@ -416,7 +416,8 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens, int32_t 
 // elements, one 256-row box per subspace, with the 64-byte (Dsub 32) or
 // 32-byte (Dsub 16) swizzle that places 16-byte chunk c of row k at
 // c ^ ((k / (128 / row bytes)) mod chunks per row) -- the kernels' layout.
-static cudaError_t codebook_tensor_map(CUtensorMap *map, const void *codebooks, int64_t num_sets, int Hkv, int M) {
+static cudaError_t codebook_tensor_map(CUtensorMap *map, const void *codebooks, int64_t num_sets, int Hkv, int M,
+                                       bool e4m3 = false) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q{};
@@ -431,13 +432,16 @@ static cudaError_t codebook_tensor_map(CUtensorMap *map, const void *codebooks, 
     const cuuint64_t rows = static_cast<cuuint64_t>(num_sets > 0 ? num_sets : 1) * Hkv * 2 * M * kCodewords;
     if (rows >= (1ull << 31)) return cudaErrorInvalidValue;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dsub), rows};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(dsub) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(dsub) * (e4m3 ? 1 : 2)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(dsub), static_cast<cuuint32_t>(kCodewords)};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(codebooks), dims, strides,
-                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              dsub == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // fp16 rows of 64 / 32 bytes: the 64B / 32B swizzle; E4M3 rows of 32 bytes:
+    // the 32B swizzle, of 16 bytes: none (one chunk per row)
+    const CUtensorMapSwizzle swz = e4m3 ? (dsub == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE)
+                                        : (dsub == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    const CUresult r = encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                              const_cast<void *>(codebooks), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -503,9 +507,9 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
     if (st != AQ_OK) return st;
     if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return AQ_ERR_WORKSPACE_TOO_SMALL;
     DecodeParams p{};
-    // a TMA view of fp16 codebooks for the kernels' slice copies
-    p.cb_map_ok = !fp16 && !(flags & AQ_STEP_E4M3) &&
-                  codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv, cfg->num_subspaces) == cudaSuccess;
+    // a TMA view of the codebooks (fp16 or E4M3) for the kernels' slice copies
+    p.cb_map_ok = !fp16 && codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv, cfg->num_subspaces,
+                                               (flags & AQ_STEP_E4M3) != 0) == cudaSuccess;
     if (pl.kernel == 2 && !p.cb_map_ok) {
         // no TMA view of these codebooks (too many rows): the token-share kernel
         const size_t ws_need = pl.workspace;
@@ -736,8 +740,8 @@ aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t n
         p.share = ppq.share;
         p.overlap = (flags & AQ_STEP_OVERLAP) ? 1 : 0;
         p.codebook_e4m3 = (flags & AQ_STEP_E4M3) ? 1 : 0;
-        p.cb_map_ok = !p.codebook_e4m3 &&
-                      codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv - n16, cfg->num_subspaces) == cudaSuccess;
+        p.cb_map_ok = codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv - n16, cfg->num_subspaces,
+                                          p.codebook_e4m3 != 0) == cudaSuccess;
         if (ppq.kernel == 2 && !p.cb_map_ok) {
             st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
                            &ppq, true, false);

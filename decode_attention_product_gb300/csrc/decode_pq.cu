@@ -140,43 +140,75 @@ __device__ __forceinline__ void copy_slice(__half *dst, const __half *src, uint6
     cp_async_mbar_arrive(bar);
 }
 
-// The same slice from FP8 E4M3 codebooks (one byte per element, same element
-// order): 8-byte loads widened exactly to fp16 and stored in the same layout,
-// then one plain arrival per thread on `bar`.
-template <int DSUB, int CHUNKS>
-__device__ __forceinline__ void copy_slice_e4m3(__half *dst, const uint8_t *src, uint64_t *bar) {
-    constexpr int NCH = DSUB / 8, NI = CHUNKS / kThreads;
-    const int t = static_cast<int>(threadIdx.x);
-    const int r0 = t / NCH, c = t % NCH;
-    const uint32_t d0 = smem_u32(dst) + static_cast<uint32_t>(r0 * NCH + chunk_pos<DSUB>(r0, c)) * 16u;
-    const uint8_t *s0 = src + static_cast<size_t>(t) * 8;
-    uint2 raw[NI];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) raw[i] = ldg_stream_v2(s0 + static_cast<size_t>(i) * kThreads * 8);
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        const uint32_t w[4] = {raw[i].x & 0xffffu, raw[i].x >> 16, raw[i].y & 0xffffu, raw[i].y >> 16};
-        uint32_t h[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[j]), __NV_E4M3);
-            h[j] = static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-        }
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d0 + static_cast<uint32_t>(i * kThreads * 16)),
-                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                     : "memory");
-    }
-    mbar_arrive(bar);
+// Eight fp16 values (one 16-byte chunk) as four packed fp32 pairs.
+__device__ __forceinline__ void to_f2p4(const uint4 &u, unsigned long long (&f)[4]) {
+    f[0] = h2_to_f2p(u.x);
+    f[1] = h2_to_f2p(u.y);
+    f[2] = h2_to_f2p(u.z);
+    f[3] = h2_to_f2p(u.w);
 }
 
-// A codebook slice of `elems` elements from offset `off` of the codebook array
-// (fp16 or, with E4M3, FP8 codes) into the swizzled fp16 layout.
-template <int DSUB, int CHUNKS, bool E4M3>
-__device__ __forceinline__ void copy_codebook_slice(__half *dst, const void *codebooks, size_t off, uint64_t *bar) {
-    if constexpr (E4M3)
-        copy_slice_e4m3<DSUB, CHUNKS>(dst, static_cast<const uint8_t *>(codebooks) + off, bar);
-    else
-        copy_slice<DSUB, CHUNKS>(dst, static_cast<const __half *>(codebooks) + off, bar);
+// Raw E4M3 slices (one byte per element, rows of DSUB bytes): 16-byte chunk e
+// of row k sits at e ^ ((k / 4) & 1) when rows are 32 bytes (the 32-byte TMA
+// swizzle: rows k..k+7 read at once cover every bank group), in place when
+// they are 16 bytes (one chunk).
+template <int DSUB>
+__device__ __forceinline__ int e8_pos(int k, int e) {
+    if constexpr (DSUB == 32) return e ^ ((k >> 2) & 1);
+    else return e;
+}
+
+// 8 E4M3 values (two 32-bit words, first value in the lowest byte) as four
+// packed fp32 pairs: widened exactly through fp16.
+__device__ __forceinline__ void e4m3x8_to_f2p4(uint32_t lo, uint32_t hi, unsigned long long (&f)[4]) {
+    const uint32_t w[4] = {lo & 0xffffu, lo >> 16, hi & 0xffffu, hi >> 16};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[j]), __NV_E4M3);
+        f[j] = h2_to_f2p(static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16));
+    }
+}
+
+// Calls fn(c, f) for the 8-element chunks c = 0 .. DSUB/8-1 of codeword row
+// `row` of a slice, f = its values as four packed fp32 pairs (in order): fp16
+// slices in the swizzled chunk layout, or raw E4M3 slices (two chunks per
+// 16-byte load).
+template <int DSUB, bool E4M3, typename F>
+__device__ __forceinline__ void for_row_chunks(const void *slice, int row, F &&fn) {
+    if constexpr (!E4M3) {
+        constexpr int NCH = DSUB / 8;
+        const uint4 *r = reinterpret_cast<const uint4 *>(slice) + row * NCH;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            unsigned long long f[4];
+            to_f2p4(r[chunk_pos<DSUB>(row, c)], f);
+            fn(c, f);
+        }
+    } else {
+        constexpr int NE = DSUB / 16;
+        const uint4 *r = reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(slice) + row * DSUB);
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const uint4 u = r[e8_pos<DSUB>(row, e)];
+            unsigned long long f[4];
+            e4m3x8_to_f2p4(u.x, u.y, f);
+            fn(2 * e, f);
+            e4m3x8_to_f2p4(u.z, u.w, f);
+            fn(2 * e + 1, f);
+        }
+    }
+}
+
+// A raw E4M3 slice [rows][DSUB] bytes by per-thread 16-byte cp.async copies
+// into the e8_pos layout (the TMA copy's fallback); one arrival per thread.
+template <int DSUB, int ROWS>
+__device__ __forceinline__ void copy_slice_e4m3_raw(unsigned char *dst, const uint8_t *src, uint64_t *bar) {
+    constexpr int NE = DSUB / 16, CHUNKS = ROWS * NE;
+    for (int q = static_cast<int>(threadIdx.x); q < CHUNKS; q += kThreads) {
+        const int row = q / NE, e = q % NE;
+        cp_async_16(smem_u32(dst + row * DSUB + e8_pos<DSUB>(row, e) * 16), src + static_cast<size_t>(q) * 16);
+    }
+    cp_async_mbar_arrive(bar);
 }
 
 template <int N>
@@ -277,12 +309,6 @@ __device__ __forceinline__ float sqdist8(float d, const float *x, const unsigned
     return d;
 }
 
-__device__ __forceinline__ void to_f2p4(const uint4 &u, unsigned long long (&f)[4]) {
-    f[0] = h2_to_f2p(u.x);
-    f[1] = h2_to_f2p(u.y);
-    f[2] = h2_to_f2p(u.z);
-    f[3] = h2_to_f2p(u.w);
-}
 
 // CTA-wide argmin, lowest index on ties, of one distance per thread (thread =
 // codeword): the warp's smallest distance by an integer min-reduction over the
@@ -301,20 +327,16 @@ __device__ __forceinline__ void warp_argmin_into(float d, unsigned long long *sl
 // The new token's value codes of the owned subspaces (thread = codeword):
 // exact distances to its value sub-vectors xv [MC][DSUB], argmin into
 // keys[0..MC) (visible to all threads after the next barrier).
-template <int DSUB, int MC, int K, int NCH>
+template <int DSUB, int MC, int K, int NCH, bool E4M3 = false>
 __device__ __forceinline__ void encode_new_value(const __half *cbv, const float *xv, unsigned long long *keys) {
     const int tid = threadIdx.x;
     float dv[MC];
 #pragma unroll
     for (int mi = 0; mi < MC; ++mi) {
-        const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
         float d = 0.f;
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            unsigned long long f[4];
-            to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
+        for_row_chunks<DSUB, E4M3>(cbv, mi * K + tid, [&](int c, const unsigned long long (&f)[4]) {
             d = sqdist8(d, xv + mi * DSUB + c * 8, f);
-        }
+        });
         dv[mi] = d;
     }
 #pragma unroll
@@ -329,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);   // CK, CV, LUT in, bins in, query
     int *sflag = reinterpret_cast<int *>(smem + S::OFF_MISC);           // [0] local bad, [1] all
     __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CB);       // K slice
-    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);      // V slice (may alias it)
+    // V slice: its own buffer, or the K slice's; raw E4M3 slices are half the
+    // size, so with a shared buffer the V slice takes its upper half
+    constexpr bool SHARED_V = S::SHARED_CB && !E4M3;
+    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV + (S::SHARED_CB && E4M3 ? S::CB_BYTES / 2 : 0));
     float *lut = reinterpret_cast<float *>(smem + S::OFF_LUT);
     float *bins = reinterpret_cast<float *>(smem + S::OFF_BINS);
     float *inc = reinterpret_cast<float *>(smem + S::OFF_INC);
@@ -357,7 +382,27 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // slices by TMA (one elected thread, hardware swizzle) when the base is
     // 1024-byte aligned and a tensor map was made; else by per-thread 16-byte
     // copies into the same layout (one arrival per thread)
-    const bool use_tma = !E4M3 && p.cb_map_ok && (smem_u32(smem) & 1023u) == 0;
+    const bool use_tma = p.cb_map_ok && (smem_u32(smem) & 1023u) == 0;
+    // bytes of one slice as copied (E4M3 slices stay one byte per element and
+    // are widened by their readers) and of one subspace's box within it
+    constexpr uint32_t SLICE_BYTES = E4M3 ? S::CB_BYTES / 2 : S::CB_BYTES;
+    constexpr int SUB_BYTES = K * DSUB * (E4M3 ? 1 : 2);
+    auto slice_copy = [&](void *dst, int row0, uint64_t *b) {      // rows row0 .. of the codebooks
+        if (use_tma) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(b, SLICE_BYTES);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi)
+                    tma_load_2d(static_cast<unsigned char *>(dst) + mi * SUB_BYTES, &p.cb_map, 0, row0 + mi * K, b);
+            }
+        } else if constexpr (E4M3) {
+            copy_slice_e4m3_raw<DSUB, MC * K>(static_cast<unsigned char *>(dst),
+                                              static_cast<const uint8_t *>(p.codebooks) + static_cast<size_t>(row0) * DSUB, b);
+        } else {
+            copy_slice<DSUB, S::CB_CHUNKS>(static_cast<__half *>(dst),
+                                           static_cast<const __half *>(p.codebooks) + static_cast<size_t>(row0) * DSUB, b);
+        }
+    };
     if (tid == 0) {
         mbar_init(&bar[0], use_tma ? 1 : kThreads);
         mbar_init(&bar[1], use_tma ? 1 : kThreads);
@@ -397,17 +442,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     const int rowK = ((set_ok ? set : 0) * Hkv + kvh) * 2 * M * K + rank * MC * K;
     // the K slice now; the V slice too with its own buffer and TMA, else once
     // the K slice has landed (own buffer) or is no longer read (shared buffer)
-    if (set_ok) {
-        if (use_tma) {
-            if (tid == 0) {
-                mbar_arrive_expect_tx(&bar[0], S::CB_BYTES);
-#pragma unroll
-                for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, rowK + mi * K, &bar[0]);
-            }
-        } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbk, p.codebooks, static_cast<size_t>(rowK) * DSUB, &bar[0]);
-        }
-    }
+    if (set_ok) slice_copy(cbk, rowK, &bar[0]);
 
     // ---- request-level checks: uniform over the cluster ------------------
     int bad0 = 0;
@@ -502,19 +537,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     bool tmo = !mbar_wait_limit(&bar[0], 0, p.wait_limit_ns);
     // the V slice into its own buffer once the K slice has landed, so that
     // the K slice, which the table build waits for, has the bandwidth first
-    if constexpr (!S::SHARED_CB) {
-        if (use_tma) {
-            if (tid == 0) {
-                mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
-#pragma unroll
-                for (int mi = 0; mi < MC; ++mi)
-                    tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
-            }
-        } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, static_cast<size_t>(rowK + M * K) * DSUB,
-                                                          &bar[1]);
-        }
-    }
+    if constexpr (!SHARED_V) slice_copy(cbv, rowK + M * K, &bar[1]);
     tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
     if constexpr (C > 1) cluster_wait_acquire();       // peers' barriers expect our pushes
     float dkv[MC];
@@ -525,15 +548,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     for (int mi = 0; mi < MC; ++mi) {
         const int m = rank * MC + mi;
         const float *qm = qs + m * DSUB;
-        const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
         unsigned long long acc2[G];
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) acc2[gg] = 0ull;
         float dk = 0.f;
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            unsigned long long f[4];
-            to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
+        for_row_chunks<DSUB, E4M3>(cbk, mi * K + tid, [&](int c, const unsigned long long (&f)[4]) {
 #pragma unroll
             for (int gg = 0; gg < G; ++gg) {
                 const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qm + gg * D + c * 8);
@@ -546,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 acc2[gg] = a;
             }
             if (APPEND && cl_new) dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
-        }
+        });
         float acc[G];
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) {
@@ -564,19 +583,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the rows, for the bulk copies below
     __syncthreads();                                   // every read of the K slice is done
-    if constexpr (S::SHARED_CB) {
-        if (use_tma) {
-            if (tid == 0) {
-                fence_proxy_async_shared();            // the K slice's reads precede the overwrite
-                mbar_arrive_expect_tx(&bar[1], S::CB_BYTES);
-#pragma unroll
-                for (int mi = 0; mi < MC; ++mi)
-                    tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, rowK + M * K + mi * K, &bar[1]);
-            }
-        } else {
-            copy_codebook_slice<DSUB, S::CB_CHUNKS, E4M3>(cbv, p.codebooks, static_cast<size_t>(rowK + M * K) * DSUB,
-                                                          &bar[1]);
-        }
+    if constexpr (SHARED_V) {
+        if (use_tma && tid == 0) fence_proxy_async_shared();   // the K slice's reads precede the overwrite
+        slice_copy(cbv, rowK + M * K, &bar[1]);
     }
     if constexpr (C > 1) {
         // this CTA's rows to every peer in one bulk copy each; the source is not
@@ -606,10 +615,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         }
     }
     // with its own V buffer, the new value's codes while the peers' rows land
-    if constexpr (APPEND && !S::SHARED_CB) {
+    if constexpr (APPEND && !SHARED_V) {
         if (cl_new) {
             tmo |= !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns);
-            encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+            encode_new_value<DSUB, MC, K, NCH, E4M3>(cbv, xnew + MC * DSUB, keys + MC);
         }
     }
     if constexpr (C > 1) tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
@@ -861,9 +870,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // its codes into its page slot, its page id checked here
     if constexpr (APPEND) {
         if (cl_new) {
-            if constexpr (S::SHARED_CB) {
+            if constexpr (SHARED_V) {
                 if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-                encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+                encode_new_value<DSUB, MC, K, NCH, E4M3>(cbv, xnew + MC * DSUB, keys + MC);
                 __syncthreads();
             }
 #pragma unroll
@@ -973,14 +982,28 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         // same swizzled position, so all loads are at fixed offsets
         const int kx = ks ^ ((mi * S::VP_XOR) & (KSQ - 1));
         const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
+        // raw E4M3 slice: the quad's 4 bytes (the rows kx + i*KSQ share kx's chunk position)
+        const unsigned char *vrow8 = reinterpret_cast<const unsigned char *>(cbv) + (mi * K + kx) * DSUB +
+                                     e8_pos<DSUB>(kx, j4 / 16) * 16 + j4 % 16;
+        static_assert(!E4M3 || DSUB == 16 || KSQ % 8 == 0, "row step keeps the E4M3 chunk position");
         const float *wrow = wtot + (static_cast<size_t>(mi) * K + kx) * G;
         unsigned long long acc[G][2];
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
 #pragma unroll 8
         for (int i = 0; i < KSLQ; ++i) {
-            const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
-            const unsigned long long c01 = h2_to_f2p(cv2.x), c23 = h2_to_f2p(cv2.y);
+            unsigned long long c01, c23;
+            if constexpr (E4M3) {
+                const uint32_t b4 = *reinterpret_cast<const uint32_t *>(vrow8 + i * KSQ * DSUB);
+                const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(b4 & 0xffffu), __NV_E4M3);
+                const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(b4 >> 16), __NV_E4M3);
+                c01 = h2_to_f2p(static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16));
+                c23 = h2_to_f2p(static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16));
+            } else {
+                const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
+                c01 = h2_to_f2p(cv2.x);
+                c23 = h2_to_f2p(cv2.y);
+            }
             float w[G];
             load_vec<G>(w, wrow + i * KSQ * G);
 #pragma unroll
