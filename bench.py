@@ -153,6 +153,15 @@ def measured_traffic(workload: str, mode: str):
     return float(e["dram_bytes"]) if e.get("decode_pq_sha256") == digest else None
 
 
+def step_kernel_name(group: int) -> str:
+    """The decode kernel the library's planner picks for a fused step: the
+    whole-split kernel when at least 4 query heads share a kv head (and no
+    AQPQ_DECODE_KERNEL override asks for the other), else the token-share one."""
+    forced = os.environ.get("AQPQ_DECODE_KERNEL", "")
+    attend = forced == "2" or (forced != "1" and group >= 4)
+    return ("pq_attend_kernel" if attend else "pq_decode_kernel") + " (fused step)"
+
+
 def workload_desc(w) -> str:
     return (f"{w.name}: B{w.batch} Hq{w.num_q_heads} Hkv{w.num_kv_heads} D{w.head_dim} "
             f"M{w.num_subspaces} K{w.num_codewords} L{int(w.seq_lens.max())}"
@@ -439,7 +448,7 @@ def measure_fused_step(args, w, api, torch, T, base, local_rank, dist, world, e4
               f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(w.name, "step"),
-                     "kernel": "pq_decode_kernel (fused step)", "bytes_per_launch": byt["total"],
+                     "kernel": step_kernel_name(Hq // Hkv), "bytes_per_launch": byt["total"],
                      "launch_ms": ms, "peak_kind": peak_kind},
         "code_stream": {"gbs": byt["code_stream"] / (ms / 1e3) / 1e9,
                         "codes_only_gbs": byt["codes"] / (ms / 1e3) / 1e9,
@@ -528,7 +537,7 @@ def run_ours(args, w, rank, world, local_rank):
     # fp16 comparison kernel on the same shape (cache of the same raw vectors)
     fp16 = None if args.no_fp16 else measure_fp16(args, w, api, torch, base, Lmax, units, T)
     sweep = (measure_layer_sweep(args, w, api, torch, base, Lmax, T)
-             if w.layers > 1 and not args.two_call else None)
+             if w.layers > 1 and not args.two_call and not args.no_sweep else None)
     mixed = (measure_mixed(args, w, api, torch, T, base, max(1, w.num_kv_heads // 8), local_rank)
              if not args.two_call else None)
     line = {
@@ -572,7 +581,7 @@ def run_ours(args, w, rank, world, local_rank):
             bx = build_cache(wx, api, torch)
             ex = measure_fused_step(args, wx, api, torch, T, bx, local_rank, dist, world)
             ex.pop("launches_per_step")
-            if wx.layers > 1:
+            if wx.layers > 1 and not args.no_sweep:
                 ex["layer_sweep"] = measure_layer_sweep(args, wx, api, torch, bx, int(wx.seq_lens.max()), T)
             extra[name] = ex
             del bx
@@ -869,6 +878,7 @@ def main():
     ap.add_argument("--two-call", action="store_true",
                     help="time aq_encode_append + aq_decode_attention instead of the fused step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-sweep", action="store_true", help="qwen_gqa: skip the 80-layer sweep")
     ap.add_argument("--min-region-ms", type=float, default=200.0,
                     help="shortest timed region (repeats of the K steps); lower only for profiler runs")
     args = ap.parse_args()
