@@ -1147,8 +1147,8 @@ struct AtCfg {
     static constexpr int OFF_Q = OFF_BINS + BIN_WORDS * 4;
     static constexpr int OFF_PART = OFF_Q + G * D * 4;      // V-product partials [kWarps][NOUT]
     static constexpr int OFF_RED = OFF_PART + kWarps * NOUT * 4;   // red_m, red_l [kWarps][G]
-    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mx, lsum, cfac, s_new [G]
-    static constexpr int OFF_NEW = OFF_STAT + 4 * G * 4;    // xnew [2][MC][DSUB] f32, newc [M]
+    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // mx, lsum, cfac, s_new, qscale [G]
+    static constexpr int OFF_NEW = (OFF_STAT + 5 * G * 4 + 15) / 16 * 16;  // xnew [2][MC][DSUB] f32, newc [M]
     static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + M * 4 + 7) / 8 * 8;  // [2][MC] u64
     static constexpr int OFF_BAR = OFF_KEYS + 2 * MC * 8;   // K, V, codes, q, rows
     static constexpr int OFF_FLAG = OFF_BAR + 5 * 8;
@@ -1160,10 +1160,62 @@ struct AtCfg {
     static_assert(OFF_LUT % 16 == 0 && OFF_Q % 16 == 0 && OFF_PART % 16 == 0, "alignment");
     static_assert((MC * DSUB / 4) <= 32 && 32 % (MC * DSUB / 4) == 0, "V-product quads within a warp");
     static_assert(ROW_FLOATS % 4 == 0, "bulk copies of whole rows");
+    // GQA groups of 4 or more: one thread scores whole tokens for all G heads
+    static constexpr bool PER_TOKEN = G >= 4;
+    static constexpr int NQ = MC * DSUB / 4;                // value product: 4-dim quads per row
+    static constexpr int KSQ = kThreads / NQ;               // its row step
+    static constexpr int VPX = (M == 8 && C == 4) ? 2 : 1;  // its k-slice XOR per owned subspace
+    // the head permutation of a thread's bin rows is the same across each
+    // warp (the lanes differ only in bits of k below the swizzled ones): it
+    // is undone where the warps' partials are summed
+    static constexpr bool XU = PER_TOKEN && NQ >= (32 >> (5 - (G == 8 ? 3 : 2)));
+    static constexpr int TT = MAX_SPLIT / kThreads;         // tokens per thread on that path
+    static_assert(!PER_TOKEN || MAX_SPLIT % kThreads == 0, "whole tokens per thread");
 };
 
 template <int G>
 constexpr int kAtMinBlocks = G == 1 ? 4 : (G == 2 ? 3 : 2);
+
+// Table rows of 8 heads are two 16-byte halves; half h of the row of codeword
+// k sits at h ^ ((k >> 2) & 1), so that the rows a warp reads for 32 tokens
+// with unrelated codes spread over all eight 16-byte bank groups (without it
+// only the even or only the odd groups take a given half).  Rows of 4 heads
+// are one 16-byte group already spread by k.
+template <int G>
+__device__ __forceinline__ int lut_hswz(int k) {
+    return G == 8 ? (k >> 2) & 1 : 0;
+}
+
+// One table row (G = 4 or 8 floats) as packed pairs, in head order.
+template <int G>
+__device__ __forceinline__ void lut_row2(const float *lut, int row, unsigned long long (&v)[G / 2]) {
+    const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(lut + static_cast<size_t>(row) * G);
+    if constexpr (G == 8) {
+        const int h = lut_hswz<G>(row);                 // row = m*K + k with K a multiple of 8
+        const ulonglong2 a = p[h], b = p[h ^ 1];
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+        static_assert(G == 4, "rows of 4 or 8 heads");
+        const ulonglong2 a = p[0];
+        v[0] = a.x; v[1] = a.y;
+    }
+}
+
+// Value bins of a GQA group of 4 or 8 filled one token (all G heads) per
+// thread: head g of codeword k sits at word g ^ s(k) of its row, s(k) taken
+// from the bits of k just above those that pick the bank group of the row,
+// so that 32 tokens with unrelated codes adding head g spread over all 32
+// banks (unswizzled, rows of 8 words would put them on 4 banks).  s(k) uses
+// bits below log2(KSQ) only, the bits that stay fixed along the rows one
+// thread reads in the value product (its rows step by KSQ).
+template <int G, int KSQ>
+__device__ __forceinline__ int bin_wswz(int k) {
+    constexpr int LG = G == 8 ? 3 : (G == 4 ? 2 : 0);
+    constexpr int SH = 5 - LG;                          // bits of k above the row's bank group
+    constexpr int BITS = (KSQ >= 32 ? 5 : (KSQ >= 16 ? 4 : 3)) - SH;
+    constexpr int NB = BITS < LG ? (BITS > 0 ? BITS : 0) : LG;
+    return (k >> SH) & ((1 << NB) - 1);
+}
 
 template <int M, int G, int C, bool APPEND>
 __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(const __grid_constant__ DecodeParams p) {
@@ -1180,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     float *red_m = reinterpret_cast<float *>(smem + S::OFF_RED);
     float *red_l = red_m + kWarps * G;
     float *st_mx = reinterpret_cast<float *>(smem + S::OFF_STAT);
-    float *st_l = st_mx + G, *st_c = st_l + G, *st_sn = st_c + G;
+    float *st_l = st_mx + G, *st_c = st_l + G, *st_sn = st_c + G, *st_qs = st_sn + G;
     float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);      // [2][MC][DSUB]
     int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);        // [M] key codes of the new token
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
@@ -1238,6 +1290,8 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     const bool cl_new = APPEND && new_pos >= ts && new_pos < te;
     const int ntok = (cl_new ? new_pos : te) - ts;   // streamed tokens [ts, ts + ntok)
     const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    // the new token's page (written by thread 0 at the end), loaded early
+    const int pg_new = (APPEND && cl_new && tid == 0) ? __ldg(bt + new_pos / P) : -1;
     if (tid == 0) {
         // the two codebook slices: one 256-row TMA box per owned subspace
         const int row0 = ((set * Hkv + kvh) * 2) * M * K + rank * MC * K;
@@ -1334,7 +1388,14 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
                 const float2 a = f2_unpack(acc2[gg]);
                 acc[gg] = (a.x + a.y) * p.scale_log2;
             }
-            store_vec<G>(lut + (static_cast<size_t>(m) * K + tid) * G, acc);
+            if constexpr (G == 8) {
+                float4 *row = reinterpret_cast<float4 *>(lut + (static_cast<size_t>(m) * K + tid) * G);
+                const int h = lut_hswz<G>(tid);
+                row[h] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                row[h ^ 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            } else {
+                store_vec<G>(lut + (static_cast<size_t>(m) * K + tid) * G, acc);
+            }
             dkv[mi] = dk;
         }
         if constexpr (APPEND) {
@@ -1383,100 +1444,165 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     // are merged over the lanes of head g and then over the warps (PAM article
     // §2.2.3 item 1), so mx and lsum -- the same in every CTA of the cluster --
     // are known before any weight is binned.
-    const int g = tid % G, jslot = tid / G;
-    float s_new = -INFINITY;
-    if constexpr (APPEND) {
-        if (cl_new && tid < G) {
-            s_new = 0.f;
+    if constexpr (S::PER_TOKEN) {
+        // GQA group of 4 or 8: thread tid scores tokens tid, tid + 256, ... for
+        // all G heads, one vector read of each table row per subspace.  The
+        // max of each head over the warp comes from one redux, each thread's
+        // weights are taken relative to it, and the warp's sums per head by a
+        // butterfly that halves the heads a lane carries at each step; the
+        // warps' (max, sum) pairs merge as on the other path (PAM article
+        // §2.2.3 item 1), by the first G threads, between two barriers.
+        constexpr int TT = S::TT, LG = G == 8 ? 3 : 2;
+        float sc[TT][G];
+        float mloc[G], sn[G];
 #pragma unroll
-            for (int m = 0; m < M; ++m) s_new += lut[(m * K + newc[m]) * G + tid];
-        }
-    }
-    const int nslot = (ntok + S::TOK_PER_PASS - 1) / S::TOK_PER_PASS;
-    float sc[TPT];
-    float mloc = s_new;
+        for (int gg = 0; gg < G; ++gg) mloc[gg] = sn[gg] = -INFINITY;
+        if constexpr (APPEND) {
+            if (cl_new && tid == 0) {
+                unsigned long long a2[G / 2];
+                lut_row2<G>(lut, newc[0], a2);
 #pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (i >= nslot) break;
-        const int r = jslot + i * S::TOK_PER_PASS;
-        if (r < ntok) {
-            Codes<M> cw;
-            cw.load_shared(codes + r * 2 * M);
-            float s = 0.f;
+                for (int m = 1; m < M; ++m) {
+                    unsigned long long r2[G / 2];
+                    lut_row2<G>(lut, m * K + newc[m], r2);
 #pragma unroll
-            for (int m = 0; m < M; ++m) s += lut[(m * K + cw.k(m)) * G + g];
-            sc[i] = s;
-            mloc = fmaxf(mloc, s);
-        }
-    }
-    float lloc = (s_new != -INFINITY) ? fast_exp2(s_new - mloc) : 0.f;
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) {
-        if (i >= nslot) break;
-        if (jslot + i * S::TOK_PER_PASS < ntok) {
-            sc[i] = fast_exp2(sc[i] - mloc);
-            lloc += sc[i];
-        }
-    }
-    {
-        float mt = mloc, lt = lloc;
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, mt, off);
-            const float l2 = __shfl_xor_sync(0xffffffffu, lt, off);
-            const float mn = fmaxf(mt, m2);
-            lt = (mt == mn ? lt : lt * fast_exp2(mt - mn)) + (m2 == mn ? l2 : l2 * fast_exp2(m2 - mn));
-            mt = mn;
-        }
-        if (lane < G) {
-            red_m[warp * G + lane] = mt;
-            red_l[warp * G + lane] = lt;
-        }
-    }
-    __syncthreads();
-    float mx = red_m[g];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
-    float lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const float mw = red_m[w * G + g];
-        if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
-    }
-    // value bins in fixed point: round(p * 2^31 / lsum) per token; the bins of
-    // one head sum to 2^31 (plus at most ntok/2 from rounding), and rounding
-    // loses at most a relative ntok/2^32 of the weight
-    const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
-    const float cfac = lsum * (1.0f / 2147483648.0f);
-    if (tid < G) {
-        st_mx[tid] = mx;
-        st_l[tid] = lsum;
-        st_c[tid] = cfac;
-        st_sn[tid] = s_new;
-    }
-    // the new token's value codes of the owned subspaces
-    if constexpr (APPEND) {
-        if (cl_new) {
-            if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-            float dv[MC];
-#pragma unroll
-            for (int mi = 0; mi < MC; ++mi) {
-                const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
-                float d = 0.f;
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    unsigned long long f[4];
-                    to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
-                    d = sqdist8(d, xnew + (MC + mi) * DSUB + c * 8, f);
+                    for (int j = 0; j < G / 2; ++j) a2[j] = f2_add(a2[j], r2[j]);
                 }
-                dv[mi] = d;
-            }
 #pragma unroll
-            for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[MC + mi]);
+                for (int j = 0; j < G / 2; ++j) {
+                    const float2 a = f2_unpack(a2[j]);
+                    sn[2 * j] = mloc[2 * j] = a.x;
+                    sn[2 * j + 1] = mloc[2 * j + 1] = a.y;
+                }
+            }
         }
-    }
-    {
-        const float rq = (mloc == -INFINITY) ? 0.f : (mloc == mx ? qscale : fast_exp2(mloc - mx) * qscale);
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
+            const int r = tid + i * kThreads;
+            if (r < ntok) {
+                Codes<M> cw;
+                cw.load_shared(codes + r * 2 * M);
+                unsigned long long a2[G / 2];
+                lut_row2<G>(lut, cw.k(0), a2);
+#pragma unroll
+                for (int m = 1; m < M; ++m) {
+                    unsigned long long r2[G / 2];
+                    lut_row2<G>(lut, m * K + cw.k(m), r2);
+#pragma unroll
+                    for (int j = 0; j < G / 2; ++j) a2[j] = f2_add(a2[j], r2[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    const float2 a = f2_unpack(a2[j]);
+                    sc[i][2 * j] = a.x;
+                    sc[i][2 * j + 1] = a.y;
+                }
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) mloc[gg] = fmaxf(mloc[gg], sc[i][gg]);
+            } else {
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) sc[i][gg] = -INFINITY;
+            }
+        }
+        float wmax[G], lw[G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            wmax[gg] = warp_max_f32(mloc[gg]);
+            const float ref = wmax[gg] == -INFINITY ? 0.f : wmax[gg];
+            float l = fast_exp2(sn[gg] - ref);              // the new token (thread 0), else 0
+#pragma unroll
+            for (int i = 0; i < TT; ++i) {
+                sc[i][gg] = fast_exp2(sc[i][gg] - ref);     // 0 for an empty slot
+                l += sc[i][gg];
+            }
+            lw[gg] = l;
+        }
+        // warp sums: at offset 16 >> t a lane keeps the upper or the lower half
+        // of the heads it carries and adds its partner's copy of that half;
+        // after LG steps lane carries head (lane >> (5 - LG)) & (G - 1), summed
+        // over the lanes that agree with it in bits 5-LG .. 4
+#pragma unroll
+        for (int t = 0; t < LG; ++t) {
+            const int off = 16 >> t, n = G >> t;
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int j = 0; j < n / 2; ++j) {
+                const float send = up ? lw[j] : lw[j + n / 2];
+                const float keep = up ? lw[j + n / 2] : lw[j];
+                lw[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+#pragma unroll
+        for (int off = 16 >> LG; off > 0; off >>= 1) lw[0] += __shfl_xor_sync(0xffffffffu, lw[0], off);
+        if (lane == 0) store_vec<G>(red_m + warp * G, wmax);
+        if ((lane & ((32 >> LG) - 1)) == 0) red_l[warp * G + ((lane >> (5 - LG)) & (G - 1))] = lw[0];
+        __syncthreads();
+        if (tid < G) {
+            float mx = red_m[tid];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + tid]);
+            float lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = red_m[w * G + tid];
+                if (mw != -INFINITY) lsum += red_l[w * G + tid] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+            }
+            // fixed-point value bins: round(p * 2^31 / lsum) per token and head
+            st_mx[tid] = mx;
+            st_l[tid] = lsum;
+            st_c[tid] = lsum * (1.0f / 2147483648.0f);
+            st_qs[tid] = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        }
+        if (tid == 0) store_vec<G>(st_sn, sn);
+        if constexpr (APPEND) {
+            if (cl_new) {
+                if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+                encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+            }
+        }
+        __syncthreads();                               // statistics of every head
+        float rq[G];
+        {
+            float mxv[G], qsv[G];
+            load_vec<G>(mxv, st_mx);
+            load_vec<G>(qsv, st_qs);
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+                rq[gg] = wmax[gg] == -INFINITY ? 0.f
+                                               : (wmax[gg] == mxv[gg] ? qsv[gg] : fast_exp2(wmax[gg] - mxv[gg]) * qsv[gg]);
+        }
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
+            const int r = tid + i * kThreads;
+            if (r < ntok) {
+                Codes<M> cw;
+                cw.load_shared(codes + r * 2 * M);
+                unsigned qv[G];
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) qv[gg] = __float2uint_rn(sc[i][gg] * rq[gg]);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) {
+                    const int v = cw.vv(rank * MC + mi);
+                    const int sw = bin_wswz<G, S::KSQ>(v);
+                    unsigned *row = bins + (mi * K + v) * G;
+#pragma unroll
+                    for (int gg = 0; gg < G; ++gg) atomicAdd(row + (gg ^ sw), qv[gg]);
+                }
+            }
+        }
+    } else {
+        const int g = tid % G, jslot = tid / G;
+        float s_new = -INFINITY;
+        if constexpr (APPEND) {
+            if (cl_new && tid < G) {
+                s_new = 0.f;
+#pragma unroll
+                for (int m = 0; m < M; ++m) s_new += lut[(m * K + newc[m]) * G + tid];
+            }
+        }
+        const int nslot = (ntok + S::TOK_PER_PASS - 1) / S::TOK_PER_PASS;
+        float sc[TPT];
+        float mloc = s_new;
 #pragma unroll
         for (int i = 0; i < TPT; ++i) {
             if (i >= nslot) break;
@@ -1484,9 +1610,92 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
             if (r < ntok) {
                 Codes<M> cw;
                 cw.load_shared(codes + r * 2 * M);
-                const unsigned qv = __float2uint_rn(sc[i] * rq);
+                float s = 0.f;
 #pragma unroll
-                for (int mi = 0; mi < MC; ++mi) atomicAdd(&bins[(mi * K + cw.vv(rank * MC + mi)) * G + g], qv);
+                for (int m = 0; m < M; ++m) s += lut[(m * K + cw.k(m)) * G + g];
+                sc[i] = s;
+                mloc = fmaxf(mloc, s);
+            }
+        }
+        float lloc = (s_new != -INFINITY) ? fast_exp2(s_new - mloc) : 0.f;
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            if (i >= nslot) break;
+            if (jslot + i * S::TOK_PER_PASS < ntok) {
+                sc[i] = fast_exp2(sc[i] - mloc);
+                lloc += sc[i];
+            }
+        }
+        {
+            float mt = mloc, lt = lloc;
+#pragma unroll
+            for (int off = G; off < 32; off <<= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, mt, off);
+                const float l2 = __shfl_xor_sync(0xffffffffu, lt, off);
+                const float mn = fmaxf(mt, m2);
+                lt = (mt == mn ? lt : lt * fast_exp2(mt - mn)) + (m2 == mn ? l2 : l2 * fast_exp2(m2 - mn));
+                mt = mn;
+            }
+            if (lane < G) {
+                red_m[warp * G + lane] = mt;
+                red_l[warp * G + lane] = lt;
+            }
+        }
+        __syncthreads();
+        float mx = red_m[g];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = red_m[w * G + g];
+            if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+        }
+        // value bins in fixed point: round(p * 2^31 / lsum) per token; the bins of
+        // one head sum to 2^31 (plus at most ntok/2 from rounding), and rounding
+        // loses at most a relative ntok/2^32 of the weight
+        const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        const float cfac = lsum * (1.0f / 2147483648.0f);
+        if (tid < G) {
+            st_mx[tid] = mx;
+            st_l[tid] = lsum;
+            st_c[tid] = cfac;
+            st_sn[tid] = s_new;
+        }
+        // the new token's value codes of the owned subspaces
+        if constexpr (APPEND) {
+            if (cl_new) {
+                if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+                float dv[MC];
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) {
+                    const uint4 *rowv = reinterpret_cast<const uint4 *>(cbv) + (mi * K + tid) * NCH;
+                    float d = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        unsigned long long f[4];
+                        to_f2p4(rowv[chunk_pos<DSUB>(tid, c)], f);
+                        d = sqdist8(d, xnew + (MC + mi) * DSUB + c * 8, f);
+                    }
+                    dv[mi] = d;
+                }
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dv[mi], &keys[MC + mi]);
+            }
+        }
+        {
+            const float rq = (mloc == -INFINITY) ? 0.f : (mloc == mx ? qscale : fast_exp2(mloc - mx) * qscale);
+#pragma unroll
+            for (int i = 0; i < TPT; ++i) {
+                if (i >= nslot) break;
+                const int r = jslot + i * S::TOK_PER_PASS;
+                if (r < ntok) {
+                    Codes<M> cw;
+                    cw.load_shared(codes + r * 2 * M);
+                    const unsigned qv = __float2uint_rn(sc[i] * rq);
+#pragma unroll
+                    for (int mi = 0; mi < MC; ++mi) atomicAdd(&bins[(mi * K + cw.vv(rank * MC + mi)) * G + g], qv);
+                }
             }
         }
     }
@@ -1498,7 +1707,6 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     if constexpr (APPEND) {
         if (cl_new && tid == 0) {
             // this CTA's codes of the new token into its page slot
-            const int pg_new = __ldg(bt + new_pos / P);
             if (sflag[0] & AQ_DEV_TIMEOUT) {
                 // no codes from data that may not have landed
             } else if (pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages) {
@@ -1527,7 +1735,7 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
         const int qd = tid % NQ, ks = tid / NQ;
         const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
         const int cj = j4 / 8, hj = j4 % 8;
-        constexpr int VPX = (M == 8 && C == 4) ? 2 : 1;
+        constexpr int VPX = S::VPX;
         const int kx = ks ^ ((mi * VPX) & (KSQ - 1));
         const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
         const unsigned *wrow = bins + (static_cast<size_t>(mi) * K + kx) * G;
@@ -1554,6 +1762,26 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
             const float2 a01 = f2_unpack(acc[gg][0]), a23 = f2_unpack(acc[gg][1]);
             accf[gg][0] = a01.x; accf[gg][1] = a01.y; accf[gg][2] = a23.x; accf[gg][3] = a23.y;
         }
+        if constexpr (S::PER_TOKEN && !S::XU) {
+            // this thread's rows agree in the bits of k below log2(KSQ), so one
+            // permutation for all of them: word w of a row holds head w ^ x
+            static_assert(KSQ == S::KSQ, "row step of the value product");
+            const int x = bin_wswz<G, KSQ>(kx);
+#pragma unroll
+            for (int bv = 1; bv < G; bv <<= 1) {
+                const bool sw = (x & bv) != 0;
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    if (gg & bv) continue;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = accf[gg][e], c = accf[gg | bv][e];
+                        accf[gg][e] = sw ? c : a;
+                        accf[gg | bv][e] = sw ? a : c;
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int off = NQ; off < 32; off <<= 1) {
 #pragma unroll
@@ -1573,10 +1801,18 @@ __global__ void __launch_bounds__(kThreads, kAtMinBlocks<G>) pq_attend_kernel(co
     }
     __syncthreads();
     for (int i = tid; i < S::NOUT; i += kThreads) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) o += part[static_cast<size_t>(w) * S::NOUT + i];
         const int gg = i % G, dl = i / G;                 // dl in [0, MC*DSUB)
+        float o = 0.f;
+        if constexpr (S::XU) {
+            // warp w's partials hold head gg at word gg ^ x_w
+            const int cx = ((dl / DSUB) * S::VPX) & (S::KSQ - 1);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                o += part[static_cast<size_t>(w) * S::NOUT + dl * G + (gg ^ bin_wswz<G, S::KSQ>((w * 32 / S::NQ) ^ cx))];
+        } else {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) o += part[static_cast<size_t>(w) * S::NOUT + i];
+        }
         o *= st_c[gg];
         if constexpr (APPEND) {
             if (cl_new) {
@@ -1641,13 +1877,652 @@ cudaError_t launch_attend(const DecodeParams &p, const Plan &plan, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// ============================================================================
+// pq_headsplit_kernel: the whole-split design with the query heads of the
+// group, not the table work, divided over the cluster (GQA groups of G >= C,
+// G >= 4; qwen-shaped B8 Hq64 Hkv8: C = 4, two query heads per CTA).
+//
+// One cluster of C CTAs per (request, kv head, split); CTA `rank` owns
+// subspaces [rank*MC, (rank+1)*MC) of both codebooks and query heads
+// [rank*H, (rank+1)*H), H = G/C:
+//  1. table rows q_g[m] . C^K_m[k] for its own subspaces and all G heads (the
+//     rows need every head's query, the codebook slice is this CTA's); each
+//     peer receives the rows of its own heads only (AQPIM blog §4.1);
+//  2. every token of the split scored for its H heads, so the (max, sum) of
+//     each of them is complete in this CTA (PAM article §2.2.3 item 1);
+//  3. fixed-point value bins of its heads for all M subspaces; each peer
+//     receives the bins of the subspaces it owns and the heads' statistics
+//     (PAM article §2.2.3 item 3, inside one cluster);
+//  4. the value product W . C^V for its own subspaces and all G heads, as in
+//     the other kernels; normalise and store, or store split partials.
+// Against pq_attend_kernel (every CTA scores every token for all G heads),
+// the table reads of the scores and the rows sent fall by C, at the price of
+// a second exchange (bins) of MC*256*H words per peer.
+// ============================================================================
+template <int M, int G, int C>
+struct HsCfg {
+    static constexpr int D = kHeadDim, K = kCodewords, P = kPage;
+    static constexpr int DSUB = D / M;
+    static constexpr int NCH = DSUB / 8;
+    static constexpr int MC = M / C;
+    static constexpr int H = G / C;                         // query heads scored per CTA
+    static constexpr int SLICE_BYTES = MC * K * DSUB * 2;
+    static constexpr int T_FLOATS = M * K * H;              // table of this CTA's heads [M][K][H]
+    static constexpr int SB_FLOATS = MC * K * H;            // rows for one peer [MC][K][H]
+    static constexpr int B_WORDS = M * K * H;               // bins of this CTA's heads [M][K][H]
+    static constexpr int RB_WORDS = MC * K * H;             // bins of one source [MC][K][H]
+    static constexpr int STX = 4 * H;                       // mx, lsum, cfac, s_new of one rank's heads
+    static constexpr int TT = 4;                            // tokens per thread
+    static constexpr int CODE_CAP = 32768;
+    static constexpr int MAX_SPLIT = (TT * kThreads < CODE_CAP / (2 * M) ? TT * kThreads : CODE_CAP / (2 * M)) / P * P;
+    static constexpr int NOUT = MC * DSUB * G;
+    static constexpr int NQ = MC * DSUB / 4, KSQ = kThreads / NQ, KSLQ = K / KSQ;
+    static constexpr int VPX = (M == 8 && C == 4) ? 2 : 1;
+    // layout from the 1024-aligned base.  The peers' bins land in the key
+    // slice (read for the last time before this CTA sends its rows, long
+    // before any peer can have bins to send); the value-product partials use
+    // the table (read for the last time by the scores).
+    static constexpr int OFF_CBK = 0;
+    static constexpr int OFF_RB = 0;                        // [C][MC][K][H] u32, slot rank unused
+    static constexpr int OFF_CBV = SLICE_BYTES;
+    static constexpr int OFF_T = 2 * SLICE_BYTES;
+    static constexpr int OFF_PART = OFF_T;                  // [kWarps][NOUT]
+    static constexpr int T_BYTES = (T_FLOATS > kWarps * NOUT ? T_FLOATS : kWarps * NOUT) * 4;
+    static constexpr int OFF_SB = OFF_T + T_BYTES;          // [C][MC][K][H], slot rank unused
+    static constexpr int OFF_B = OFF_SB + C * SB_FLOATS * 4;
+    static constexpr int OFF_STX = OFF_B + B_WORDS * 4;     // [C][STX]
+    static constexpr int OFF_Q = (OFF_STX + C * STX * 4 + 15) / 16 * 16;
+    static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_m, red_l [kWarps][H]
+    static constexpr int OFF_QS = OFF_RED + 2 * kWarps * H * 4;  // qscale [H]
+    static constexpr int OFF_NEW = (OFF_QS + H * 4 + 15) / 16 * 16;  // xnew [2][MC][DSUB], newc [M]
+    static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + M * 4 + 7) / 8 * 8;
+    static constexpr int OFF_BAR = OFF_KEYS + 2 * MC * 8;   // K, V, codes, q, rows, bins
+    static constexpr int OFF_FLAG = OFF_BAR + 6 * 8;
+    static constexpr int OFF_PBAD = OFF_FLAG + 16;
+    static constexpr int OFF_CODES = (OFF_PBAD + 4 * C + 15) / 16 * 16;
+    static size_t smem(int split_len) { return 1024 + OFF_CODES + static_cast<size_t>(split_len) * 2 * M; }
+    static_assert(G >= C && G % C == 0 && G >= 4, "the group covers the cluster");
+    static_assert(K == kThreads, "one thread per codeword in the table build");
+    static_assert(SLICE_BYTES % 1024 == 0, "slices keep the swizzle alignment");
+    static_assert(C * RB_WORDS * 4 <= SLICE_BYTES, "the peers' bins fit in the key slice");
+    static_assert(OFF_T % 16 == 0 && OFF_SB % 16 == 0 && OFF_B % 16 == 0 && OFF_Q % 16 == 0, "alignment");
+    static_assert(NQ <= 32 && 32 % NQ == 0, "V-product quads within a warp");
+    static_assert(SB_FLOATS % 4 == 0 && RB_WORDS % 4 == 0, "bulk copies of 16-byte multiples");
+    static_assert(MAX_SPLIT % kThreads == 0, "whole tokens per thread");
+};
+
+template <int H>
+constexpr int kHsMinBlocks = 2;
+
+// bins row of codeword k for the H heads of one CTA: head h at word h ^ s(k)
+// (H = 2: s from bit 4 of k, H = 4: bits 3-4), so that the 32 tokens of an
+// atomic spread over all banks; s uses bits of k below 5 only, fixed along the
+// rows of one thread in the value product when its row step is 32 or more.
+template <int H, int KSQ>
+__device__ __forceinline__ int hs_bswz(int k) {
+    if constexpr (H == 2 && KSQ >= 32) return (k >> 4) & 1;
+    else if constexpr (H == 4 && KSQ >= 32) return (k >> 3) & 3;
+    else return 0;
+}
+
+template <int M, int G, int C, bool APPEND>
+__global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_kernel(const __grid_constant__ DecodeParams p) {
+    using S = HsCfg<M, G, C>;
+    constexpr int D = S::D, K = S::K, P = S::P, DSUB = S::DSUB, MC = S::MC, NCH = S::NCH, H = S::H, TT = S::TT;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __half *cbk = reinterpret_cast<__half *>(smem + S::OFF_CBK);
+    __half *cbv = reinterpret_cast<__half *>(smem + S::OFF_CBV);
+    unsigned *rb = reinterpret_cast<unsigned *>(smem + S::OFF_RB);
+    float *tab = reinterpret_cast<float *>(smem + S::OFF_T);
+    float *part = reinterpret_cast<float *>(smem + S::OFF_PART);
+    float *sb = reinterpret_cast<float *>(smem + S::OFF_SB);
+    unsigned *bins = reinterpret_cast<unsigned *>(smem + S::OFF_B);
+    float *stx = reinterpret_cast<float *>(smem + S::OFF_STX);
+    float *qs = reinterpret_cast<float *>(smem + S::OFF_Q);
+    float *red_m = reinterpret_cast<float *>(smem + S::OFF_RED);
+    float *red_l = red_m + kWarps * H;
+    float *qsc = reinterpret_cast<float *>(smem + S::OFF_QS);
+    float *xnew = reinterpret_cast<float *>(smem + S::OFF_NEW);      // [2][MC][DSUB]
+    int *newc = reinterpret_cast<int *>(xnew + 2 * MC * DSUB);        // [M]
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem + S::OFF_KEYS);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);  // K, V, codes, q, rows, bins
+    int *sflag = reinterpret_cast<int *>(smem + S::OFF_FLAG);
+    int *pbad = reinterpret_cast<int *>(smem + S::OFF_PBAD);
+    const unsigned char *codes = smem + S::OFF_CODES;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int split = blockIdx.x / C;
+    const int kvh = static_cast<int>(blockIdx.y >> p.head_split_log2), b = blockIdx.z;
+    const int hq0 = p.q_head_base + static_cast<int>(blockIdx.y) * G;
+    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+    const int S_ = p.num_splits;
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(&bar[i], i == 2 ? kThreads : 1);
+        fence_mbar_init();
+        sflag[0] = 0;
+    }
+    __syncthreads();
+    // ---- reads allowed before the preceding kernel completes ----------------
+    const int set = __ldg(p.req_set + b);
+    const int L_raw = __ldg(p.seq_lens + b);
+    const bool set_ok = set >= 0 && static_cast<int64_t>(set) < p.num_sets;
+    int bad0 = 0;
+    if (L_raw < 0 || L_raw > p.max_pages * P || L_raw > p.max_seq_len) bad0 |= AQ_DEV_BAD_LENGTH;
+    if (!set_ok) bad0 |= AQ_DEV_BAD_SET;
+    const int ts = split * p.split_len;
+    const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
+    if (bad0 || ts >= te) {
+        grid_dependency_wait();
+        if (rank == 0) {
+            if (bad0 && tid == 0) flag_status(p.status, bad0);
+            const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
+            for (int i = tid; i < G * D; i += kThreads) {
+                const int gg = i / D, d = i % D;
+                const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
+                if (S_ == 1) p.out[bh * D + d] = v;
+                else if (d == 0) {
+                    p.part_ml[(bh * S_ + split) * 2 + 0] = bad0 ? v : -INFINITY;
+                    p.part_ml[(bh * S_ + split) * 2 + 1] = bad0 ? v : 0.0f;
+                }
+            }
+        }
+        return;
+    }
+    const int new_pos = APPEND ? L_raw - 1 : -1;
+    const bool cl_new = APPEND && new_pos >= ts && new_pos < te;
+    const int ntok = (cl_new ? new_pos : te) - ts;
+    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    const int pg_new = (APPEND && cl_new && tid == 0) ? __ldg(bt + new_pos / P) : -1;
+    if (tid == 0) {
+        const int row0 = ((set * Hkv + kvh) * 2) * M * K + rank * MC * K;
+        mbar_arrive_expect_tx(&bar[0], S::SLICE_BYTES);
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, row0 + mi * K, &bar[0]);
+        mbar_arrive_expect_tx(&bar[1], S::SLICE_BYTES);
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, row0 + M * K + mi * K, &bar[1]);
+        // from each peer: its rows of this CTA's heads, its new-key codes and
+        // flag; later its bins of this CTA's subspaces and its heads' statistics
+        mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::SB_FLOATS + (cl_new ? MC : 0) + 1) * 4);
+        mbar_arrive_expect_tx(&bar[5], (C - 1) * (S::RB_WORDS + S::STX) * 4);
+    }
+    {
+        // the split's code pages, whole page lines, into shared memory in token
+        // order (as in pq_attend_kernel)
+        constexpr int PAGE_BYTES = P * 2 * M, CPP = PAGE_BYTES / 16;
+        const int npg = (ntok + P - 1) / P, pg0 = ts / P;
+        const size_t page_stride = static_cast<size_t>(Hkv) * PAGE_BYTES;
+        const unsigned char *src0 = p.code_pages + static_cast<size_t>(kvh) * PAGE_BYTES;
+        const uint32_t dst0 = smem_u32(codes);
+        bool bad = false;
+        for (int q = tid; q < npg * CPP; q += kThreads) {
+            const int j = q / CPP, c = q % CPP;
+            const int pg = __ldg(bt + pg0 + j);
+            if (pg >= 0 && static_cast<int64_t>(pg) < p.num_pages)
+                cp_async_16(dst0 + static_cast<uint32_t>(q) * 16u, src0 + static_cast<size_t>(pg) * page_stride + c * 16);
+            else
+                bad = true;
+        }
+        cp_async_mbar_arrive(&bar[2]);
+        if (bad) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+    }
+    // ---- the query and the new token come from the preceding kernel ----------
+    grid_dependency_wait();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[3], G * D * 4);
+        bulk_g2s(qs, p.q + (static_cast<size_t>(b) * Hq + hq0) * D, G * D * 4, &bar[3]);
+    }
+    if constexpr (APPEND) {
+        if (cl_new && tid < 2 * MC * DSUB) {
+            const int w = tid / (MC * DSUB), r = tid % (MC * DSUB);
+            xnew[tid] = __half2float(__ldg(reinterpret_cast<const __half *>(p.kv_new) +
+                                           ((static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + kvh) * 2 + w) * D +
+                                           rank * MC * DSUB + r));
+        }
+    }
+    for (int i = tid; i < S::B_WORDS / 4; i += kThreads)
+        reinterpret_cast<uint4 *>(bins)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 2 * MC) keys[tid] = ~0ull;
+    grid_launch_dependents();
+    __syncthreads();
+    cluster_arrive_relaxed();                          // this CTA's barriers are ready for pushes
+
+    // ---- table rows of the owned subspaces for all G heads --------------------
+    bool tmo = !mbar_wait_limit(&bar[0], 0, p.wait_limit_ns);
+    tmo |= !mbar_wait_limit(&bar[3], 0, p.wait_limit_ns);
+    if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    cluster_wait_acquire();                            // peers' barriers expect our pushes
+    {
+        float dkv[MC];
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) {
+            const int m = rank * MC + mi;
+            const float *qm = qs + m * DSUB;
+            const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
+            unsigned long long acc2[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) acc2[gg] = 0ull;
+            float dk = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                unsigned long long f[4];
+                to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) {
+                    const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qm + gg * D + c * 8);
+                    const ulonglong2 qa = qv[0], qb = qv[1];
+                    unsigned long long a = acc2[gg];
+                    a = f2_fma(qa.x, f[0], a);
+                    a = f2_fma(qa.y, f[1], a);
+                    a = f2_fma(qb.x, f[2], a);
+                    a = f2_fma(qb.y, f[3], a);
+                    acc2[gg] = a;
+                }
+                if (APPEND && cl_new) dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
+            }
+            // heads [r*H, (r+1)*H) go to rank r: this CTA's straight into its
+            // table, a peer's into that peer's staging rows
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                float v[H];
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 a = f2_unpack(acc2[r * H + h]);
+                    v[h] = (a.x + a.y) * p.scale_log2;
+                }
+                float *dst = r == rank ? tab + (static_cast<size_t>(m) * K + tid) * H
+                                       : sb + (static_cast<size_t>(r * MC + mi) * K + tid) * H;
+                store_vec<H>(dst, v);
+            }
+            dkv[mi] = dk;
+        }
+        if constexpr (APPEND) {
+            if (cl_new) {
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dkv[mi], &keys[mi]);
+            }
+        }
+    }
+    fence_proxy_async_shared();                        // the staged rows, for the bulk copies below
+    __syncthreads();
+    if (tid < C - 1) {
+        // peer pr's rows (its heads, this CTA's subspaces) into its table
+        const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) % C;
+        const uint32_t rbar = mapa_u32(smem_u32(&bar[4]), pr);
+        bulk_s2cluster(mapa_u32(smem_u32(tab + static_cast<size_t>(rank) * MC * K * H), pr),
+                       smem_u32(sb + static_cast<size_t>(pr) * S::SB_FLOATS), S::SB_FLOATS * 4, rbar);
+        st_async_f32(mapa_u32(smem_u32(&pbad[rank]), pr), __int_as_float(sflag[0]), rbar);
+    }
+    if constexpr (APPEND) {
+        if (cl_new && tid < MC) {
+            const int m = rank * MC + tid;
+            const int code = static_cast<int>(keys[tid] & 0xffu);
+            newc[m] = code;
+            const uint32_t la = smem_u32(&newc[m]), lb = smem_u32(&bar[4]);
+#pragma unroll
+            for (int r = 1; r < C; ++r) {
+                const uint32_t pr = static_cast<uint32_t>(rank + r) % C;
+                st_async_f32(mapa_u32(la, pr), __int_as_float(code), mapa_u32(lb, pr));
+            }
+        }
+    }
+    tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
+    tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
+    if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    __syncthreads();                                   // the table of this CTA's heads, the new key's codes
+
+    // ---- scores of this CTA's H heads over every token of the split ----------
+    constexpr int LH = H == 8 ? 3 : (H == 4 ? 2 : (H == 2 ? 1 : 0));
+    float sc[TT][H];
+    float mloc[H], sn[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) mloc[h] = sn[h] = -INFINITY;
+    if constexpr (APPEND) {
+        if (cl_new && tid == 0) {
+            float a[H];
+            load_vec<H>(a, tab + static_cast<size_t>(newc[0]) * H);
+#pragma unroll
+            for (int m = 1; m < M; ++m) {
+                float r[H];
+                load_vec<H>(r, tab + (static_cast<size_t>(m) * K + newc[m]) * H);
+#pragma unroll
+                for (int h = 0; h < H; ++h) a[h] += r[h];
+            }
+#pragma unroll
+            for (int h = 0; h < H; ++h) sn[h] = mloc[h] = a[h];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+        const int r = tid + i * kThreads;
+        if (r < ntok) {
+            Codes<M> cw;
+            cw.load_shared(codes + r * 2 * M);
+            float a[H];
+            load_vec<H>(a, tab + static_cast<size_t>(cw.k(0)) * H);
+#pragma unroll
+            for (int m = 1; m < M; ++m) {
+                float t[H];
+                load_vec<H>(t, tab + (static_cast<size_t>(m) * K + cw.k(m)) * H);
+#pragma unroll
+                for (int h = 0; h < H; ++h) a[h] += t[h];
+            }
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                sc[i][h] = a[h];
+                mloc[h] = fmaxf(mloc[h], a[h]);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < H; ++h) sc[i][h] = -INFINITY;
+        }
+    }
+    // warp max of each head (one redux), weights relative to it, warp sums
+    // by a butterfly that halves the heads a lane carries at each step
+    float wmax[H], lw[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        wmax[h] = warp_max_f32(mloc[h]);
+        const float ref = wmax[h] == -INFINITY ? 0.f : wmax[h];
+        float l = fast_exp2(sn[h] - ref);                   // the new token (thread 0), else 0
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
+            sc[i][h] = fast_exp2(sc[i][h] - ref);
+            l += sc[i][h];
+        }
+        lw[h] = l;
+    }
+#pragma unroll
+    for (int t = 0; t < LH; ++t) {
+        const int off = 16 >> t, n = H >> t;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float send = up ? lw[j] : lw[j + n / 2];
+            const float keep = up ? lw[j + n / 2] : lw[j];
+            lw[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+#pragma unroll
+    for (int off = 16 >> LH; off > 0; off >>= 1) lw[0] += __shfl_xor_sync(0xffffffffu, lw[0], off);
+    if (lane == 0) store_vec<H>(red_m + warp * H, wmax);
+    if ((lane & ((32 >> LH) - 1)) == 0) red_l[warp * H + ((lane >> (5 - LH)) & (H - 1))] = lw[0];
+    float *st_own = stx + rank * S::STX;               // mx, lsum, cfac, s_new [H] of this CTA's heads
+    if (tid == 0) store_vec<H>(st_own + 3 * H, sn);
+    __syncthreads();
+    if (tid < H) {
+        float mx = red_m[tid];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * H + tid]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float mw = red_m[w * H + tid];
+            if (mw != -INFINITY) lsum += red_l[w * H + tid] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+        }
+        // fixed-point value bins: round(p * 2^31 / lsum) per token and head
+        const float cf = lsum * (1.0f / 2147483648.0f);
+        st_own[tid] = mx;
+        st_own[H + tid] = lsum;
+        st_own[2 * H + tid] = cf;
+        qsc[tid] = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        const float snv = st_own[3 * H + tid];
+        const uint32_t lbar = smem_u32(&bar[5]);
+#pragma unroll
+        for (int r = 1; r < C; ++r) {
+            const uint32_t pr = static_cast<uint32_t>(rank + r) % C, pb = mapa_u32(lbar, pr);
+            st_async_f32(mapa_u32(smem_u32(st_own + tid), pr), mx, pb);
+            st_async_f32(mapa_u32(smem_u32(st_own + H + tid), pr), lsum, pb);
+            st_async_f32(mapa_u32(smem_u32(st_own + 2 * H + tid), pr), cf, pb);
+            st_async_f32(mapa_u32(smem_u32(st_own + 3 * H + tid), pr), snv, pb);
+        }
+    }
+    // the new token's value codes of the owned subspaces
+    if constexpr (APPEND) {
+        if (cl_new) {
+            if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+            encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+        }
+    }
+    __syncthreads();                                   // statistics of this CTA's heads
+    {
+        float rq[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float mx = st_own[h], qv = qsc[h];
+            rq[h] = wmax[h] == -INFINITY ? 0.f : (wmax[h] == mx ? qv : fast_exp2(wmax[h] - mx) * qv);
+        }
+#pragma unroll
+        for (int i = 0; i < TT; ++i) {
+            const int r = tid + i * kThreads;
+            if (r < ntok) {
+                Codes<M> cw;
+                cw.load_shared(codes + r * 2 * M);
+                unsigned qv[H];
+#pragma unroll
+                for (int h = 0; h < H; ++h) qv[h] = __float2uint_rn(sc[i][h] * rq[h]);
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const int v = cw.vv(m);
+                    unsigned *row = bins + (m * K + v) * H;
+                    const int sw = hs_bswz<H, S::KSQ>(v);
+#pragma unroll
+                    for (int h = 0; h < H; ++h) atomicAdd(row + (h ^ sw), qv[h]);
+                }
+            }
+        }
+    }
+    fence_proxy_async_shared();                        // the bins, for the bulk copies below
+    __syncthreads();
+    if (tid < C - 1) {
+        // peer pr's subspaces of this CTA's bins into its slot `rank`
+        const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) % C;
+        bulk_s2cluster(mapa_u32(smem_u32(rb + static_cast<size_t>(rank) * S::RB_WORDS), pr),
+                       smem_u32(bins + static_cast<size_t>(pr) * MC * K * H), S::RB_WORDS * 4,
+                       mapa_u32(smem_u32(&bar[5]), pr));
+    }
+    int bad_all = sflag[0];
+#pragma unroll
+    for (int r = 0; r < C; ++r)
+        if (r != rank) bad_all |= pbad[r];
+    if (!mbar_wait_limit(&bar[5], 0, p.wait_limit_ns) || !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) {
+        atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+        bad_all |= AQ_DEV_TIMEOUT;
+    }
+    cluster_arrive_relaxed();                          // everything sent to this CTA has landed
+    if constexpr (APPEND) {
+        if (cl_new && tid == 0) {
+            // this CTA's codes of the new token into its page slot
+            if (sflag[0] & AQ_DEV_TIMEOUT) {
+                // no codes from data that may not have landed
+            } else if (pg_new >= 0 && static_cast<int64_t>(pg_new) < p.num_pages) {
+                uint8_t *dst = p.code_pages_w + ((static_cast<size_t>(pg_new) * Hkv + kvh) * P + new_pos % P) * (2 * M);
+#pragma unroll
+                for (int mi = 0; mi < MC; ++mi) {
+                    dst[rank * MC + mi] = static_cast<uint8_t>(newc[rank * MC + mi]);
+                    dst[M + rank * MC + mi] = static_cast<uint8_t>(keys[MC + mi] & 0xffu);
+                }
+            } else {
+                atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+                bad_all |= AQ_DEV_BAD_PAGE;
+            }
+        }
+    }
+
+    // ---- value codebook product for the owned dims, all G heads ---------------
+    {
+        constexpr int NQ = S::NQ, KSQ = S::KSQ, KSLQ = S::KSLQ;
+        constexpr int ROWS128 = 128 / (DSUB * 2);
+        static_assert(KSQ % (ROWS128 * NCH) == 0, "row step keeps the swizzle position");
+        const int qd = tid % NQ, ks = tid / NQ;
+        const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
+        const int cj = j4 / 8, hj = j4 % 8;
+        const int kx = ks ^ ((mi * S::VPX) & (KSQ - 1));
+        const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
+        // bins of head r*H + h: this CTA's own (r == rank) or those rank r sent
+        const unsigned *wsrc[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r)
+            wsrc[r] = (r == rank ? bins + static_cast<size_t>(rank * MC + mi) * K * H
+                                 : rb + static_cast<size_t>(r * MC + mi) * K * H) + kx * H;
+        unsigned long long acc[G][2];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
+#pragma unroll 4
+        for (int i = 0; i < KSLQ; ++i) {
+            const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
+            const unsigned long long c01 = h2_to_f2p(cv2.x), c23 = h2_to_f2p(cv2.y);
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                unsigned wu[H];
+                load_vec_u<H>(wu, wsrc[r] + i * KSQ * H);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float wf = static_cast<float>(wu[h]);
+                    const unsigned long long ww = f2_pack(wf, wf);
+                    acc[r * H + h][0] = f2_fma(ww, c01, acc[r * H + h][0]);
+                    acc[r * H + h][1] = f2_fma(ww, c23, acc[r * H + h][1]);
+                }
+            }
+        }
+        float accf[G][4];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const float2 a01 = f2_unpack(acc[gg][0]), a23 = f2_unpack(acc[gg][1]);
+            accf[gg][0] = a01.x; accf[gg][1] = a01.y; accf[gg][2] = a23.x; accf[gg][3] = a23.y;
+        }
+        // word h of a row holds head h ^ x of its source (x fixed along this
+        // thread's rows)
+        const int x = hs_bswz<H, KSQ>(kx);
+#pragma unroll
+        for (int bv = 1; bv < H; bv <<= 1) {
+            const bool swp = (x & bv) != 0;
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                if (gg & bv) continue;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = accf[gg][e], c = accf[gg | bv][e];
+                    accf[gg][e] = swp ? c : a;
+                    accf[gg | bv][e] = swp ? a : c;
+                }
+            }
+        }
+#pragma unroll
+        for (int off = NQ; off < 32; off <<= 1) {
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accf[gg][e] += __shfl_xor_sync(0xffffffffu, accf[gg][e], off);
+        }
+        if (lane < NQ) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float v[G];
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) v[gg] = accf[gg][e];
+                store_vec<G>(part + (static_cast<size_t>(warp) * MC * DSUB + mi * DSUB + j4 + e) * G, v);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < S::NOUT; i += kThreads) {
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) o += part[static_cast<size_t>(w) * S::NOUT + i];
+        const int gg = i % G, dl = i / G;                 // dl in [0, MC*DSUB)
+        const float *sth = stx + (gg / H) * S::STX;       // statistics of head gg, from its CTA
+        const int hh = gg % H;
+        const float mxg = sth[hh], lg = sth[H + hh];
+        o *= sth[2 * H + hh];
+        if constexpr (APPEND) {
+            if (cl_new) {
+                // the new token: its weight times its value codeword
+                const int mi = dl / DSUB, j = dl % DSUB;
+                const int vc = static_cast<int>(keys[MC + mi] & 0xffu);
+                const float wn = fast_exp2(sth[3 * H + hh] - mxg);
+                o += wn * __half2float(cbv[((mi * K + vc) * NCH + chunk_pos<DSUB>(vc, j / 8)) * 8 + j % 8]);
+            }
+        }
+        const int d = rank * MC * DSUB + dl;
+        const size_t bh = static_cast<size_t>(b) * Hq + hq0 + gg;
+        const float nan = __int_as_float(0x7fc00000);
+        if (S_ == 1) {
+            p.out[bh * D + d] = bad_all ? nan : (lg > 0.f ? __fdividef(o, lg) : 0.f);
+        } else {
+            p.part_o[(bh * S_ + split) * D + d] = o;
+            if (rank == 0 && dl == 0) {
+                p.part_ml[(bh * S_ + split) * 2 + 0] = bad_all ? nan : mxg;
+                p.part_ml[(bh * S_ + split) * 2 + 1] = bad_all ? nan : lg;
+            }
+        }
+    }
+    if (tid == 0 && sflag[0]) flag_status(p.status, sflag[0]);
+    // A wait that ran out may leave a copy still landing: wait again (bounded)
+    // before the shared memory is released.
+    if (sflag[0] & AQ_DEV_TIMEOUT) {
+        cp_async_wait_all();
+        for (int i = 0; i < 6; ++i) mbar_wait_bounded(&bar[i], 0);
+    }
+    cluster_wait_acquire();                            // no CTA leaves while a peer may still read its rows or bins
+}
+
+template <int M, int G, int C, bool APPEND>
+cudaError_t launch_headsplit(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
+    using S = HsCfg<M, G, C>;
+    auto kern = pq_headsplit_kernel<M, G, C, APPEND>;
+    if (plan.split_len > S::MAX_SPLIT || plan.split_len % kPage) return cudaErrorInvalidValue;
+    static SmemAttr attr_state;
+    const size_t need = S::smem(plan.split_len);
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), S::smem(S::MAX_SPLIT));
+        e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(C * plan.num_splits),
+                       static_cast<unsigned>(p.num_kv_heads) << p.head_split_log2,
+                       static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = need;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.overlap ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Groups that cover the cluster (G >= C, G >= 4) split their query heads over
+// it (pq_headsplit_kernel); smaller groups score all heads in every CTA.
+template <int G, int C>
+constexpr bool kHeadSplit = G >= 4 && G >= C;
+
+template <int M, int G, int C, bool APPEND>
+cudaError_t attend_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
+    if constexpr (kHeadSplit<G, C>) return launch_headsplit<M, G, C, APPEND>(p, plan, s);
+    else return launch_attend<M, G, C, APPEND>(p, plan, s);
+}
+
+template <int M, int G, int C>
+size_t attend_smem(int split_len) {
+    if constexpr (kHeadSplit<G, C>) return HsCfg<M, G, C>::smem(split_len);
+    else return AtCfg<M, G, C>::smem(split_len);
+}
+
 template <int M, int G, bool APPEND>
 cudaError_t attend_c(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     switch (plan.cluster) {
-        case 2: return launch_attend<M, G, 2, APPEND>(p, plan, s);
-        case 4: return launch_attend<M, G, 4, APPEND>(p, plan, s);
+        case 2: return attend_one<M, G, 2, APPEND>(p, plan, s);
+        case 4: return attend_one<M, G, 4, APPEND>(p, plan, s);
         case 8:
-            if constexpr (M == 8) return launch_attend<M, G, 8, APPEND>(p, plan, s);
+            if constexpr (M == 8) return attend_one<M, G, 8, APPEND>(p, plan, s);
             else return cudaErrorInvalidConfiguration;
         default: return cudaErrorInvalidConfiguration;
     }
@@ -1767,7 +2642,7 @@ size_t pq_decode_smem_bytes(int M, int G, int cluster) {
 
 size_t pq_attend_smem_bytes(int M, int G, int cluster, int split_len) {
 #define AQ_AS(MM, GG, CC) \
-    if (M == MM && G == GG && cluster == CC) return AtCfg<MM, GG, CC>::smem(split_len);
+    if (M == MM && G == GG && cluster == CC) return attend_smem<MM, GG, CC>(split_len);
     AQ_AS(4, 1, 2) AQ_AS(4, 1, 4) AQ_AS(4, 2, 2) AQ_AS(4, 2, 4) AQ_AS(4, 4, 2) AQ_AS(4, 4, 4) AQ_AS(4, 8, 2) AQ_AS(4, 8, 4)
     AQ_AS(8, 1, 2) AQ_AS(8, 1, 4) AQ_AS(8, 1, 8) AQ_AS(8, 2, 2) AQ_AS(8, 2, 4) AQ_AS(8, 2, 8)
     AQ_AS(8, 4, 2) AQ_AS(8, 4, 4) AQ_AS(8, 4, 8) AQ_AS(8, 8, 2) AQ_AS(8, 8, 4) AQ_AS(8, 8, 8)

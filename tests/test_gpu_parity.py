@@ -87,6 +87,7 @@ CASES = [
     (2, 4, 2, 4, [64, 31]),                    # group 2
     (2, 4, 4, 8, [400, 1500]),                 # M = 8 (Dsub 16)
     (1, 16, 2, 8, [3001]),                     # M = 8 with group 8
+    (2, 8, 2, 8, [700, 45]),                   # M = 8 with group 4 (clusters of 8 cover the group twice)
     (1, 2, 2, 4, [9001]),                      # group 1, several chunks per CTA
     (4, 4, 4, 4, [0, 16, 15, 48]),             # empty request, page-exact lengths
     (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # Qwen-shaped GQA: 2 head sub-groups
@@ -407,6 +408,7 @@ STEP_CASES = [
     (3, 4, 4, 4, [1, 17, 333]),                # new token alone; page boundary at 16
     (2, 16, 2, 4, [1000, 257]),                # GQA group 8
     (2, 4, 4, 8, [400, 1500]),                 # M = 8
+    (2, 8, 2, 8, [700, 45]),                   # M = 8, group 4
     (1, 2, 2, 4, [9001]),                      # long: splits
     (4, 4, 4, 4, [16, 32, 48, 2048]),          # new token first in its page
     (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # GQA with 2 head sub-groups per kv head
