@@ -302,6 +302,39 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 
+// ---- warp-level tensor-core tiles (small fused contractions) -----------------
+// Four 8x8 fp16 matrices from shared memory, transposed: lane l gives the row
+// address of row l%8 of matrix l/8 (16 bytes each); register j of lane l then
+// holds elements (2(l%4), l/4) and (2(l%4)+1, l/4) of matrix j, i.e. the
+// m16n8k16 A fragment of the transposed 16x16 block when the matrices are
+// (rows 0-7, cols 0-7), (rows 0-7, cols 8-15), (rows 8-15, cols 0-7),
+// (rows 8-15, cols 8-15) of the stored block.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// d += A(16x16, fp16) * B(16x8, fp16) with fp32 accumulation, warp-wide.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values as an fp16 pair (x in the low half) split into a rounded
+// high part and the rounded remainder: x = hi + lo to about 22 bits.
+__device__ __forceinline__ void f16x2_split(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
 // ---- 5th-generation tensor cores (tcgen05) -----------------------------------
 // One CTA (cta_group::1) allocates tensor memory (TMEM) columns, one thread
 // issues MMAs whose operands sit in shared memory (described by 64-bit matrix

@@ -2169,10 +2169,17 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
             }
         }
     }
+    // the new token's value codes of the owned subspaces, while the peers' rows land
+    if constexpr (APPEND) {
+        if (cl_new) {
+            tmo |= !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns);
+            encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
+        }
+    }
     tmo |= !mbar_wait_limit(&bar[4], 0, p.wait_limit_ns);
     tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-    __syncthreads();                                   // the table of this CTA's heads, the new key's codes
+    __syncthreads();                                   // the table of this CTA's heads, the new token's codes
 
     // ---- scores of this CTA's H heads over every token of the split ----------
     constexpr int LH = H == 8 ? 3 : (H == 4 ? 2 : (H == 2 ? 1 : 0));
@@ -2280,13 +2287,6 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
             st_async_f32(mapa_u32(smem_u32(st_own + 3 * H + tid), pr), snv, pb);
         }
     }
-    // the new token's value codes of the owned subspaces
-    if constexpr (APPEND) {
-        if (cl_new) {
-            if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-            encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
-        }
-    }
     __syncthreads();                                   // statistics of this CTA's heads
     {
         float rq[H];
@@ -2353,80 +2353,81 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
     }
 
     // ---- value codebook product for the owned dims, all G heads ---------------
+    // A dense [dims x 256] . [256 x G] contraction per owned subspace, on the
+    // tensor cores: D[d][g] = sum_k C^V[k][d] * W[k][g] / 2^31, C^V read
+    // transposed from the swizzled slice by ldmatrix, the fixed-point bins W
+    // as fp16 high and low parts (22 significant bits; each bin / 2^31 is at
+    // most about 1), fp32 accumulation.  Warp w takes codewords [32w, 32w+32);
+    // the warps' partial sums meet in the epilogue.
     {
-        constexpr int NQ = S::NQ, KSQ = S::KSQ, KSLQ = S::KSLQ;
-        constexpr int ROWS128 = 128 / (DSUB * 2);
-        static_assert(KSQ % (ROWS128 * NCH) == 0, "row step keeps the swizzle position");
-        const int qd = tid % NQ, ks = tid / NQ;
-        const int mi = qd / (DSUB / 4), j4 = (qd % (DSUB / 4)) * 4;
-        const int cj = j4 / 8, hj = j4 % 8;
-        const int kx = ks ^ ((mi * S::VPX) & (KSQ - 1));
-        const __half *vrow = cbv + ((mi * K + kx) * NCH + chunk_pos<DSUB>(kx, cj)) * 8 + hj;
-        // bins of head r*H + h: this CTA's own (r == rank) or those rank r sent
-        const unsigned *wsrc[C];
+        static_assert(K == 32 * kWarps, "32 codewords per warp");
+        static_assert(DSUB % 16 == 0, "16-dim tiles");
+        constexpr int MT = DSUB / 16, NT = (G + 7) / 8;
+        const int gid = lane >> 2, tig = lane & 3;
+        float acc[MC][MT][NT][4];
 #pragma unroll
-        for (int r = 0; r < C; ++r)
-            wsrc[r] = (r == rank ? bins + static_cast<size_t>(rank * MC + mi) * K * H
-                                 : rb + static_cast<size_t>(r * MC + mi) * K * H) + kx * H;
-        unsigned long long acc[G][2];
+        for (int mi = 0; mi < MC; ++mi)
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) acc[gg][0] = acc[gg][1] = 0ull;
-#pragma unroll 4
-        for (int i = 0; i < KSLQ; ++i) {
-            const uint2 cv2 = *reinterpret_cast<const uint2 *>(vrow + i * KSQ * NCH * 8);
-            const unsigned long long c01 = h2_to_f2p(cv2.x), c23 = h2_to_f2p(cv2.y);
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                unsigned wu[H];
-                load_vec_u<H>(wu, wsrc[r] + i * KSQ * H);
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const float wf = static_cast<float>(wu[h]);
-                    const unsigned long long ww = f2_pack(wf, wf);
-                    acc[r * H + h][0] = f2_fma(ww, c01, acc[r * H + h][0]);
-                    acc[r * H + h][1] = f2_fma(ww, c23, acc[r * H + h][1]);
+                    for (int e = 0; e < 4; ++e) acc[mi][mt][nt][e] = 0.f;
+#pragma unroll
+        for (int mi = 0; mi < MC; ++mi) {
+            const __half *vs = cbv + static_cast<size_t>(mi) * K * DSUB;
+#pragma unroll
+            for (int kstep = 0; kstep < 2; ++kstep) {
+                const int k0 = warp * 32 + kstep * 16;
+                uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    // head n's bins of codewords k0 + 2 tig + {0, 1} and + 8
+                    const int n = nt * 8 + gid, src = n / H, hh = n % H;
+                    const unsigned *wb = src == rank ? bins + static_cast<size_t>(rank * MC + mi) * K * H
+                                                     : rb + static_cast<size_t>(src * MC + mi) * K * H;
+                    float w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int k = k0 + 2 * tig + (j & 1) + (j >> 1) * 8;
+                        w[j] = n < G ? static_cast<float>(wb[k * H + (hh ^ hs_bswz<H, S::KSQ>(k))]) * (1.0f / 2147483648.0f)
+                                     : 0.f;
+                    }
+                    f16x2_split(w[0], w[1], bh[nt][0], bl[nt][0]);
+                    f16x2_split(w[2], w[3], bh[nt][1], bl[nt][1]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    // rows k0 + l%8 (+8 for matrices 2, 3), 8-dim chunk 2 mt (+1 for matrices 1, 3)
+                    const int kr = k0 + (lane & 7) + ((lane >> 4) << 3);
+                    const int c = 2 * mt + ((lane >> 3) & 1);
+                    uint32_t a[4];
+                    ldsm_x4_trans(smem_u32(vs + (kr * NCH + chunk_pos<DSUB>(kr, c)) * 8), a);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_16816(acc[mi][mt][nt], a, bh[nt][0], bh[nt][1]);
+                        mma_16816(acc[mi][mt][nt], a, bl[nt][0], bl[nt][1]);
+                    }
                 }
             }
         }
-        float accf[G][4];
+        // D fragment: (dim gid, heads 2 tig, 2 tig + 1) and (dim gid + 8, same heads)
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-            const float2 a01 = f2_unpack(acc[gg][0]), a23 = f2_unpack(acc[gg][1]);
-            accf[gg][0] = a01.x; accf[gg][1] = a01.y; accf[gg][2] = a23.x; accf[gg][3] = a23.y;
-        }
-        // word h of a row holds head h ^ x of its source (x fixed along this
-        // thread's rows)
-        const int x = hs_bswz<H, KSQ>(kx);
+        for (int mi = 0; mi < MC; ++mi)
 #pragma unroll
-        for (int bv = 1; bv < H; bv <<= 1) {
-            const bool swp = (x & bv) != 0;
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                if (gg & bv) continue;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int n = nt * 8 + 2 * tig;
+                    if (n < G) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = accf[gg][e], c = accf[gg | bv][e];
-                    accf[gg][e] = swp ? c : a;
-                    accf[gg | bv][e] = swp ? a : c;
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int dl = mi * DSUB + mt * 16 + gid + 8 * hf;
+                            *reinterpret_cast<float2 *>(part + (static_cast<size_t>(warp) * MC * DSUB + dl) * G + n) =
+                                make_float2(acc[mi][mt][nt][2 * hf], acc[mi][mt][nt][2 * hf + 1]);
+                        }
+                    }
                 }
-            }
-        }
-#pragma unroll
-        for (int off = NQ; off < 32; off <<= 1) {
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accf[gg][e] += __shfl_xor_sync(0xffffffffu, accf[gg][e], off);
-        }
-        if (lane < NQ) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v[G];
-#pragma unroll
-                for (int gg = 0; gg < G; ++gg) v[gg] = accf[gg][e];
-                store_vec<G>(part + (static_cast<size_t>(warp) * MC * DSUB + mi * DSUB + j4 + e) * G, v);
-            }
-        }
     }
     __syncthreads();
     for (int i = tid; i < S::NOUT; i += kThreads) {
@@ -2437,7 +2438,7 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         const float *sth = stx + (gg / H) * S::STX;       // statistics of head gg, from its CTA
         const int hh = gg % H;
         const float mxg = sth[hh], lg = sth[H + hh];
-        o *= sth[2 * H + hh];
+        o *= sth[2 * H + hh] * 2147483648.0f;         // the product's bins were scaled by 2^-31
         if constexpr (APPEND) {
             if (cl_new) {
                 // the new token: its weight times its value codeword
