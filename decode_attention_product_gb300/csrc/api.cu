@@ -58,15 +58,20 @@ std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
 
 unsigned long long decode_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
-cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need) {
+cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need, int carveout_pct) {
+    auto set = [&]() {
+        cudaError_t r = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(need));
+        if (r == cudaSuccess && carveout_pct >= 0)
+            r = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, carveout_pct);
+        return r;
+    };
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(need));
+    if (dev < 0 || dev >= kMaxDevices) return set();
     std::lock_guard<std::mutex> lock(a.mu);
     if (a.bytes[dev] >= need) return cudaSuccess;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(need));
+    e = set();
     if (e == cudaSuccess) a.bytes[dev] = need;
     return e;
 }

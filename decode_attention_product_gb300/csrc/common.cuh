@@ -316,6 +316,17 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                  : "memory");
 }
 
+// The same four matrices untransposed: register j of lane l holds elements
+// (l/4, 2(l%4)) and (l/4, 2(l%4)+1) of matrix j -- the A fragment when the
+// matrices are (rows 0-7, cols 0-7), (rows 8-15, cols 0-7), (rows 0-7,
+// cols 8-15), (rows 8-15, cols 8-15) of a row-major 16x16 block.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 // d += A(16x16, fp16) * B(16x8, fp16) with fp32 accumulation, warp-wide.
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(

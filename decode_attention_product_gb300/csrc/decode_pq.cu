@@ -2095,54 +2095,87 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
     tmo |= !mbar_wait_limit(&bar[3], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     cluster_wait_acquire();                            // peers' barriers expect our pushes
+    // Table rows on the tensor cores: D[k][g] = sum_d C^K_m[k][d] q_g[m][d]
+    // for the owned subspaces, codebook rows by ldmatrix from the swizzled
+    // slice, the queries as fp16 high and low parts (about 22 significant
+    // bits), fp32 accumulation; warp w computes codewords [32w, 32w+32) for
+    // all G heads, and each value goes to the CTA that owns its head.
     {
-        float dkv[MC];
+        static_assert(K == 32 * kWarps && DSUB % 16 == 0, "16x16 tiles, 32 codewords per warp");
+        constexpr int KS = DSUB / 16, NT = (G + 7) / 8;
+        const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
         for (int mi = 0; mi < MC; ++mi) {
             const int m = rank * MC + mi;
-            const float *qm = qs + m * DSUB;
-            const uint4 *rowk = reinterpret_cast<const uint4 *>(cbk) + (mi * K + tid) * NCH;
-            unsigned long long acc2[G];
+            const __half *ks_ = cbk + static_cast<size_t>(mi) * K * DSUB;
+            float acc[2][NT][4];
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) acc2[gg] = 0ull;
-            float dk = 0.f;
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                unsigned long long f[4];
-                to_f2p4(rowk[chunk_pos<DSUB>(tid, c)], f);
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int gg = 0; gg < G; ++gg) {
-                    const ulonglong2 *qv = reinterpret_cast<const ulonglong2 *>(qm + gg * D + c * 8);
-                    const ulonglong2 qa = qv[0], qb = qv[1];
-                    unsigned long long a = acc2[gg];
-                    a = f2_fma(qa.x, f[0], a);
-                    a = f2_fma(qa.y, f[1], a);
-                    a = f2_fma(qb.x, f[2], a);
-                    a = f2_fma(qb.y, f[3], a);
-                    acc2[gg] = a;
+                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+#pragma unroll
+            for (int kst = 0; kst < KS; ++kst) {
+                uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    // head n's query dims 2 tig + {0, 1} and + 8 of this 16-dim step
+                    const int n = nt * 8 + gid;
+                    float2 x0 = make_float2(0.f, 0.f), x1 = x0;
+                    if (n < G) {
+                        const float *qn = qs + n * D + m * DSUB + kst * 16 + 2 * tig;
+                        x0 = *reinterpret_cast<const float2 *>(qn);
+                        x1 = *reinterpret_cast<const float2 *>(qn + 8);
+                    }
+                    f16x2_split(x0.x, x0.y, bh[nt][0], bl[nt][0]);
+                    f16x2_split(x1.x, x1.y, bh[nt][1], bl[nt][1]);
                 }
-                if (APPEND && cl_new) dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
-            }
-            // heads [r*H, (r+1)*H) go to rank r: this CTA's straight into its
-            // table, a peer's into that peer's staging rows
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float v[H];
+                for (int mt = 0; mt < 2; ++mt) {
+                    // rows 32 warp + 16 mt + l%8 (+8 for matrices 1, 3), chunk 2 kst (+1 for matrices 2, 3)
+                    const int row = warp * 32 + mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int c = 2 * kst + (lane >> 4);
+                    uint32_t a[4];
+                    ldsm_x4(smem_u32(ks_ + (row * NCH + chunk_pos<DSUB>(row, c)) * 8), a);
 #pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const float2 a = f2_unpack(acc2[r * H + h]);
-                    v[h] = (a.x + a.y) * p.scale_log2;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_16816(acc[mt][nt], a, bh[nt][0], bh[nt][1]);
+                        mma_16816(acc[mt][nt], a, bl[nt][0], bl[nt][1]);
+                    }
                 }
-                float *dst = r == rank ? tab + (static_cast<size_t>(m) * K + tid) * H
-                                       : sb + (static_cast<size_t>(r * MC + mi) * K + tid) * H;
-                store_vec<H>(dst, v);
             }
-            dkv[mi] = dk;
+            // D fragment: codeword 32 warp + 16 mt + gid (+8), heads nt*8 + 2 tig + {0, 1}
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int k = warp * 32 + mt * 16 + gid + 8 * hf;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int n = nt * 8 + 2 * tig + e;
+                            if (n < G) {
+                                const int r = n / H, h = n % H;
+                                float *dst = r == rank ? tab + (static_cast<size_t>(m) * K + k) * H + h
+                                                       : sb + (static_cast<size_t>(r * MC + mi) * K + k) * H + h;
+                                *dst = acc[mt][nt][2 * hf + e] * p.scale_log2;
+                            }
+                        }
+                    }
         }
+        // the new key's codes: exact-rule distances, one thread per codeword
         if constexpr (APPEND) {
             if (cl_new) {
 #pragma unroll
-                for (int mi = 0; mi < MC; ++mi) warp_argmin_into(dkv[mi], &keys[mi]);
+                for (int mi = 0; mi < MC; ++mi) {
+                    float dk = 0.f;
+                    for_row_chunks<DSUB, false>(cbk, mi * K + tid, [&](int c, const unsigned long long (&f)[4]) {
+                        dk = sqdist8(dk, xnew + mi * DSUB + c * 8, f);
+                    });
+                    warp_argmin_into(dk, &keys[mi]);
+                }
             }
         }
     }
@@ -2478,7 +2511,14 @@ cudaError_t launch_headsplit(const DecodeParams &p, const Plan &plan, cudaStream
     if (plan.split_len > S::MAX_SPLIT || plan.split_len % kPage) return cudaErrorInvalidValue;
     static SmemAttr attr_state;
     const size_t need = S::smem(plan.split_len);
-    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), S::smem(S::MAX_SPLIT));
+    // Shared memory for two resident CTAs per SM, the rest as L1: the launch
+    // is one wave at two per SM, and a third CTA (the next launch's, under
+    // programmatic dependent launch) only competes with the running ones
+    // (measured on qwen_gqa: 10.5 us per step with three, 9.6 with two).
+    constexpr size_t kSmPerSM = 233472;                // 228 KiB
+    const int pct = static_cast<int>((2 * (S::smem(S::MAX_SPLIT) + 1024) * 100 + kSmPerSM - 1) / kSmPerSM);
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), S::smem(S::MAX_SPLIT),
+                                         pct < 100 ? pct : 100);
         e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

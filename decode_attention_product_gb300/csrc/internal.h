@@ -131,7 +131,9 @@ struct SmemAttr {
 };
 // Make sure `func` may launch with `need` bytes of dynamic shared memory on the
 // current device (sets the attribute the first time a larger size is asked
-// for on that device; thread-safe).
-cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need);
+// for on that device; thread-safe).  carveout_pct >= 0 also sets the
+// preferred shared-memory carveout (percent of the SM's shared memory; the
+// rest serves as L1) at that point.
+cudaError_t ensure_smem_attr(SmemAttr &a, const void *func, size_t need, int carveout_pct = -1);
 
 }  // namespace aq
