@@ -153,13 +153,18 @@ def measured_traffic(workload: str, mode: str):
     return float(e["dram_bytes"]) if e.get("decode_pq_sha256") == digest else None
 
 
-def step_kernel_name(group: int) -> str:
-    """The decode kernel the library's planner picks for a fused step: the
-    whole-split kernel when at least 4 query heads share a kv head (and no
-    AQPQ_DECODE_KERNEL override asks for the other), else the token-share one."""
+def step_kernel_name(group: int, subspaces: int) -> str:
+    """The decode kernel the library's planner picks for a fused step: for at
+    least 4 query heads per kv head (and no AQPQ_DECODE_KERNEL override asking
+    for the other) the whole-split design on clusters of one subspace per CTA --
+    the head-split kernel when the group covers the cluster, else the
+    whole-split kernel -- otherwise the token-share kernel."""
     forced = os.environ.get("AQPQ_DECODE_KERNEL", "")
-    attend = forced == "2" or (forced != "1" and group >= 4)
-    return ("pq_attend_kernel" if attend else "pq_decode_kernel") + " (fused step)"
+    if forced == "2" or (forced != "1" and group >= 4):
+        name = "pq_headsplit_kernel" if group >= 4 and group >= subspaces else "pq_attend_kernel"
+    else:
+        name = "pq_decode_kernel"
+    return name + " (fused step)"
 
 
 def workload_desc(w) -> str:
@@ -448,7 +453,7 @@ def measure_fused_step(args, w, api, torch, T, base, local_rank, dist, world, e4
               f"({R * per_copy / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB)",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": measured_traffic(w.name, "step"),
-                     "kernel": step_kernel_name(Hq // Hkv), "bytes_per_launch": byt["total"],
+                     "kernel": step_kernel_name(Hq // Hkv, M), "bytes_per_launch": byt["total"],
                      "launch_ms": ms, "peak_kind": peak_kind},
         "code_stream": {"gbs": byt["code_stream"] / (ms / 1e3) / 1e9,
                         "codes_only_gbs": byt["codes"] / (ms / 1e3) / 1e9,
