@@ -279,6 +279,38 @@ static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv,
 
 }  // namespace aq
 
+namespace aq {
+namespace {
+
+// The device address of page-locked host memory the device can reach (pinned
+// with cudaHostAlloc / cudaMallocHost or registered), or null for any other
+// pointer (pageable memory, device memory).
+void *mapped_host(const void *h) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// The step's query and new K/V from mapped host memory into the device
+// staging, 16 bytes per thread over the NVLink-C2C link: the host-to-device
+// copy of a step without a DMA set-up, ahead of the step, which starts as its
+// programmatic dependent and reads the staging after it completes.
+__global__ void __launch_bounds__(256) host_gather_kernel(const uint4 *q_h, uint4 *q_d, size_t nq, const uint4 *kv_h,
+                                                          uint4 *kv_d, size_t nkv) {
+    grid_launch_dependents();
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t j = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < nq + nkv; j += stride) {
+        if (j < nq) q_d[j] = q_h[j];
+        else kv_d[j - nq] = kv_h[j - nq];
+    }
+}
+
+}  // namespace
+}  // namespace aq
+
 using namespace aq;
 
 extern "C" {
@@ -614,8 +646,29 @@ aq_status aq_decode_step_host(const aq_pq_config *cfg, int32_t batch, int32_t nu
     void *kv_d = st + (qb + 255) / 256 * 256;
     float *out_d = reinterpret_cast<float *>(st + (qb + 255) / 256 * 256 + (kvb + 255) / 256 * 256);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the copies precede the step in stream order; no programmatic overlap
-    // with a preceding kernel (the step's inputs come from the copies)
+    // page-locked buffers the device can reach: the inputs by a gather kernel,
+    // the output written by the step straight into host memory
+    void *q_m = misaligned(q_host) ? nullptr : mapped_host(q_host);
+    void *kv_m = q_m && !misaligned(kv_new_host) ? mapped_host(kv_new_host) : nullptr;
+    void *out_m = kv_m ? mapped_host(out_host) : nullptr;
+    if (out_m) {
+        const size_t nq = qb / 16, nkv = kvb / 16;
+        size_t blocks = (nq + nkv + 255) / 256;
+        if (blocks > 4 * static_cast<size_t>(kPlanSMs)) blocks = 4 * static_cast<size_t>(kPlanSMs);
+        host_gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            static_cast<const uint4 *>(q_m), reinterpret_cast<uint4 *>(q_d), nq, static_cast<const uint4 *>(kv_m),
+            static_cast<uint4 *>(kv_d), nkv);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+        // the step as a programmatic dependent of the gather, which writes none
+        // of its early inputs (codebooks, req_set, seq_lens, block table, pages)
+        return aq_decode_step(cfg, batch, num_q_heads, num_kv_heads, q_d, kv_d, code_pages, num_pages, codebooks_f16,
+                              num_sets, req_set, block_table, max_pages, seq_lens, max_seq_len, scale, num_splits,
+                              (flags & ~AQ_STEP_OVERLAP) | AQ_STEP_OVERLAP, static_cast<float *>(out_m), workspace,
+                              workspace_bytes, device_status, stream);
+    }
+    // otherwise DMA copies, which precede the step in stream order; no
+    // programmatic overlap with a preceding kernel
     cudaError_t e = cudaMemcpyAsync(q_d, q_host, qb, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(kv_d, kv_new_host, kvb, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);

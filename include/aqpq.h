@@ -320,16 +320,22 @@ aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch,
  * output in host memory (a serving loop's view: one call per step).  An
  * interface convenience of this library; the pages describe the step itself.
  *
- * Enqueues on `stream`: the copy of q_host [B][Hq][D] fp32 and kv_new_host
+ * Enqueues on `stream` the transfer of q_host [B][Hq][D] fp32 and kv_new_host
  * [B][Hkv][2][D] fp16 into the caller's device `staging`, the fused step, and
- * the copy of the output into out_host [B][Hq][D] fp32.  Returns once they
+ * the transfer of the output into out_host [B][Hq][D] fp32.  Returns once they
  * are enqueued; out_host holds the step's output when the stream has passed
- * this point.  For asynchronous copies the host buffers are page-locked
- * (pinned); pageable ones make the copies synchronous.
+ * this point.  When all three buffers are page-locked host memory the device
+ * can address (cudaHostAlloc / cudaMallocHost / cudaHostRegister) and q_host
+ * and kv_new_host are 16-byte aligned, a gather kernel reads the inputs over
+ * the host link into `staging`, the step starts as its programmatic dependent
+ * and writes its output directly into out_host (no DMA copies); otherwise the
+ * inputs and the output move by cudaMemcpyAsync (pageable buffers make those
+ * copies synchronous).  Either way the host must not rewrite the inputs or
+ * read the output until the stream has passed the step.
  *   staging        device memory of >= aq_decode_step_host_staging() bytes,
  *                  16-byte aligned, owned by the caller (no allocation here)
- *   flags          AQ_STEP_E4M3 only (AQ_STEP_OVERLAP is ignored: the step's
- *                  inputs come from the copies just before it)
+ *   flags          AQ_STEP_E4M3 only (AQ_STEP_OVERLAP is ignored: the step
+ *                  follows its own input transfer)
  *   other arguments as aq_decode_step.
  * ------------------------------------------------------------------------- */
 size_t aq_decode_step_host_staging(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads);

@@ -612,3 +612,39 @@ def test_decode_step_host_buffers(A, orc):
     want = orc.decode_attention(q, want_pages, p["codebooks"], p["req_set"], p["block_table"], p["seq_lens"],
                                 1.0 / np.sqrt(128), 16)
     close(got, want)
+
+
+def test_decode_step_host_pageable_matches_pinned(A):
+    """aq_decode_step_host on pageable host buffers (plain numpy arrays: the
+    DMA-copy path) and on page-locked ones (api.HostDecodeStep: the gather
+    kernel and the direct output write): the same outputs and codes bit for
+    bit, over two steps with new inputs."""
+    import ctypes
+    B, Hq, Hkv, M, lens = 3, 8, 4, 4, [333, 1024, 17]
+    p = W.paged_codes_problem(68, B, Hq, Hkv, M, lens, num_sets=B)
+    rng = np.random.default_rng(68)
+    args = (dev(p["codebooks"]), dev(p["req_set"]), dev(p["block_table"]), dev(p["seq_lens"]), max(lens))
+    pages_a, pages_b = dev(p["code_pages"]), dev(p["code_pages"])
+    pinned = A.HostDecodeStep(pages_a, *args, Hq, 1.0 / np.sqrt(128))
+    paged = A.HostDecodeStep(pages_b, *args, Hq, 1.0 / np.sqrt(128))
+    q_np = np.zeros((B, Hq, 128), np.float32)
+    kv_np = np.zeros((B, Hkv, 2, 128), np.float16)
+    out_np = np.zeros((B, Hq, 128), np.float32)
+    call = list(paged._args)
+    call[4], call[5], call[18] = (ctypes.c_void_p(a.ctypes.data) for a in (q_np, kv_np, out_np))
+    for _ in range(2):
+        q = rng.standard_normal((B, Hq, 128)).astype(np.float32)
+        kv = rng.standard_normal((B, Hkv, 2, 128)).astype(np.float16)
+        pinned.q_host.copy_(torch.from_numpy(q))
+        pinned.kv_host.copy_(torch.from_numpy(kv))
+        pinned.launch()
+        q_np[...] = q
+        kv_np[...] = kv
+        assert paged._fn(*call) == 0
+        pinned.sync()
+        paged.sync()
+        pinned.check_status()
+        paged.check_status()
+        assert np.array_equal(pinned.out_host.numpy(), out_np)
+        assert torch.equal(pages_a, pages_b)
+
