@@ -192,7 +192,7 @@ static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv,
 
 // The plan of a decode call.  PQ: the whole-split kernel for GQA groups of 4
 // or more query heads per kv head when a split of at most two fits its
-// capacity (and the codebooks are fp16) -- there the table and value product
+// capacity (with E4M3 codebooks only its head-split form) -- there the table and value product
 // per query head dominate and scoring every token in each CTA is cheap
 // (measured: B8 Hq64 Hkv8 L1000 13.3 -> 12.9 us) -- else the token-share
 // kernel, whose split of the token work across the cluster is cheaper when
@@ -221,7 +221,10 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
                            ? static_cast<size_t>(batch) * Hq * p2.num_splits * (kHeadDim + 2) * sizeof(float)
                            : 0;
         const size_t ws = p2.workspace > p1.workspace ? p2.workspace : p1.workspace;
-        *pl = e4m3 ? p1 : p2;
+        // E4M3 codebooks: the head-split kernel (the group covers the cluster of
+        // one subspace per CTA) widens its slices; the whole-split one reads fp16
+        const int G = Hq / Hkv, M = cfg->num_subspaces;
+        *pl = (e4m3 && !(G >= 4 && G >= M)) ? p1 : p2;
         pl->workspace = ws;
         return AQ_OK;
     }

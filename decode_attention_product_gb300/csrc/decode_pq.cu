@@ -1965,6 +1965,40 @@ __device__ __forceinline__ int hs_bswz(int k) {
     else return 0;
 }
 
+// An E4M3 slice landed raw (one byte per element, rows of DSUB bytes in the
+// e8_pos layout) in the upper half of its fp16 buffer: widened exactly to fp16
+// (E4M3 is a subset of fp16) into the buffer's swizzled fp16 layout.  Every
+// thread reads its chunks first, a barrier, then writes (the halves overlap).
+template <int DSUB, int MC>
+__device__ __forceinline__ void widen_e4m3_slice(__half *buf) {
+    constexpr int NE = DSUB / 16, NCH = DSUB / 8, ROWS = MC * kCodewords, PER = ROWS * NE / kThreads;
+    static_assert(ROWS * NE % kThreads == 0, "whole chunks per thread");
+    const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(buf) + ROWS * DSUB);
+    uint4 raw[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int q = static_cast<int>(threadIdx.x) + i * kThreads, row = q / NE, e = q % NE;
+        raw[i] = src[row * NE + e8_pos<DSUB>(row, e)];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int q = static_cast<int>(threadIdx.x) + i * kThreads, row = q / NE, e = q % NE;
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((w[j / 2] >> (16 * (j % 2))) & 0xffffu), __NV_E4M3);
+            h[j] = static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(buf) + row * NCH;
+        dst[chunk_pos<DSUB>(row, 2 * e)] = make_uint4(h[0], h[1], h[2], h[3]);
+        dst[chunk_pos<DSUB>(row, 2 * e + 1)] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+    __syncthreads();
+}
+
 template <int M, int G, int C, bool APPEND>
 __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_kernel(const __grid_constant__ DecodeParams p) {
     using S = HsCfg<M, G, C>;
@@ -2036,14 +2070,21 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
     const int ntok = (cl_new ? new_pos : te) - ts;
     const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
     const int pg_new = (APPEND && cl_new && tid == 0) ? __ldg(bt + new_pos / P) : -1;
+    // E4M3 codebooks: the raw slices (half the bytes) into the upper halves of
+    // the fp16 buffers, widened there once they have landed
+    const bool e8 = p.codebook_e4m3 != 0;
     if (tid == 0) {
         const int row0 = ((set * Hkv + kvh) * 2) * M * K + rank * MC * K;
-        mbar_arrive_expect_tx(&bar[0], S::SLICE_BYTES);
+        const uint32_t sl_bytes = e8 ? S::SLICE_BYTES / 2 : S::SLICE_BYTES;
+        const int row_bytes = e8 ? DSUB : 2 * DSUB;
+        unsigned char *kdst = reinterpret_cast<unsigned char *>(cbk) + (e8 ? S::SLICE_BYTES / 2 : 0);
+        unsigned char *vdst = reinterpret_cast<unsigned char *>(cbv) + (e8 ? S::SLICE_BYTES / 2 : 0);
+        mbar_arrive_expect_tx(&bar[0], sl_bytes);
 #pragma unroll
-        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbk + mi * K * DSUB, &p.cb_map, 0, row0 + mi * K, &bar[0]);
-        mbar_arrive_expect_tx(&bar[1], S::SLICE_BYTES);
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(kdst + mi * K * row_bytes, &p.cb_map, 0, row0 + mi * K, &bar[0]);
+        mbar_arrive_expect_tx(&bar[1], sl_bytes);
 #pragma unroll
-        for (int mi = 0; mi < MC; ++mi) tma_load_2d(cbv + mi * K * DSUB, &p.cb_map, 0, row0 + M * K + mi * K, &bar[1]);
+        for (int mi = 0; mi < MC; ++mi) tma_load_2d(vdst + mi * K * row_bytes, &p.cb_map, 0, row0 + M * K + mi * K, &bar[1]);
         // from each peer: its rows of this CTA's heads, its new-key codes and
         // flag; later its bins of this CTA's subspaces and its heads' statistics
         mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::SB_FLOATS + (cl_new ? MC : 0) + 1) * 4);
@@ -2094,6 +2135,7 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
     bool tmo = !mbar_wait_limit(&bar[0], 0, p.wait_limit_ns);
     tmo |= !mbar_wait_limit(&bar[3], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+    if (e8) widen_e4m3_slice<DSUB, MC>(cbk);
     cluster_wait_acquire();                            // peers' barriers expect our pushes
     // Table rows on the tensor cores: D[k][g] = sum_d C^K_m[k][d] q_g[m][d]
     // for the owned subspaces, codebook rows by ldmatrix from the swizzled
@@ -2203,9 +2245,12 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         }
     }
     // the new token's value codes of the owned subspaces, while the peers' rows land
+    bool v_wide = !e8;
     if constexpr (APPEND) {
         if (cl_new) {
             tmo |= !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns);
+            if (e8) widen_e4m3_slice<DSUB, MC>(cbv);
+            v_wide = true;
             encode_new_value<DSUB, MC, K, NCH>(cbv, xnew + MC * DSUB, keys + MC);
         }
     }
@@ -2366,6 +2411,7 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         bad_all |= AQ_DEV_TIMEOUT;
     }
     cluster_arrive_relaxed();                          // everything sent to this CTA has landed
+    if (!v_wide) widen_e4m3_slice<DSUB, MC>(cbv);
     if constexpr (APPEND) {
         if (cl_new && tid == 0) {
             // this CTA's codes of the new token into its page slot
@@ -2548,6 +2594,7 @@ constexpr bool kHeadSplit = G >= 4 && G >= C;
 template <int M, int G, int C, bool APPEND>
 cudaError_t attend_one(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     if constexpr (kHeadSplit<G, C>) return launch_headsplit<M, G, C, APPEND>(p, plan, s);
+    else if (p.codebook_e4m3) return cudaErrorInvalidValue;   // fp16 slices only
     else return launch_attend<M, G, C, APPEND>(p, plan, s);
 }
 
@@ -2724,7 +2771,7 @@ cudaError_t launch_pq_decode(const DecodeParams &p, int M, int G, const Plan &pl
 cudaError_t launch_pq_decode_step(const DecodeParams &p, int M, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
     G /= plan.head_split;
-    if (plan.kernel == 2 && !p.codebook_e4m3)
+    if (plan.kernel == 2)           // E4M3 codebooks only in the head-split kernel (the planner's choice)
         e = M == 4 ? attend_g<4, true>(p, G, plan, s) : attend_g<8, true>(p, G, plan, s);
     else if (M == 4) e = p.codebook_e4m3 ? dispatch_g<4, true, true>(p, G, plan, s) : dispatch_g<4, true, false>(p, G, plan, s);
     else if (M == 8) e = p.codebook_e4m3 ? dispatch_g<8, true, true>(p, G, plan, s) : dispatch_g<8, true, false>(p, G, plan, s);
