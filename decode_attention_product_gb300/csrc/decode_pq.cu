@@ -614,13 +614,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             }
         }
     }
-    // with its own V buffer, the new value's codes while the peers' rows land
-    if constexpr (APPEND && !SHARED_V) {
-        if (cl_new) {
-            tmo |= !mbar_wait_limit(&bar[1], 0, p.wait_limit_ns);
-            encode_new_value<DSUB, MC, K, NCH, E4M3>(cbv, xnew + MC * DSUB, keys + MC);
-        }
-    }
     if constexpr (C > 1) tmo |= !mbar_wait_limit(&bar[2], 0, p.wait_limit_ns);
     if (tmo) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
     __syncthreads();
@@ -866,15 +859,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             if (lane == 0) st_async_f32(st + 4 * (4 * G), __int_as_float(sflag[0]), rbar);
         }
     }
-    // the new token's V codes (the peers' bins are landing meanwhile), then
-    // its codes into its page slot, its page id checked here
+    // the new token's V codes (the peers' bins are landing meanwhile: the
+    // codes are first needed by the merge, so the encode stays off the path
+    // from the table rows to the scores), then its codes into its page slot,
+    // its page id checked here
     if constexpr (APPEND) {
         if (cl_new) {
-            if constexpr (SHARED_V) {
-                if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
-                encode_new_value<DSUB, MC, K, NCH, E4M3>(cbv, xnew + MC * DSUB, keys + MC);
-                __syncthreads();
-            }
+            if (!mbar_wait_limit(&bar[1], 0, p.wait_limit_ns)) atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
+            encode_new_value<DSUB, MC, K, NCH, E4M3>(cbv, xnew + MC * DSUB, keys + MC);
+            __syncthreads();
 #pragma unroll
             for (int mi = 0; mi < MC; ++mi) vcode[mi] = static_cast<int>(keys[MC + mi] & 0xffu);
             if (tid == 0) {
