@@ -612,8 +612,8 @@ def run_ours(args, w, rank, world, local_rank):
 
 def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
     """Through the C-ABI call with host buffers (aq_decode_step_host, wrapped by
-    api.HostDecodeStep): every step copies its q and new K/V in from pinned host
-    memory, runs the fused step and copies its output back, and the host reads
+    api.HostDecodeStep): every step moves its q and new K/V in from pinned host
+    memory, runs the fused step and moves its output back, and the host reads
     each step's output.  Steps alternate between two streams, each with its own
     pinned buffers, so the host enqueues step i before it waits for (and
     reads) step i-1; they rotate over cache copies larger than 2 x L2, as the
@@ -672,7 +672,8 @@ def measure_e2e(args, w, api, torch, base, Lmax, ws, units, world, dist):
     return {"value": job_value(units, n, secs, world), "unit": UNIT,
             "h2d_bytes_per_step": q_h.numel() * 4 + kv_h.numel() * 2,
             "d2h_bytes_per_step": out_h.numel() * 4, "ms_per_step": 1e3 * secs / n, "steps_timed": n,
-            "how": "aq_decode_step_host (copies in, fused step, copy out) per step over rotated cache copies, "
+            "how": "aq_decode_step_host per step (pinned buffers: a gather kernel reads q and the new K/V from "
+                   "host memory, the fused step writes its output into host memory), over rotated cache copies, "
                    "alternating two streams; step i enqueued before the host waits for and reads step i-1"}
 
 
@@ -781,7 +782,8 @@ def measure_layer_sweep(args, w, api, torch, base0, Lmax, T):
 def measure_mixed(args, w, api, torch, T, base, n16, local_rank=0):
     """The mixed-precision step (AQPIM blog §6.1 item 4): kv heads [0, n16)
     keep fp16 pages of the same raw vectors, the others the PQ cache; one
-    aq_decode_step_mixed per step (PQ step, fp16 append, fp16 attention),
+    aq_decode_step_mixed per step (the PQ step, then the fp16 heads' append +
+    attention as its programmatic dependent; a combine per part that splits),
     timed like the main step over rotated copies larger than 2 x L2."""
     Hq, Hkv, M = w.num_q_heads, w.num_kv_heads, w.num_subspaces
     G = Hq // Hkv
@@ -815,11 +817,14 @@ def measure_mixed(args, w, api, torch, T, base, n16, local_rank=0):
     f16_total = f16["total"] - f16["q"] - f16["out"] + 2 * w.batch * n16 * 2 * 128 * 2   # q/out counted once; the append
     byt = pq + f16_total
     peak, _ = measured_peaks()
+    s16 = api.decode_plan(w.batch, n16 * G, n16, Lmax, fp16=True)[0]
+    spq = api.decode_plan(w.batch, (Hkv - n16) * G, Hkv - n16, Lmax, M)[0]
+    launches = 2 + (s16 > 1) + (spq > 1)
     del copies, mb
     return {"fp16_kv_heads": n16, "pq_kv_heads": Hkv - n16, "ms_per_step": ms, "steps_timed": n_timed,
             "bytes_per_step": byt, "gbs": byt / (ms / 1e3) / 1e9, "frac_of_peak": byt / (ms / 1e3) / 1e9 / peak,
             "value": T.kv_tokens_heads(w.seq_lens, Hkv) / (ms / 1e3), "unit": UNIT,
-            "launches_per_step": 3, "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB"}
+            "launches_per_step": launches, "l2": f"rotating {R} input copies of {per_copy / 1e6:.1f} MB"}
 
 
 def ctypes_workspace(api, w, n16, Lmax, torch):

@@ -836,8 +836,13 @@ aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t n
             p.part_o = wsp;
             p.part_ml = p.part_o + static_cast<size_t>(batch) * Hq * p16.num_splits * kHeadDim;
         }
-        cudaError_t e = launch_append_fp16(p, s);
-        if (e == cudaSuccess) e = launch_fp16_decode(p, G, p16, s);
+        // one kernel appends the new tokens and attends (fp16_decode_kernel's
+        // APPEND form); after the PQ step it starts as that step's programmatic
+        // dependent: it reads none of the step's outputs, and the step lets
+        // dependents start only once it has passed its own dependency wait, so
+        // the kernels before the step are complete.  It finishes after the step.
+        p.overlap = n16 < Hkv ? 1 : 0;
+        cudaError_t e = launch_fp16_decode(p, G, p16, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return AQ_OK;

@@ -7,7 +7,10 @@
 // 16-token pages (4 KiB of keys, 4 KiB of values) with 8-byte loads, lane l
 // holding dims [4l, 4l+4).  Scores are warp all-reduced dot products; every
 // warp keeps its own running (max, sum, acc) per query head of the GQA group;
-// the 8 warp states are merged in shared memory at the end.
+// the 8 warp states are merged in shared memory at the end.  With APPEND (the
+// fp16 heads of a mixed-precision step) the CTA whose split holds position
+// seq_lens[b] - 1 writes the new key and value into that page slot and its
+// page's warp scores them from kv_new directly.
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,7 +26,7 @@ __device__ __forceinline__ float4 h4_to_f4(uint2 u) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-template <int G>
+template <int G, bool APPEND>
 __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int D = kHeadDim, P = kPage;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -42,6 +45,9 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
     const int ts = split * p.split_len;
     const int te = bad0 ? ts : min(L_raw, ts + p.split_len);
     if (bad0 || ts >= te) {
+        // launched as a programmatic dependent (mixed step): finish after the
+        // preceding kernel, so that stream order holds for what follows
+        grid_dependency_wait();
         if (bad0 && tid == 0) flag_status(p.status, bad0);
         const float v = bad0 ? __int_as_float(0x7fc00000) : 0.0f;
         for (int i = tid; i < G * D; i += kThreads) {
@@ -56,6 +62,25 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
         return;
     }
     if (tid == 0) *sbad = 0;
+    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    // the fused step's new token (position L-1), this lane's dims of its key
+    // and value; the page slot is written by warp 0 and read by nobody here
+    const int new_pos = APPEND ? L_raw - 1 : -1;
+    const bool own_new = APPEND && new_pos >= ts && new_pos < te;
+    uint2 knew = make_uint2(0u, 0u), vnew = knew;
+    if (own_new) {
+        const uint2 *src = reinterpret_cast<const uint2 *>(p.kv_new) +
+                           (static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + kvh) * 2 * (D / 4);
+        knew = src[lane];
+        vnew = src[D / 4 + lane];
+        const int pgn = bt[new_pos / P];
+        if (warp == 0 && pgn >= 0 && static_cast<int64_t>(pgn) < p.num_pages) {
+            uint2 *dst = reinterpret_cast<uint2 *>(const_cast<void *>(p.kv_pages)) +
+                         ((static_cast<size_t>(pgn) * Hkv + kvh) * 2 * P + static_cast<size_t>(new_pos % P)) * (D / 4);
+            dst[lane] = knew;
+            dst[static_cast<size_t>(P) * (D / 4) + lane] = vnew;
+        }
+    }
 
     // this lane's query slice, pre-scaled into the log2 domain
     float4 qv[G];
@@ -76,7 +101,6 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
     }
     __syncthreads();
 
-    const int32_t *bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
     const int pg0 = ts / P, pg1 = (te + P - 1) / P;
     int badpage = 0;
 #pragma unroll 1
@@ -95,6 +119,15 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
         for (int t = 0; t < P; ++t) {
             kr[t] = ldg_stream_v2(kp + t * D);
             vr[t] = ldg_stream_v2(vp + t * D);
+        }
+        if (APPEND && own_new && pi == new_pos / P) {
+            const int tn = new_pos % P;
+#pragma unroll
+            for (int t = 0; t < P; ++t)
+                if (t == tn) {
+                    kr[t] = knew;
+                    vr[t] = vnew;
+                }
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -143,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
         *reinterpret_cast<float4 *>(wacc + (warp * G + g) * D + 4 * lane) = acc[g];
     }
     __syncthreads();
+    grid_dependency_wait();                            // (as above)
     const int bad = *sbad;
     if (bad && tid == 0) flag_status(p.status, bad);
     for (int i = tid; i < G * D; i += kThreads) {
@@ -175,63 +209,42 @@ __global__ void __launch_bounds__(kThreads) fp16_decode_kernel(const __grid_cons
     }
 }
 
-template <int G>
+template <int G, bool APPEND>
 cudaError_t launch_g(const DecodeParams &p, const Plan &plan, cudaStream_t s) {
     const size_t smem = (2 * kWarps * G + kWarps * G * kHeadDim) * sizeof(float) + 16;
+    auto kern = fp16_decode_kernel<G, APPEND>;
     static SmemAttr attr_state;                    // opt-in dynamic shared memory, per device
-    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(fp16_decode_kernel<G>), smem);
-        e != cudaSuccess)
+    if (cudaError_t e = ensure_smem_attr(attr_state, reinterpret_cast<const void *>(kern), smem); e != cudaSuccess)
         return e;
-    dim3 grid(static_cast<unsigned>(plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
-              static_cast<unsigned>(p.batch));
-    fp16_decode_kernel<G><<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.num_splits), static_cast<unsigned>(p.num_kv_heads),
+                       static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
 
 cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, cudaStream_t s) {
     cudaError_t e;
+    const bool app = p.kv_new != nullptr;
     switch (G) {
-        case 1: e = launch_g<1>(p, plan, s); break;
-        case 2: e = launch_g<2>(p, plan, s); break;
-        case 4: e = launch_g<4>(p, plan, s); break;
-        case 8: e = launch_g<8>(p, plan, s); break;
+        case 1: e = app ? launch_g<1, true>(p, plan, s) : launch_g<1, false>(p, plan, s); break;
+        case 2: e = app ? launch_g<2, true>(p, plan, s) : launch_g<2, false>(p, plan, s); break;
+        case 4: e = app ? launch_g<4, true>(p, plan, s) : launch_g<4, false>(p, plan, s); break;
+        case 8: e = app ? launch_g<8, true>(p, plan, s) : launch_g<8, false>(p, plan, s); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     if (plan.num_splits > 1) return launch_combine(p, p.num_kv_heads * G, s);
     return cudaSuccess;
-}
-
-// One thread per 8 bytes of a new key or value: kv_new[b][kv_head_base + h]
-// into slot (seq_lens[b] - 1) % P of page block_table[b][(seq_lens[b] - 1) / P],
-// kv head h of the fp16 pool.  A length or page outside its range sets the
-// status bit and skips the copy (the attention of that request reports it
-// too).
-__global__ void __launch_bounds__(256) append_fp16_kernel(const __grid_constant__ DecodeParams p) {
-    constexpr int D = kHeadDim, P = kPage, PER = D * 2 * 2 / 8;   // 8-byte words per (K, V) pair
-    const int b = blockIdx.y, h = blockIdx.x;
-    const int L = p.seq_lens[b];
-    if (L < 1 || L > p.max_pages * P) return;                  // an empty or bad request: nothing to append
-    const int t = L - 1;
-    const int pg = p.block_table[static_cast<size_t>(b) * p.max_pages + t / P];
-    if (pg < 0 || static_cast<int64_t>(pg) >= p.num_pages) {
-        if (threadIdx.x == 0) flag_status(p.status, AQ_DEV_BAD_PAGE);
-        return;
-    }
-    for (int i = threadIdx.x; i < PER; i += blockDim.x) {
-        const int kv = i / (PER / 2), w = i % (PER / 2);          // K then V; 8-byte word within the vector
-        const uint2 v = reinterpret_cast<const uint2 *>(p.kv_new)
-            [((static_cast<size_t>(b) * p.qo_kv_heads + p.kv_head_base + h) * 2 + kv) * (D / 4) + w];
-        reinterpret_cast<uint2 *>(const_cast<void *>(p.kv_pages))
-            [(((static_cast<size_t>(pg) * p.num_kv_heads + h) * 2 + kv) * P + t % P) * (D / 4) + w] = v;
-    }
-}
-
-cudaError_t launch_append_fp16(const DecodeParams &p, cudaStream_t s) {
-    append_fp16_kernel<<<dim3(static_cast<unsigned>(p.num_kv_heads), static_cast<unsigned>(p.batch)), 64, 0, s>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace aq

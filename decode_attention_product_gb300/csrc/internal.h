@@ -95,7 +95,6 @@ cudaError_t launch_fp16_decode(const DecodeParams &p, int G, const Plan &plan, c
 cudaError_t launch_combine(const DecodeParams &p, int num_q_heads_launch, cudaStream_t s);
 // Copy each request's new fp16 key and value (kv_new) into its page slot of an
 // fp16 cache, for this launch's kv heads.
-cudaError_t launch_append_fp16(const DecodeParams &p, cudaStream_t s);
 cudaError_t launch_encode(const EncodeParams &p, int M, cudaStream_t s);
 cudaError_t launch_to_e4m3(int64_t n, const void *src_f16, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_from_e4m3(int64_t n, const uint8_t *src, void *dst_f16, cudaStream_t s);
