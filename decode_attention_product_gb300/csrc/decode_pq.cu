@@ -82,8 +82,8 @@ struct PqCfg {
     // [C-1][INC_STRIDE] from the peers; sender src lands in slot (src - dst - 1) mod C
     static constexpr int OFF_INC = OFF_BINS + BIN_WORDS * 4;
     static constexpr int OFF_Q = OFF_INC + (C > 1 ? (C - 1) * INC_STRIDE * 4 : 0);
-    static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_m, red_l [kWarps][G]
-    static constexpr int OFF_STAT = OFF_RED + 2 * kWarps * G * 4;  // merged mst, lst [G]
+    static constexpr int OFF_RED = OFF_Q + G * D * 4;       // red_m, red_l [kWarps][G], twice (streamed shares)
+    static constexpr int OFF_STAT = OFF_RED + 4 * kWarps * G * 4;  // merged mst, lst [G]
     // new token: owned sub-vectors [2][MC][DSUB] f32, codes [2][M] int, score [G]
     static constexpr int OFF_NEW = (OFF_STAT + 2 * G * 4 + 15) / 16 * 16;
     static constexpr int OFF_KEYS = (OFF_NEW + 2 * MC * DSUB * 4 + 2 * M * 4 + G * 4 + 7) / 8 * 8;
@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     // the scores and bins the weights against the block's statistics.
     constexpr int CHUNK = TPT * S::TOK_PER_PASS;
     const int nch = (max(eS - a0, 0) + CHUNK - 1) / CHUNK;
-    float mx, lsum;
+    float mx, lsum, cfac;                              // cfac: integer bin -> weight
     auto score = [&](const Codes<M> &cw) {
         float s = 0.f;
 #pragma unroll
@@ -708,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
         }
         // lsum >= 1 whenever this CTA holds a token of head g (its max weighs 1)
         const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
+        cfac = lsum * (1.0f / 2147483648.0f);
         {
             // weight relative to mx, in bin units: sc[i] * 2^(mg - mx) * qscale
             const float rq = (mg == -INFINITY) ? 0.f : (mg == mx ? qscale : fast_exp2(mg - mx) * qscale);
@@ -771,71 +772,119 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 }
             }
         };
-        // pass 1: (max, sum) online (chunk 0 = halves 0 and 1 came with the prologue)
-        float mrun = s_new, lrun = (s_new != -INFINITY) ? 1.0f : 0.f;
+        // One pass: each half is scored, its block-wide (max, sum) per head
+        // merged over the warps (two alternating buffers, one barrier), and its
+        // weights binned at once in fixed point against a per-head frame (Mb,
+        // Sb): a bin holds sum round(2^(s - Mb) * Sb) over its tokens, Lb =
+        // sum 2^(s - Mb) over every token seen.  The frame moves only when a
+        // half would take the bins' total Lb * Sb past 2^31: then Mb becomes
+        // the running max, Sb = 2^30 / Lb, and the bins already filled are
+        // rescaled once (factor <= 1).  So no bin overflows 32 bits, the
+        // final resolution is at least 2^-31 of the weight sum (each weight
+        // rounded by half a unit, each rescale by half a unit per bin), and
+        // the codes are read once (PAM article §2.2.3 item 1: blockwise
+        // statistics merged by rescaling).  The new token's weight enters Lb
+        // (not the bins: its value bin is added after the merge).
+        float Mb = -INFINITY, Lb = 0.f, Sb = 0.f;
+        __syncthreads();                               // the new token's score in snew
+        {
+            const float sn = snew[g];
+            if (sn != -INFINITY) {
+                Mb = sn;
+                Lb = 1.f;
+                Sb = 1073741824.0f;
+            }
+        }
+        int hh = 0;                                    // halves consumed (buffer parity)
         pass([&](auto slot, int) {
             constexpr int sl = decltype(slot)::value;
             float sc[HT];
-            float mc = -INFINITY;
+            float mloc = -INFINITY;
 #pragma unroll
             for (int i = 0; i < HT; ++i)
                 if (valid & (1u << (sl * HT + i))) {
                     sc[i] = score(cc[sl * HT + i]);
-                    mc = fmaxf(mc, sc[i]);
+                    mloc = fmaxf(mloc, sc[i]);
                 }
-            if (mc > mrun) {
-                lrun = (mrun == -INFINITY) ? 0.f : lrun * fast_exp2(mrun - mc);
-                mrun = mc;
+            float mg;
+            if constexpr (G == 1) {
+                mg = warp_max_f32(mloc);
+            } else {
+                mg = mloc;
+#pragma unroll
+                for (int off = G; off < 32; off <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, off));
             }
+            float lt = 0.f;
 #pragma unroll
             for (int i = 0; i < HT; ++i)
-                if (valid & (1u << (sl * HT + i))) lrun += fast_exp2(sc[i] - mrun);
-        });
-        if (bad_pg) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
-        // (max, sum) pairs over the lanes of head g, then over the warps
-        float mt = mrun, lt = lrun;
+                if (valid & (1u << (sl * HT + i))) {
+                    sc[i] = fast_exp2(sc[i] - mg);
+                    lt += sc[i];
+                }
 #pragma unroll
-        for (int off = G; off < 32; off <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, mt, off);
-            const float l2 = __shfl_xor_sync(0xffffffffu, lt, off);
-            const float mn = fmaxf(mt, m2);
-            lt = (mt == mn ? lt : lt * fast_exp2(mt - mn)) + (m2 == mn ? l2 : l2 * fast_exp2(m2 - mn));
-            mt = mn;
-        }
-        if (lane < G) {
-            red_m[warp * G + lane] = mt;
-            red_l[warp * G + lane] = lt;
-        }
-        __syncthreads();
-        mx = red_m[g];
+            for (int off = G; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+            float *rm = red_m + (hh & 1) * 2 * kWarps * G, *rl = rm + kWarps * G;
+            if (lane < G) {
+                rm[warp * G + lane] = mg;
+                rl[warp * G + lane] = lt;
+            }
+            __syncthreads();
+            float hm = -INFINITY;
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
-        lsum = 0.f;
+            for (int w = 0; w < kWarps; ++w) hm = fmaxf(hm, rm[w * G + g]);
+            float hl = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float mw = red_m[w * G + g];
-            if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
-        }
-        const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
-        // pass 2: the halves again from the start, weights binned against the
-        // block's statistics
-        load_pids(0);
-        issue(IntC<0>{}, 0);
-        load_pids(1);
-        issue(IntC<1>{}, 1);
-        pass([&](auto slot, int) {
-            constexpr int sl = decltype(slot)::value;
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = rm[w * G + g];
+                if (mw != -INFINITY) hl += rl[w * G + g] * (mw == hm ? 1.0f : fast_exp2(mw - hm));
+            }
+            bool resc = false;
+            float f = 1.f;
+            if (hl > 0.f) {
+                if (Lb == 0.f) {                       // first weights of head g: the bins are empty
+                    Mb = hm;
+                    Lb = hl;
+                    Sb = __fdividef(1073741824.0f, hl);
+                } else {
+                    const float add = hl * fast_exp2(hm - Mb);   // this half's weight in the frame (may be inf)
+                    if ((Lb + add) * Sb <= 2147483648.0f) {
+                        Lb += add;
+                    } else {
+                        const float Mn = fmaxf(Mb, hm);
+                        const float Ln = Lb * fast_exp2(Mb - Mn) + hl * fast_exp2(hm - Mn);
+                        const float Sn = __fdividef(1073741824.0f, Ln);
+                        f = Sn / Sb * fast_exp2(Mb - Mn);
+                        Mb = Mn;
+                        Lb = Ln;
+                        Sb = Sn;
+                        resc = true;
+                    }
+                }
+            }
+            bool any = resc;
+            if constexpr (G > 1) any = __syncthreads_or(resc);
+            if (any) {
+                if (resc)                              // this thread's bins: e mod G == g
+                    for (int e = tid; e < S::BIN_WORDS; e += kThreads)
+                        ibins[e] = __float2uint_rn(static_cast<float>(ibins[e]) * f);
+                __syncthreads();
+            }
+            const float rq = (mg == -INFINITY) ? 0.f : Sb * fast_exp2(mg - Mb);
 #pragma unroll
             for (int i = 0; i < HT; ++i)
                 if (valid & (1u << (sl * HT + i))) {
                     const Codes<M> &cw = cc[sl * HT + i];
-                    const unsigned q = __float2uint_rn(fast_exp2(score(cw) - mx) * qscale);
+                    const unsigned q = __float2uint_rn(sc[i] * rq);
 #pragma unroll
                     for (int m = 0; m < M; ++m) atomicAdd(&ibins[(m * K + cw.vv(m)) * G + g], q);
                 }
+            ++hh;
         });
+        if (bad_pg) atomicOr(&sflag[0], AQ_DEV_BAD_PAGE);
+        mx = Mb;
+        lsum = Lb;
+        cfac = Lb > 0.f ? __fdividef(1.0f, Sb) : 0.f;
     }
-    const float cfac = lsum * (1.0f / 2147483648.0f);  // integer bin -> weight
     if constexpr (C > 1) fence_proxy_async_shared();  // the bins, for the bulk copies below
     __syncthreads();                                   // every atomic of this CTA is done
 
@@ -1904,7 +1953,8 @@ struct HsCfg {
     static constexpr int SB_FLOATS = MC * K * H;            // rows for one peer [MC][K][H]
     static constexpr int B_WORDS = M * K * H;               // bins of this CTA's heads [M][K][H]
     static constexpr int RB_WORDS = MC * K * H;             // bins of one source [MC][K][H]
-    static constexpr int STX = 4 * H;                       // mx, lsum, cfac, s_new of one rank's heads
+    static constexpr int STX_SENT = 4 * H + 1;              // mx, lsum, cfac, s_new of one rank's heads, its flags
+    static constexpr int STX = 4 * H + 4;                   // one rank's row (16-byte multiple: vector accesses)
     static constexpr int TT = 4;                            // tokens per thread
     static constexpr int CODE_CAP = 32768;
     static constexpr int MAX_SPLIT = (TT * kThreads < CODE_CAP / (2 * M) ? TT * kThreads : CODE_CAP / (2 * M)) / P * P;
@@ -2081,7 +2131,7 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         // from each peer: its rows of this CTA's heads, its new-key codes and
         // flag; later its bins of this CTA's subspaces and its heads' statistics
         mbar_arrive_expect_tx(&bar[4], (C - 1) * (S::SB_FLOATS + (cl_new ? MC : 0) + 1) * 4);
-        mbar_arrive_expect_tx(&bar[5], (C - 1) * (S::RB_WORDS + S::STX) * 4);
+        mbar_arrive_expect_tx(&bar[5], (C - 1) * (S::RB_WORDS + S::STX_SENT) * 4);
     }
     {
         // the split's code pages, whole page lines, into shared memory in token
@@ -2356,6 +2406,10 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
             st_async_f32(mapa_u32(smem_u32(st_own + H + tid), pr), lsum, pb);
             st_async_f32(mapa_u32(smem_u32(st_own + 2 * H + tid), pr), cf, pb);
             st_async_f32(mapa_u32(smem_u32(st_own + 3 * H + tid), pr), snv, pb);
+            // this CTA's flags as they stand after its waits for the rows and
+            // codes: bins built from data that had not landed reach the peers
+            // with the timeout bit
+            if (tid == 0) st_async_f32(mapa_u32(smem_u32(st_own + 4 * H), pr), __int_as_float(sflag[0]), pb);
         }
     }
     __syncthreads();                                   // statistics of this CTA's heads
@@ -2403,6 +2457,9 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         atomicOr(&sflag[0], AQ_DEV_TIMEOUT);
         bad_all |= AQ_DEV_TIMEOUT;
     }
+#pragma unroll
+    for (int r = 0; r < C; ++r)
+        if (r != rank) bad_all |= __float_as_int(stx[r * S::STX + 4 * H]);
     cluster_arrive_relaxed();                          // everything sent to this CTA has landed
     if (!v_wide) widen_e4m3_slice<DSUB, MC>(cbv);
     if constexpr (APPEND) {
