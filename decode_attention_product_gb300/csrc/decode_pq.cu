@@ -829,14 +829,23 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 rl[warp * G + lane] = lt;
             }
             __syncthreads();
-            float hm = -INFINITY;
+            float hm = -INFINITY, hl = 0.f;
+            if constexpr (G == 1) {
+                // lane w < kWarps takes warp w's pair; the same reduction in
+                // every warp gives every thread the same (max, sum)
+                const float mw = lane < kWarps ? rm[lane] : -INFINITY;
+                hm = warp_max_f32(mw);
+                hl = (mw != -INFINITY) ? rl[lane] * (mw == hm ? 1.0f : fast_exp2(mw - hm)) : 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) hm = fmaxf(hm, rm[w * G + g]);
-            float hl = 0.f;
+                for (int off = 16; off > 0; off >>= 1) hl += __shfl_xor_sync(0xffffffffu, hl, off);
+            } else {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = rm[w * G + g];
-                if (mw != -INFINITY) hl += rl[w * G + g] * (mw == hm ? 1.0f : fast_exp2(mw - hm));
+                for (int w = 0; w < kWarps; ++w) hm = fmaxf(hm, rm[w * G + g]);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = rm[w * G + g];
+                    if (mw != -INFINITY) hl += rl[w * G + g] * (mw == hm ? 1.0f : fast_exp2(mw - hm));
+                }
             }
             bool resc = false;
             float f = 1.f;
