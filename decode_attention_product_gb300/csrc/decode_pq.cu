@@ -697,14 +697,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
             red_l[warp * G + lane] = lt;
         }
         __syncthreads();
-        mx = red_m[g];
+        if constexpr (G == 1) {
+            // lane w < kWarps takes warp w's pair; the same reduction in every
+            // warp gives every thread the same (max, sum)
+            const float mw = lane < kWarps ? red_m[lane] : -INFINITY;
+            mx = warp_max_f32(mw);
+            lsum = (mw != -INFINITY) ? red_l[lane] * (mw == mx ? 1.0f : fast_exp2(mw - mx)) : 0.f;
     #pragma unroll
-        for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
-        lsum = 0.f;
+            for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        } else {
+            mx = red_m[g];
     #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float mw = red_m[w * G + g];
-            if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+            for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, red_m[w * G + g]);
+            lsum = 0.f;
+    #pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = red_m[w * G + g];
+                if (mw != -INFINITY) lsum += red_l[w * G + g] * (mw == mx ? 1.0f : fast_exp2(mw - mx));
+            }
         }
         // lsum >= 1 whenever this CTA holds a token of head g (its max weighs 1)
         const float qscale = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
