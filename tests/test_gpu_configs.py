@@ -8,7 +8,7 @@ The GPU runs each workload at full size, so the decode launch has the plan
 bench.py times (page1: the token-share kernel in clusters of 4; ragged: the
 token-share kernel in clusters of 2, 2048 tokens per CTA for the 4096-token
 requests; long: the token-share kernel, 2 splits of clusters of 8, each CTA
-streaming 8192 tokens in two passes, with the outlier channels; qwen_gqa: the whole-split kernel, clusters of 4 CTAs each
+streaming 8192 tokens in one pass, with the outlier channels; qwen_gqa: the whole-split kernel, clusters of 4 CTAs each
 scoring all 1000 tokens for 8 query heads).  The oracle repeats fit, encode and decode from the same raw
 vectors for a stated subset of (request, kv head) pairs -- every pair for page1
 and qwen_gqa -- and the GPU results are compared on that subset:

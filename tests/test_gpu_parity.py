@@ -91,8 +91,10 @@ CASES = [
     (1, 2, 2, 4, [9001]),                      # group 1, several chunks per CTA
     (4, 4, 4, 4, [0, 16, 15, 48]),             # empty request, page-exact lengths
     (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # Qwen-shaped GQA: 2 head sub-groups
-    (1, 2, 2, 4, [30000]),                     # one split: a CTA streams several chunks in two passes
+    (1, 2, 2, 4, [30000]),                     # one split: a CTA streams several chunks
     (1, 4, 2, 8, [20000, ]),                   # the same with M = 8, group 2
+    (1, 8, 2, 4, [12000]),                     # streamed with group 4: a fixed-point frame per head
+    (1, 16, 2, 4, [8000]),                     # streamed with group 8
 ]
 
 
@@ -413,7 +415,8 @@ STEP_CASES = [
     (4, 4, 4, 4, [16, 32, 48, 2048]),          # new token first in its page
     (8, 64, 8, 4, [300, 1, 77, 160, 999, 64, 5, 410]),   # GQA with 2 head sub-groups per kv head
     (1, 4, 4, 8, [20000]),                     # M = 8, long: clusters of 8 over several splits
-    (1, 2, 2, 4, [30001]),                     # with one split: several chunks per CTA, two passes
+    (1, 2, 2, 4, [30001]),                     # with one split: several chunks per CTA, one pass
+    (1, 8, 2, 4, [12001]),                     # the same with group 4 (per-head frames)
 ]
 
 
