@@ -12,11 +12,12 @@ import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libaqpq.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build_debug", "libaqpq.so")   # AQ_DEBUG_CHECKS build
 
 AQ_OK = 0
 STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARGUMENT", 2: "AQ_ERR_UNSUPPORTED",
                 3: "AQ_ERR_WORKSPACE_TOO_SMALL", 4: "AQ_ERR_CUDA"}
-DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_SET, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_SET, DEV_TIMEOUT, DEV_INVARIANT = 1, 2, 4, 8, 16
 STEP_OVERLAP = 1
 STEP_E4M3 = 2
 
@@ -72,12 +73,14 @@ _lock = threading.Lock()
 
 def load(path: str | None = None):
     """Load libaqpq.so (once).  Raises if it is missing.  The environment
-    variable AQPQ_LIB names another build of the library to load instead."""
+    variable AQPQ_LIB names another build of the library to load instead;
+    AQPQ_DEBUG_CHECKS=1 selects the AQ_DEBUG_CHECKS build."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or os.environ.get("AQPQ_LIB") or LIB_PATH
+        p = path or os.environ.get("AQPQ_LIB") or (
+            DEBUG_LIB_PATH if os.environ.get("AQPQ_DEBUG_CHECKS") == "1" else LIB_PATH)
         if not os.path.exists(p):
             raise RuntimeError(
                 f"libaqpq.so not found at {p}; build it with "

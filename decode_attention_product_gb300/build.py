@@ -18,6 +18,14 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libaqpq.so")
+# the same sources with AQ_DEBUG_CHECKS: internal invariants reported through
+# the device status word (AQ_DEV_INVARIANT); selected by AQPQ_DEBUG_CHECKS=1
+DEBUG_BUILD = os.path.join(HERE, "_build_debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "libaqpq.so")
+
+
+def debug_requested() -> bool:
+    return os.environ.get("AQPQ_DEBUG_CHECKS") == "1"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -40,24 +48,31 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile and link; returns the library path.  Raises on a compile error."""
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None,
+          debug: bool | None = None) -> str:
+    """Compile and link; returns the library path.  Raises on a compile error.
+    `debug` (default: AQPQ_DEBUG_CHECKS=1 in the environment) builds the
+    AQ_DEBUG_CHECKS variant into its own directory."""
+    if debug is None:
+        debug = debug_requested()
+    build_dir, lib_path = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    if not force and not needs_build(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
+    extra = ["-DAQ_DEBUG_CHECKS"] if debug else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr[-6000:]}")
@@ -67,16 +82,16 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
 
     with ThreadPoolExecutor(max_workers=jobs or min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", tmp,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

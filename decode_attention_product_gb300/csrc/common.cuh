@@ -182,6 +182,19 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Internal invariants, checked only in builds with AQ_DEBUG_CHECKS: a failed
+// one sets AQ_DEV_INVARIANT in the status word (no trap, no early exit).
+#ifdef AQ_DEBUG_CHECKS
+#define AQ_DCHECK(status, cond)                                       \
+    do {                                                              \
+        if (!(cond)) ::aq::flag_status((status), AQ_DEV_INVARIANT);   \
+    } while (0)
+#else
+#define AQ_DCHECK(status, cond) \
+    do {                        \
+    } while (0)
+#endif
+
 __device__ __forceinline__ float2 h2_to_f2(uint32_t u) {
     __half2 h = *reinterpret_cast<__half2 *>(&u);
     return __half22float2(h);

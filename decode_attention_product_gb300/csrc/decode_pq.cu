@@ -880,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                     }
                 }
             }
+            AQ_DCHECK(p.status, !(Lb > 0.f) || (Lb * Sb <= 2147483648.0f * 1.001f && f <= 1.0001f));
             bool any = resc;
             if constexpr (G > 1) any = __syncthreads_or(resc);
             if (any) {
@@ -906,6 +907,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
     }
     if constexpr (C > 1) fence_proxy_async_shared();  // the bins, for the bulk copies below
     __syncthreads();                                   // every atomic of this CTA is done
+#ifdef AQ_DEBUG_CHECKS
+    // every token adds the same integer weight to one bin of every subspace:
+    // the subspaces' bin sums agree (a streamed share's rescales round each
+    // bin by at most half a unit: K/2 per rescale, at most 32 of them), and
+    // stay below 2^31 + rounding
+    if (tid < M * G) {
+        const int m = tid / G, gg = tid % G;
+        unsigned long long s0 = 0, sm = 0;
+        for (int k = 0; k < K; ++k) {
+            s0 += ibins[k * G + gg];
+            sm += ibins[(m * K + k) * G + gg];
+        }
+        const unsigned long long slack = (STREAM && nch > 1) ? 16ull * K : 0ull;
+        AQ_DCHECK(p.status, sm <= s0 + slack && s0 <= sm + slack && s0 < 3ull * 1073741824ull);
+    }
+#endif
 
     // ---- bins rows (integers, one bulk copy per peer) and statistics to the
     // peers that own them; sender rank lands in slot (rank - pr - 1) mod C ----
@@ -1112,6 +1129,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<G, C>) pq_decode_kernel(c
                 const float l = lst[gg];
                 p.out[bh * D + d] = bad_all ? nan : (l > 0.f ? __fdividef(o, l) : 0.f);
             } else {
+                AQ_DCHECK(p.status, bh < static_cast<size_t>(p.batch) * Hq && split < S_);
                 p.part_o[(bh * S_ + split) * D + d] = o;
                 if (rank == 0 && dl == 0) {
                     p.part_ml[(bh * S_ + split) * 2 + 0] = bad_all ? nan : mst[gg];
@@ -2461,6 +2479,20 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
     }
     fence_proxy_async_shared();                        // the bins, for the bulk copies below
     __syncthreads();
+#ifdef AQ_DEBUG_CHECKS
+    // the bin sums of every subspace agree for each head (each token adds one
+    // weight per subspace) and stay below 2^31 + rounding
+    if (tid < M * H) {
+        const int m = tid / H, hd = tid % H;
+        unsigned long long s0 = 0, sm = 0;
+        for (int k = 0; k < K; ++k) {
+            const int w = hd ^ hs_bswz<H, S::KSQ>(k);
+            s0 += bins[k * H + w];
+            sm += bins[(m * K + k) * H + w];
+        }
+        AQ_DCHECK(p.status, sm == s0 && s0 < 3ull * 1073741824ull);
+    }
+#endif
     if (tid < C - 1) {
         // peer pr's subspaces of this CTA's bins into its slot `rank`
         const uint32_t pr = static_cast<uint32_t>(rank + tid + 1) % C;

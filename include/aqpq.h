@@ -74,6 +74,8 @@ typedef int32_t aq_status;
 #define AQ_DEV_BAD_LENGTH  2  /* seq_len < 0, > max_pages * P or > max_seq_len     */
 #define AQ_DEV_BAD_SET     4  /* req_set / token_set outside [0, num_sets)         */
 #define AQ_DEV_TIMEOUT     8  /* an asynchronous copy did not land in time         */
+#define AQ_DEV_INVARIANT  16  /* builds with AQ_DEBUG_CHECKS only: an internal
+                                 invariant of a kernel failed (never set otherwise) */
 
 typedef struct CUstream_st *aq_stream_t;   /* == cudaStream_t */
 
