@@ -2435,6 +2435,16 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
         st_own[2 * H + tid] = cf;
         qsc[tid] = lsum > 0.f ? __fdividef(2147483648.0f, lsum) : 0.f;
         const float snv = st_own[3 * H + tid];
+        // this CTA's flags as they stand after its waits for the rows and
+        // codes, with those the peers sent with their rows, go to every peer
+        // with the statistics, and every CTA of the cluster NaNs its outputs
+        // when any is set: a CTA whose wait gave up may send its bins early,
+        // into a peer's key-slice buffer still being read, so the damage is not
+        // confined to the heads of the CTA that flagged
+        int fl = sflag[0];
+#pragma unroll
+        for (int r = 0; r < C; ++r)
+            if (r != rank) fl |= pbad[r];
         const uint32_t lbar = smem_u32(&bar[5]);
 #pragma unroll
         for (int r = 1; r < C; ++r) {
@@ -2443,10 +2453,7 @@ __global__ void __launch_bounds__(kThreads, kHsMinBlocks<G / C>) pq_headsplit_ke
             st_async_f32(mapa_u32(smem_u32(st_own + H + tid), pr), lsum, pb);
             st_async_f32(mapa_u32(smem_u32(st_own + 2 * H + tid), pr), cf, pb);
             st_async_f32(mapa_u32(smem_u32(st_own + 3 * H + tid), pr), snv, pb);
-            // this CTA's flags as they stand after its waits for the rows and
-            // codes: bins built from data that had not landed reach the peers
-            // with the timeout bit
-            if (tid == 0) st_async_f32(mapa_u32(smem_u32(st_own + 4 * H), pr), __int_as_float(sflag[0]), pb);
+            if (tid == 0) st_async_f32(mapa_u32(smem_u32(st_own + 4 * H), pr), __int_as_float(fl), pb);
         }
     }
     __syncthreads();                                   // statistics of this CTA's heads
