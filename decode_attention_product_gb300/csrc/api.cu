@@ -526,7 +526,7 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
                              const int32_t *req_set, const int32_t *block_table, int32_t max_pages,
                              const int32_t *seq_lens, int32_t max_seq_len, float scale,
                              int32_t num_splits, float *out, void *ws, size_t ws_bytes,
-                             int32_t *device_status, aq_stream_t stream) {
+                             int32_t *device_status, aq_stream_t stream, bool check_only = false) {
     aq_status st = check_decode_common(cfg, !fp16, batch, Hq, Hkv, max_pages, max_seq_len, num_splits);
     if (st != AQ_OK) return st;
     if (!std::isfinite(scale)) return AQ_ERR_INVALID_ARGUMENT;
@@ -546,6 +546,7 @@ static aq_status decode_impl(const aq_pq_config *cfg, bool fp16, int32_t batch, 
                    (flags & AQ_STEP_E4M3) != 0);
     if (st != AQ_OK) return st;
     if (pl.workspace > 0 && (!ws || ws_bytes < pl.workspace)) return AQ_ERR_WORKSPACE_TOO_SMALL;
+    if (check_only) return AQ_OK;
     DecodeParams p{};
     // a TMA view of the codebooks (fp16 or E4M3) for the kernels' slice copies
     p.cb_map_ok = !fp16 && codebook_tensor_map(&p.cb_map, codebooks, num_sets, Hkv, cfg->num_subspaces,
@@ -637,23 +638,30 @@ aq_status aq_decode_step_host(const aq_pq_config *cfg, int32_t batch, int32_t nu
                               void *staging, size_t staging_bytes, void *workspace, size_t workspace_bytes,
                               int32_t *device_status, aq_stream_t stream) {
     if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1) return AQ_ERR_INVALID_ARGUMENT;
-    if (batch == 0) return AQ_OK;
-    if (!q_host || !kv_new_host || !out_host || !staging) return AQ_ERR_INVALID_ARGUMENT;
+    if (batch > 0 && (!q_host || !kv_new_host || !out_host || !staging)) return AQ_ERR_INVALID_ARGUMENT;
     if (misaligned(staging)) return AQ_ERR_INVALID_ARGUMENT;
     if (staging_bytes < aq_decode_step_host_staging(batch, num_q_heads, num_kv_heads))
         return AQ_ERR_WORKSPACE_TOO_SMALL;
+    if (flags & ~(AQ_STEP_OVERLAP | AQ_STEP_E4M3)) return AQ_ERR_INVALID_ARGUMENT;
     const size_t qb = static_cast<size_t>(batch) * num_q_heads * kHeadDim * sizeof(float);
     const size_t kvb = static_cast<size_t>(batch) * num_kv_heads * 2 * kHeadDim * 2;
     unsigned char *st = static_cast<unsigned char *>(staging);
     float *q_d = reinterpret_cast<float *>(st);
     void *kv_d = st + (qb + 255) / 256 * 256;
     float *out_d = reinterpret_cast<float *>(st + (qb + 255) / 256 * 256 + (kvb + 255) / 256 * 256);
+    // every argument of the step is checked before anything is enqueued, so a
+    // rejected call leaves the stream and the staging buffer untouched
+    const aq_status chk = decode_impl(cfg, false, batch, num_q_heads, num_kv_heads, q_d, code_pages, nullptr, kv_d,
+                                      code_pages, flags & ~AQ_STEP_OVERLAP, num_pages, codebooks_f16, num_sets,
+                                      req_set, block_table, max_pages, seq_lens, max_seq_len, scale, num_splits,
+                                      out_d, workspace, workspace_bytes, device_status, stream, true);
+    if (chk != AQ_OK || batch == 0) return chk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // page-locked buffers the device can reach: the inputs by a gather kernel,
     // the output written by the step straight into host memory
     void *q_m = misaligned(q_host) ? nullptr : mapped_host(q_host);
     void *kv_m = q_m && !misaligned(kv_new_host) ? mapped_host(kv_new_host) : nullptr;
-    void *out_m = kv_m ? mapped_host(out_host) : nullptr;
+    void *out_m = kv_m && !misaligned(out_host) ? mapped_host(out_host) : nullptr;
     if (out_m) {
         const size_t nq = qb / 16, nkv = kvb / 16;
         size_t blocks = (nq + nkv + 255) / 256;
@@ -715,12 +723,18 @@ static aq_status mixed_plans(const aq_pq_config *cfg, int32_t batch, int32_t Hq,
         aq_status st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs,
                                  kPlanSmemCap, ppq, e4m3);
         if (st != AQ_OK) return st;
-        // the workspace covers either PQ kernel (the format is not known to the size query)
-        Plan other{};
+        // the workspace covers the plan of either codebook format (the size
+        // query does not know the format) and the token-share plan that
+        // replaces the head-split one when the codebooks get no TMA view
+        Plan other{}, share{};
         st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
                        &other, !e4m3);
         if (st != AQ_OK) return st;
-        const int s = ppq->num_splits > other.num_splits ? ppq->num_splits : other.num_splits;
+        st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
+                       &share, true, false);
+        if (st != AQ_OK) return st;
+        int s = ppq->num_splits > other.num_splits ? ppq->num_splits : other.num_splits;
+        if (share.num_splits > s) s = share.num_splits;
         *ws += part_bytes(batch, Hq, s);
     }
     return AQ_OK;
@@ -807,7 +821,7 @@ aq_status aq_decode_step_mixed(const aq_pq_config *cfg, int32_t batch, int32_t n
             st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
                            &ppq, true, false);
             if (st != AQ_OK) return st;
-            p.num_splits = ppq.num_splits;
+            p.num_splits = ppq.num_splits;                 // within the workspace: mixed_plans covers this plan
             p.split_len = ppq.split_len;
             p.share = ppq.share;
         }

@@ -327,13 +327,15 @@ aq_status aq_decode_step(const aq_pq_config *cfg, int32_t batch,
  * the transfer of the output into out_host [B][Hq][D] fp32.  Returns once they
  * are enqueued; out_host holds the step's output when the stream has passed
  * this point.  When all three buffers are page-locked host memory the device
- * can address (cudaHostAlloc / cudaMallocHost / cudaHostRegister) and q_host
- * and kv_new_host are 16-byte aligned, a gather kernel reads the inputs over
+ * can address (cudaHostAlloc / cudaMallocHost / cudaHostRegister) and all
+ * three are 16-byte aligned, a gather kernel reads the inputs over
  * the host link into `staging`, the step starts as its programmatic dependent
  * and writes its output directly into out_host (no DMA copies); otherwise the
  * inputs and the output move by cudaMemcpyAsync (pageable buffers make those
  * copies synchronous).  Either way the host must not rewrite the inputs or
- * read the output until the stream has passed the step.
+ * read the output until the stream has passed the step.  Every argument, the
+ * step's included, is checked before anything is enqueued: a call that
+ * returns an error has enqueued nothing and left `staging` untouched.
  *   staging        device memory of >= aq_decode_step_host_staging() bytes,
  *                  16-byte aligned, owned by the caller (no allocation here)
  *   flags          AQ_STEP_E4M3 only (AQ_STEP_OVERLAP is ignored: the step

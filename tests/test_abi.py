@@ -136,6 +136,36 @@ def test_decode_step_flags_checked(lib):
     assert step(2, kv_new=None) == 1                    # a step needs its new token
 
 
+def test_decode_step_host_argument_checks(lib):
+    """The host-buffer step checks every argument (its own and the step's)
+    before it enqueues a transfer or a kernel: without a GPU each rejected call
+    returns its argument error, never a CUDA one."""
+    cfg = _cfg()
+    B, Hq, Hkv = 2, 4, 4
+    need = lib.aq_decode_step_host_staging(B, Hq, Hkv)
+    assert need >= B * Hq * 128 * 4 * 2 + B * Hkv * 2 * 128 * 2
+
+    def step(c=cfg, batch=B, Hq=Hq, q=FAKE, staging=FAKE, sbytes=None, flags=0, scale=0.1, splits=0,
+             max_seq_len=100):
+        if sbytes is None:
+            sbytes = lib.aq_decode_step_host_staging(batch, Hq, Hkv)
+        return lib.aq_decode_step_host(ctypes.byref(c) if c is not None else None, batch, Hq, Hkv, q, FAKE, FAKE,
+                                       64, FAKE, 4, FAKE, FAKE, 8, FAKE, max_seq_len, scale, splits, flags, FAKE,
+                                       staging, sbytes, None, 0, None, None)
+    assert step(q=None) == 1                            # host query missing
+    assert step(staging=None) == 1
+    assert step(staging=ctypes.c_void_p(0x10008)) == 1  # staging not 16-byte aligned
+    assert step(sbytes=need - 1) == 3                   # staging too small
+    assert step(flags=4) == 1                           # unknown flag
+    assert step(c=None) == 1                            # the step's own checks, before any transfer
+    assert step(c=_cfg(M=16)) == 2
+    assert step(Hq=6) == 1
+    assert step(scale=float("nan")) == 1
+    assert step(splits=3) == 3                          # forced splits need a workspace
+    assert step(c=None, batch=0) == 1                   # an empty batch still needs a valid config
+    assert step(batch=0, q=None, staging=None, sbytes=0) == 0   # nothing to do
+
+
 def test_e4m3_conversion_argument_checks(lib):
     assert lib.aq_codebooks_to_e4m3(-1, FAKE, FAKE, None) == 1
     assert lib.aq_codebooks_to_e4m3(0, None, None, None) == 0
@@ -186,3 +216,23 @@ def test_every_supported_shape_has_a_plan(lib):
                 assert w >= (2 * 4 * G * s * 130 * 4 if s > 1 else 0)
                 if L == 131072:
                     assert w > 0
+
+
+def test_mixed_workspace_covers_every_pq_plan(lib):
+    """The mixed step's workspace holds the fp16 part's split partials and the
+    PQ part's for any plan that part can take: either codebook format, and the
+    token-share plan that replaces the head-split one when the codebooks get no
+    TMA view.  aq_decode_plan's workspace for the PQ heads alone covers those
+    plans (B * Hq_pq * S * (D + 2) floats); the mixed step indexes partials by
+    the full query-head numbering, so it needs the same S over all Hq heads."""
+    for (B, Hq, Hkv, n16, L, M) in [(1, 64, 8, 2, 131072, 4), (1, 64, 8, 2, 131072, 8), (2, 32, 8, 4, 20000, 4),
+                                    (1, 32, 32, 4, 131072, 8), (4, 32, 32, 4, 2048, 4), (8, 64, 8, 1, 1000, 4)]:
+        cfg = _cfg(M=M)
+        ws = ctypes.c_size_t()
+        assert lib.aq_decode_step_mixed_workspace(ctypes.byref(cfg), B, Hq, Hkv, n16, L, ctypes.byref(ws)) == 0
+        G = Hq // Hkv
+        s16, _, _ = _plan(lib, B, n16 * G, n16, L, M=M, fp16=1)
+        _, _, wpq = _plan(lib, B, (Hkv - n16) * G, Hkv - n16, L, M=M)
+        spq = wpq // (B * (Hkv - n16) * G * 130 * 4)
+        need = (B * Hq * s16 * 130 * 4 if s16 > 1 else 0) + (B * Hq * spq * 130 * 4 if spq > 1 else 0)
+        assert ws.value >= need, (B, Hq, Hkv, n16, L, M, ws.value, need)
