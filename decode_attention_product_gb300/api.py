@@ -21,8 +21,16 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _stream():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _same_device(ref, **tensors):
+    """Every given tensor on ref's device (the library launches on the current
+    device, which each wrapper sets to that one for the call)."""
+    for name, t in tensors.items():
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device}, the call's other tensors on {ref.device}")
 
 
 def _need(t, dtype, name, ndim=None):
@@ -53,8 +61,9 @@ def fit_codebooks(samples: torch.Tensor, num_subspaces: int, iters: int = 10,
     cb = torch.empty((U, M, CODEWORDS, D // M), dtype=torch.float16, device=samples.device)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
     cfg = _lib.config(M, head_dim=D)
-    st = _lib.load().aq_fit_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(cb),
-                                      _ptr(asg), _stream())
+    with torch.cuda.device(samples.device):
+        st = _lib.load().aq_fit_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(cb),
+                                          _ptr(asg), _stream(samples.device))
     _lib.check(st, "aq_fit_codebooks")
     return (cb, asg) if with_assign else cb
 
@@ -70,10 +79,12 @@ def refine_codebooks(samples: torch.Tensor, codebooks: torch.Tensor, iters: int 
     M = codebooks.shape[1]
     if codebooks.shape[0] != U:
         raise ValueError("one codebook per sample unit")
+    _same_device(samples, codebooks=codebooks)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
     cfg = _lib.config(M, head_dim=D)
-    st = _lib.load().aq_refine_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(codebooks),
-                                         _ptr(asg), _stream())
+    with torch.cuda.device(samples.device):
+        st = _lib.load().aq_refine_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(codebooks),
+                                             _ptr(asg), _stream(samples.device))
     _lib.check(st, "aq_refine_codebooks")
     return asg
 
@@ -83,7 +94,8 @@ def to_e4m3(x: torch.Tensor) -> torch.Tensor:
     even, saturating)."""
     _need(x, torch.float16, "x")
     out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    st = _lib.load().aq_codebooks_to_e4m3(x.numel(), _ptr(x), _ptr(out), _stream())
+    with torch.cuda.device(x.device):
+        st = _lib.load().aq_codebooks_to_e4m3(x.numel(), _ptr(x), _ptr(out), _stream(x.device))
     _lib.check(st, "aq_codebooks_to_e4m3")
     return out
 
@@ -92,7 +104,8 @@ def from_e4m3(codes: torch.Tensor) -> torch.Tensor:
     """The exact fp16 values (same shape) of FP8 E4M3 codes."""
     _need(codes, torch.uint8, "codes")
     out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device)
-    st = _lib.load().aq_codebooks_from_e4m3(codes.numel(), _ptr(codes), _ptr(out), _stream())
+    with torch.cuda.device(codes.device):
+        st = _lib.load().aq_codebooks_from_e4m3(codes.numel(), _ptr(codes), _ptr(out), _stream(codes.device))
     _lib.check(st, "aq_codebooks_from_e4m3")
     return out
 
@@ -103,11 +116,13 @@ def kmeans_step(samples: torch.Tensor, centroids: torch.Tensor):
     _need(centroids, torch.float32, "centroids", 4)
     U, N, D = samples.shape
     M = centroids.shape[1]
+    _same_device(samples, centroids=centroids)
     out = torch.empty_like(centroids)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device)
     cfg = _lib.config(M, head_dim=D)
-    st = _lib.load().aq_kmeans_step(ctypes.byref(cfg), U, N, _ptr(samples), _ptr(centroids),
-                                    _ptr(out), _ptr(asg), _stream())
+    with torch.cuda.device(samples.device):
+        st = _lib.load().aq_kmeans_step(ctypes.byref(cfg), U, N, _ptr(samples), _ptr(centroids),
+                                        _ptr(out), _ptr(asg), _stream(samples.device))
     _lib.check(st, "aq_kmeans_step")
     return out, asg
 
@@ -123,10 +138,13 @@ def encode_append(kv: torch.Tensor, token_set: torch.Tensor, slot_mapping: torch
     _need(code_pages, torch.uint8, "code_pages", 5)
     T, Hkv, _, D = kv.shape
     M = codebooks.shape[3]
+    _same_device(kv, token_set=token_set, slot_mapping=slot_mapping, codebooks=codebooks,
+                 code_pages=code_pages, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    st = _lib.load().aq_encode_append(
-        ctypes.byref(cfg), T, Hkv, _ptr(kv), _ptr(token_set), _ptr(slot_mapping), _ptr(codebooks),
-        codebooks.shape[0], _ptr(code_pages), code_pages.shape[0], _ptr(status), _stream())
+    with torch.cuda.device(kv.device):
+        st = _lib.load().aq_encode_append(
+            ctypes.byref(cfg), T, Hkv, _ptr(kv), _ptr(token_set), _ptr(slot_mapping), _ptr(codebooks),
+            codebooks.shape[0], _ptr(code_pages), code_pages.shape[0], _ptr(status), _stream(kv.device))
     _lib.check(st, "aq_encode_append")
 
 
@@ -170,12 +188,15 @@ def decode_attention(q: torch.Tensor, code_pages: torch.Tensor, codebooks: torch
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
+    _same_device(q, code_pages=code_pages, codebooks=codebooks, req_set=req_set, block_table=block_table,
+                 seq_lens=seq_lens, out=out, workspace=workspace, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    st = _lib.load().aq_decode_attention(
-        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(code_pages), code_pages.shape[0],
-        _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), max_seq_len, float(scale), num_splits, _ptr(out), _ptr(workspace),
-        workspace.numel() if workspace is not None else 0, _ptr(status), _stream())
+    with torch.cuda.device(q.device):
+        st = _lib.load().aq_decode_attention(
+            ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(code_pages), code_pages.shape[0],
+            _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), max_seq_len, float(scale), num_splits, _ptr(out), _ptr(workspace),
+            workspace.numel() if workspace is not None else 0, _ptr(status), _stream(q.device))
     _lib.check(st, "aq_decode_attention")
     return out
 
@@ -206,14 +227,17 @@ def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
+    _same_device(q, kv_new=kv_new, code_pages=code_pages, codebooks=codebooks, req_set=req_set,
+                 block_table=block_table, seq_lens=seq_lens, out=out, workspace=workspace, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    st = _lib.load().aq_decode_step(
-        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_new), _ptr(code_pages), code_pages.shape[0],
-        _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), max_seq_len, float(scale), num_splits,
-        (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0),
-        _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status),
-        _stream())
+    with torch.cuda.device(q.device):
+        st = _lib.load().aq_decode_step(
+            ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_new), _ptr(code_pages), code_pages.shape[0],
+            _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), max_seq_len, float(scale), num_splits,
+            (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0),
+            _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status),
+            _stream(q.device))
     _lib.check(st, "aq_decode_step")
     return out
 
@@ -256,14 +280,18 @@ def decode_step_mixed(q: torch.Tensor, kv_new: torch.Tensor, num_fp16_heads: int
                                                         ctypes.byref(w))
         _lib.check(st, "aq_decode_step_mixed_workspace")
         workspace = torch.empty(w.value, dtype=torch.uint8, device=q.device) if w.value else None
-    st = _lib.load().aq_decode_step_mixed(
-        ctypes.byref(cfg), B, Hq, Hkv, n16, _ptr(q), _ptr(kv_new), _ptr(kv_pages_f16),
-        kv_pages_f16.shape[0] if kv_pages_f16 is not None else 0, _ptr(code_pages),
-        code_pages.shape[0] if code_pages is not None else 0, _ptr(codebooks),
-        codebooks.shape[0] if codebooks is not None else 0, _ptr(req_set), _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
-        (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0), _ptr(out),
-        _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status), _stream())
+    _same_device(q, kv_new=kv_new, kv_pages_f16=kv_pages_f16, code_pages=code_pages, codebooks=codebooks,
+                 req_set=req_set, block_table=block_table, seq_lens=seq_lens, out=out, workspace=workspace,
+                 status=status)
+    with torch.cuda.device(q.device):
+        st = _lib.load().aq_decode_step_mixed(
+            ctypes.byref(cfg), B, Hq, Hkv, n16, _ptr(q), _ptr(kv_new), _ptr(kv_pages_f16),
+            kv_pages_f16.shape[0] if kv_pages_f16 is not None else 0, _ptr(code_pages),
+            code_pages.shape[0] if code_pages is not None else 0, _ptr(codebooks),
+            codebooks.shape[0] if codebooks is not None else 0, _ptr(req_set), _ptr(block_table),
+            block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
+            (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0), _ptr(out),
+            _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status), _stream(q.device))
     _lib.check(st, "aq_decode_step_mixed")
     return out
 
@@ -286,12 +314,15 @@ def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: 
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, 4, num_splits, fp16=True, device=q.device)
+    _same_device(q, kv_pages=kv_pages, block_table=block_table, seq_lens=seq_lens, out=out,
+                 workspace=workspace, status=status)
     cfg = _lib.config(4, head_dim=D, page_size=kv_pages.shape[3])
-    st = _lib.load().aq_decode_attention_fp16(
-        ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_pages), kv_pages.shape[0],
-        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
-        num_splits, _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
-        _ptr(status), _stream())
+    with torch.cuda.device(q.device):
+        st = _lib.load().aq_decode_attention_fp16(
+            ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_pages), kv_pages.shape[0],
+            _ptr(block_table), block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
+            num_splits, _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+            _ptr(status), _stream(q.device))
     _lib.check(st, "aq_decode_attention_fp16")
     return out
 
@@ -423,7 +454,8 @@ class HostDecodeStep:
     `q_host`, `kv_host`, `out_host` are the pinned tensors (write the next
     step's inputs into the first two, read the output from the last one after
     `sync()`); `launch()` enqueues one step.  The call's arguments are
-    marshalled once, here.
+    marshalled once, here; `launch()` itself does no device switch, so the
+    cache's device must be the current one when it is called.
     """
 
     def __init__(self, code_pages, codebooks, req_set, block_table, seq_lens, max_seq_len,
@@ -437,7 +469,9 @@ class HostDecodeStep:
         self.B, self.Hq = int(seq_lens.shape[0]), int(num_q_heads)
         self.Hkv, self.M = int(codebooks.shape[1]), int(codebooks.shape[3])
         dev = code_pages.device
-        self.stream = stream or torch.cuda.current_stream()
+        _same_device(code_pages, codebooks=codebooks, req_set=req_set, block_table=block_table,
+                     seq_lens=seq_lens)
+        self.stream = stream or torch.cuda.current_stream(dev)
         self.q_host = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32).pin_memory()
         self.kv_host = torch.empty((self.B, self.Hkv, 2, HEAD_DIM), dtype=torch.float16).pin_memory()
         self.out_host = torch.empty((self.B, self.Hq, HEAD_DIM), dtype=torch.float32).pin_memory()

@@ -236,3 +236,15 @@ def test_mixed_workspace_covers_every_pq_plan(lib):
         spq = wpq // (B * (Hkv - n16) * G * 130 * 4)
         need = (B * Hq * s16 * 130 * 4 if s16 > 1 else 0) + (B * Hq * spq * 130 * 4 if spq > 1 else 0)
         assert ws.value >= need, (B, Hq, Hkv, n16, L, M, ws.value, need)
+
+
+def test_wrappers_reject_tensors_on_another_device():
+    """The torch wrappers run the C call with the tensors' device current and
+    refuse a call whose tensors sit on different devices (checked without a
+    GPU on a CPU and a meta tensor)."""
+    torch = pytest.importorskip("torch")
+    from decode_attention_product_gb300 import api
+    a, b = torch.zeros(4), torch.zeros(4, device="meta")
+    api._same_device(a, x=torch.zeros(2), y=None)
+    with pytest.raises(ValueError, match="meta"):
+        api._same_device(a, codebooks=b)
