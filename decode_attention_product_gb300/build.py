@@ -6,6 +6,7 @@ Rebuilds only when a source or header is newer than the library.
 """
 from __future__ import annotations
 
+import fcntl
 import glob
 import os
 import shutil
@@ -66,6 +67,23 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None,
     if not force and not needs_build(lib_path):
         return lib_path
     os.makedirs(build_dir, exist_ok=True)
+    # one build at a time per directory (parallel test workers, a child
+    # process building while its parent runs): the others wait, then find the
+    # library current
+    with open(os.path.join(build_dir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not needs_build(lib_path):
+                return lib_path
+            _compile_and_link(build_dir, lib_path, debug, jobs)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+    if verbose:
+        print("built", lib_path)
+    return lib_path
+
+
+def _compile_and_link(build_dir: str, lib_path: str, debug: bool, jobs: int | None) -> None:
     nvcc = _nvcc()
     srcs = _sources()
     extra = ["-DAQ_DEBUG_CHECKS"] if debug else []
@@ -89,9 +107,6 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None,
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
     os.replace(tmp, lib_path)
-    if verbose:
-        print("built", lib_path)
-    return lib_path
 
 
 if __name__ == "__main__":

@@ -51,14 +51,17 @@ def build(force: bool = False) -> str:
     if (not force and os.path.exists(_SO)
             and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
         return _SO
+    # a temporary of this process's own, renamed into place at once: builds
+    # in parallel processes never write the same file
+    tmp = f"{_SO}.{os.getpid()}.tmp"
     base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-            _SRC, "-o", _SO + ".tmp", "-lm"]
+            _SRC, "-o", tmp, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(_SO + ".tmp", _SO)
+    os.replace(tmp, _SO)
     return _SO
 
 
