@@ -25,12 +25,15 @@ def _stream(device=None):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _same_device(ref, **tensors):
-    """Every given tensor on ref's device (the library launches on the current
-    device, which each wrapper sets to that one for the call)."""
+def _same_device(ref, **tensors) -> int:
+    """ref's device index, once every given tensor is on that device (the
+    library launches on the current device, which each wrapper sets to this
+    one for the call)."""
+    d = ref.get_device()
     for name, t in tensors.items():
-        if t is not None and t.device != ref.device:
+        if t is not None and t.get_device() != d:
             raise ValueError(f"{name} is on {t.device}, the call's other tensors on {ref.device}")
+    return d
 
 
 def _need(t, dtype, name, ndim=None):
@@ -61,9 +64,10 @@ def fit_codebooks(samples: torch.Tensor, num_subspaces: int, iters: int = 10,
     cb = torch.empty((U, M, CODEWORDS, D // M), dtype=torch.float16, device=samples.device)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
     cfg = _lib.config(M, head_dim=D)
-    with torch.cuda.device(samples.device):
+    dev = samples.get_device()
+    with torch.cuda.device(dev):
         st = _lib.load().aq_fit_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(cb),
-                                          _ptr(asg), _stream(samples.device))
+                                          _ptr(asg), _stream(dev))
     _lib.check(st, "aq_fit_codebooks")
     return (cb, asg) if with_assign else cb
 
@@ -79,12 +83,12 @@ def refine_codebooks(samples: torch.Tensor, codebooks: torch.Tensor, iters: int 
     M = codebooks.shape[1]
     if codebooks.shape[0] != U:
         raise ValueError("one codebook per sample unit")
-    _same_device(samples, codebooks=codebooks)
+    dev = _same_device(samples, codebooks=codebooks)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device) if with_assign else None
     cfg = _lib.config(M, head_dim=D)
-    with torch.cuda.device(samples.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_refine_codebooks(ctypes.byref(cfg), U, N, iters, _ptr(samples), _ptr(codebooks),
-                                             _ptr(asg), _stream(samples.device))
+                                             _ptr(asg), _stream(dev))
     _lib.check(st, "aq_refine_codebooks")
     return asg
 
@@ -94,8 +98,9 @@ def to_e4m3(x: torch.Tensor) -> torch.Tensor:
     even, saturating)."""
     _need(x, torch.float16, "x")
     out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    with torch.cuda.device(x.device):
-        st = _lib.load().aq_codebooks_to_e4m3(x.numel(), _ptr(x), _ptr(out), _stream(x.device))
+    dev = x.get_device()
+    with torch.cuda.device(dev):
+        st = _lib.load().aq_codebooks_to_e4m3(x.numel(), _ptr(x), _ptr(out), _stream(dev))
     _lib.check(st, "aq_codebooks_to_e4m3")
     return out
 
@@ -104,8 +109,9 @@ def from_e4m3(codes: torch.Tensor) -> torch.Tensor:
     """The exact fp16 values (same shape) of FP8 E4M3 codes."""
     _need(codes, torch.uint8, "codes")
     out = torch.empty(codes.shape, dtype=torch.float16, device=codes.device)
-    with torch.cuda.device(codes.device):
-        st = _lib.load().aq_codebooks_from_e4m3(codes.numel(), _ptr(codes), _ptr(out), _stream(codes.device))
+    dev = codes.get_device()
+    with torch.cuda.device(dev):
+        st = _lib.load().aq_codebooks_from_e4m3(codes.numel(), _ptr(codes), _ptr(out), _stream(dev))
     _lib.check(st, "aq_codebooks_from_e4m3")
     return out
 
@@ -116,13 +122,13 @@ def kmeans_step(samples: torch.Tensor, centroids: torch.Tensor):
     _need(centroids, torch.float32, "centroids", 4)
     U, N, D = samples.shape
     M = centroids.shape[1]
-    _same_device(samples, centroids=centroids)
+    dev = _same_device(samples, centroids=centroids)
     out = torch.empty_like(centroids)
     asg = torch.empty((U, N, M), dtype=torch.int32, device=samples.device)
     cfg = _lib.config(M, head_dim=D)
-    with torch.cuda.device(samples.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_kmeans_step(ctypes.byref(cfg), U, N, _ptr(samples), _ptr(centroids),
-                                        _ptr(out), _ptr(asg), _stream(samples.device))
+                                        _ptr(out), _ptr(asg), _stream(dev))
     _lib.check(st, "aq_kmeans_step")
     return out, asg
 
@@ -138,13 +144,13 @@ def encode_append(kv: torch.Tensor, token_set: torch.Tensor, slot_mapping: torch
     _need(code_pages, torch.uint8, "code_pages", 5)
     T, Hkv, _, D = kv.shape
     M = codebooks.shape[3]
-    _same_device(kv, token_set=token_set, slot_mapping=slot_mapping, codebooks=codebooks,
+    dev = _same_device(kv, token_set=token_set, slot_mapping=slot_mapping, codebooks=codebooks,
                  code_pages=code_pages, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    with torch.cuda.device(kv.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_encode_append(
             ctypes.byref(cfg), T, Hkv, _ptr(kv), _ptr(token_set), _ptr(slot_mapping), _ptr(codebooks),
-            codebooks.shape[0], _ptr(code_pages), code_pages.shape[0], _ptr(status), _stream(kv.device))
+            codebooks.shape[0], _ptr(code_pages), code_pages.shape[0], _ptr(status), _stream(dev))
     _lib.check(st, "aq_encode_append")
 
 
@@ -188,15 +194,15 @@ def decode_attention(q: torch.Tensor, code_pages: torch.Tensor, codebooks: torch
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
-    _same_device(q, code_pages=code_pages, codebooks=codebooks, req_set=req_set, block_table=block_table,
+    dev = _same_device(q, code_pages=code_pages, codebooks=codebooks, req_set=req_set, block_table=block_table,
                  seq_lens=seq_lens, out=out, workspace=workspace, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    with torch.cuda.device(q.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_decode_attention(
             ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(code_pages), code_pages.shape[0],
             _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
             _ptr(seq_lens), max_seq_len, float(scale), num_splits, _ptr(out), _ptr(workspace),
-            workspace.numel() if workspace is not None else 0, _ptr(status), _stream(q.device))
+            workspace.numel() if workspace is not None else 0, _ptr(status), _stream(dev))
     _lib.check(st, "aq_decode_attention")
     return out
 
@@ -227,17 +233,17 @@ def decode_step(q: torch.Tensor, kv_new: torch.Tensor, code_pages: torch.Tensor,
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, M, num_splits, device=q.device)
-    _same_device(q, kv_new=kv_new, code_pages=code_pages, codebooks=codebooks, req_set=req_set,
+    dev = _same_device(q, kv_new=kv_new, code_pages=code_pages, codebooks=codebooks, req_set=req_set,
                  block_table=block_table, seq_lens=seq_lens, out=out, workspace=workspace, status=status)
     cfg = _lib.config(M, head_dim=D, page_size=code_pages.shape[2])
-    with torch.cuda.device(q.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_decode_step(
             ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_new), _ptr(code_pages), code_pages.shape[0],
             _ptr(codebooks), codebooks.shape[0], _ptr(req_set), _ptr(block_table), block_table.shape[1],
             _ptr(seq_lens), max_seq_len, float(scale), num_splits,
             (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0),
             _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status),
-            _stream(q.device))
+            _stream(dev))
     _lib.check(st, "aq_decode_step")
     return out
 
@@ -280,10 +286,10 @@ def decode_step_mixed(q: torch.Tensor, kv_new: torch.Tensor, num_fp16_heads: int
                                                         ctypes.byref(w))
         _lib.check(st, "aq_decode_step_mixed_workspace")
         workspace = torch.empty(w.value, dtype=torch.uint8, device=q.device) if w.value else None
-    _same_device(q, kv_new=kv_new, kv_pages_f16=kv_pages_f16, code_pages=code_pages, codebooks=codebooks,
+    dev = _same_device(q, kv_new=kv_new, kv_pages_f16=kv_pages_f16, code_pages=code_pages, codebooks=codebooks,
                  req_set=req_set, block_table=block_table, seq_lens=seq_lens, out=out, workspace=workspace,
                  status=status)
-    with torch.cuda.device(q.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_decode_step_mixed(
             ctypes.byref(cfg), B, Hq, Hkv, n16, _ptr(q), _ptr(kv_new), _ptr(kv_pages_f16),
             kv_pages_f16.shape[0] if kv_pages_f16 is not None else 0, _ptr(code_pages),
@@ -291,7 +297,7 @@ def decode_step_mixed(q: torch.Tensor, kv_new: torch.Tensor, num_fp16_heads: int
             codebooks.shape[0] if codebooks is not None else 0, _ptr(req_set), _ptr(block_table),
             block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
             (_lib.STEP_OVERLAP if overlap else 0) | (_lib.STEP_E4M3 if e4m3 else 0), _ptr(out),
-            _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status), _stream(q.device))
+            _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(status), _stream(dev))
     _lib.check(st, "aq_decode_step_mixed")
     return out
 
@@ -314,15 +320,15 @@ def decode_attention_fp16(q: torch.Tensor, kv_pages: torch.Tensor, block_table: 
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, Hq, Hkv, max_seq_len, 4, num_splits, fp16=True, device=q.device)
-    _same_device(q, kv_pages=kv_pages, block_table=block_table, seq_lens=seq_lens, out=out,
+    dev = _same_device(q, kv_pages=kv_pages, block_table=block_table, seq_lens=seq_lens, out=out,
                  workspace=workspace, status=status)
     cfg = _lib.config(4, head_dim=D, page_size=kv_pages.shape[3])
-    with torch.cuda.device(q.device):
+    with torch.cuda.device(dev):
         st = _lib.load().aq_decode_attention_fp16(
             ctypes.byref(cfg), B, Hq, Hkv, _ptr(q), _ptr(kv_pages), kv_pages.shape[0],
             _ptr(block_table), block_table.shape[1], _ptr(seq_lens), max_seq_len, float(scale),
             num_splits, _ptr(out), _ptr(workspace), workspace.numel() if workspace is not None else 0,
-            _ptr(status), _stream(q.device))
+            _ptr(status), _stream(dev))
     _lib.check(st, "aq_decode_attention_fp16")
     return out
 

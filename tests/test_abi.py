@@ -241,10 +241,16 @@ def test_mixed_workspace_covers_every_pq_plan(lib):
 def test_wrappers_reject_tensors_on_another_device():
     """The torch wrappers run the C call with the tensors' device current and
     refuse a call whose tensors sit on different devices (checked without a
-    GPU on a CPU and a meta tensor)."""
+    GPU: CPU tensors report device index -1, the stand-in reports device 1)."""
     torch = pytest.importorskip("torch")
     from decode_attention_product_gb300 import api
-    a, b = torch.zeros(4), torch.zeros(4, device="meta")
-    api._same_device(a, x=torch.zeros(2), y=None)
-    with pytest.raises(ValueError, match="meta"):
-        api._same_device(a, codebooks=b)
+
+    class OnDevice1:
+        device = "cuda:1"
+
+        def get_device(self):
+            return 1
+    a = torch.zeros(4)
+    assert api._same_device(a, x=torch.zeros(2), y=None) == -1
+    with pytest.raises(ValueError, match="cuda:1"):
+        api._same_device(a, codebooks=OnDevice1())
