@@ -278,7 +278,8 @@ def run_reference(args, w, rank, world):
         return
     ost = OracleStep(w)
     # each step a bounded sample, the whole run within about two minutes
-    budget = min(4.0, 120.0 / (args.steps + args.warmup))
+    # (--cpu-budget caps a step's sample too: short runs for tests)
+    budget = min(4.0, 120.0 / (args.steps + args.warmup), args.cpu_budget)
     units = secs = n_tot = 0
     for i in range(args.warmup + args.steps):
         u, s_, n = ost.run(budget)
@@ -887,7 +888,8 @@ def main():
                     help="page1 only: skip the ragged, long and qwen_gqa step objects")
     ap.add_argument("--two-call", action="store_true",
                     help="time aq_encode_append + aq_decode_attention instead of the fused step")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for cpu_baseline; also caps each step of --impl reference")
     ap.add_argument("--no-sweep", action="store_true", help="qwen_gqa: skip the 80-layer sweep")
     ap.add_argument("--min-region-ms", type=float, default=200.0,
                     help="shortest timed region (repeats of the K steps); lower only for profiler runs")

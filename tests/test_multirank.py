@@ -136,3 +136,28 @@ def test_split_kv_across_ranks_merges_to_single_pass():
     res = sorted(q.get(timeout=5) for _ in range(world))
     for rank, err in res:
         assert err < 1e-12, (rank, err)
+
+
+def test_reference_arm_prints_once_under_torchrun():
+    """bench.py --impl reference launched as the multi-GPU bench is (torchrun,
+    2 ranks on 127.0.0.1): rank 0 alone times the oracle and prints one JSON
+    line with the reference arm's keys; the other rank exits 0 without work.
+    No GPU is touched."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--workload", "tiny", "--gpus", "2", "--steps", "2", "--warmup", "3", "--cpu-budget", "0.2"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("tiny")
