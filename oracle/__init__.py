@@ -20,7 +20,11 @@ What each function computes, and the passage it follows, is stated in
 * ``decode_attention_mixed``: fp16 attention for the first kv heads, PQ for
   the rest (AQPIM blog §6.1 item 4).
 * ``kmeans_fit`` / ``kmeans_step``: Lloyd k-means codebook fit (AQPIM blog
-  §3.2 item 2, §5.2 item 1).
+  §3.2 item 2, §5.2 item 1); ``kmeans_distortion``: its objective.
+* ``kmeans_refine``: the periodic refresh, Lloyd steps on recent vectors
+  seeded from the codebook in use (AQPIM blog §6.1 item 3).
+* ``e4m3_from_float`` / ``e4m3_to_float``: FP8 E4M3 codebook storage, nearest
+  with ties to even, saturating at 448 (AQPIM blog §4.2).
 
 Floating-point inputs given as fp16 are widened exactly; results come back in
 float64 (``kmeans_fit`` also returns the fp16 round-to-nearest-even codebook).

@@ -2,7 +2,8 @@
  * aq_oracle.c -- plain, slow CPU oracle for product-quantised (PQ) KV-cache
  * decode attention.  TEST INFRASTRUCTURE ONLY: it is compiled into
  * oracle/_build/liboracle.so and may be loaded only by tests/, by
- * __graft_entry__.smoke() and by the cpu_baseline leg of bench.py.  It shares
+ * __graft_entry__.smoke() and by the cpu_baseline and --impl reference legs
+ * of bench.py.  It shares
  * no code, header, table or helper with the CUDA library.
  *
  * Sources (cited by page title and section):
