@@ -212,7 +212,10 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens,
 
 /* ---------------------------------------------------------------------------
  * aq_decode_plan -- host-only: the split count and workspace a decode call
- * with these arguments will use (no CUDA call).
+ * with these arguments will use (no CUDA call).  A split is one block of the
+ * blockwise softmax of PAM article §2.2.3: its (max, sum, output) partials go
+ * to the workspace and the combine merges them; how many blocks, and how many
+ * CTAs share one, is this library's choice for the GPU, not the page's.
  *   num_splits_req  0 = choose automatically, else the requested count
  *   *num_splits     out: splits per (request, kv head)  (may be NULL)
  *   *cluster_size   out: CTAs cooperating on one split (may be NULL)
