@@ -68,3 +68,20 @@ def test_too_few_warmup_steps_rejected():
     r = subprocess.run([sys.executable, "bench.py", "--warmup", "2", "--steps", "1"], cwd=ROOT,
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
+
+
+def test_clock_sampler_reads_what_nvidia_smi_printed(tmp_path, monkeypatch):
+    """The sampler's own path end to end, with a stand-in nvidia-smi on PATH
+    that prints two samples and then waits to be stopped."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 2070, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '0, 2055, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    s.start()
+    c = s.stop()
+    assert c == {"sm_mhz": 2062.5, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
+    assert not os.path.exists(s.path)
