@@ -40,6 +40,18 @@ def test_library_exports_every_declared_symbol(lib):
         assert getattr(lib, name) is not None
 
 
+def test_debug_checks_build_compiles_and_exports_every_symbol():
+    """The AQ_DEBUG_CHECKS variant (kernels that also check internal invariants
+    and report AQ_DEV_INVARIANT) cross-compiles for sm_103a without a GPU, into
+    its own directory, and exports the same entry points."""
+    path = B.build(debug=True)
+    assert path == B.DEBUG_LIB and path != _lib.LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (aq_[a-z0-9_]+)$", out, flags=re.M))
+    assert set(_declared()) <= exported
+
+
 def test_status_strings(lib):
     assert lib.aq_status_string(0) == b"AQ_OK"
     assert lib.aq_status_string(3) == b"AQ_ERR_WORKSPACE_TOO_SMALL"
