@@ -102,7 +102,11 @@ constexpr size_t kPlanSmemCap = 232448;
 //         keeping >= 256 tokens.
 constexpr int kManyWaves = 8;          // waves of 4 CTAs per SM
 
-static void split_plan(int C, int share_max, bool fp16, int64_t units, int max_seq_len, int req, int sms, int P,
+// Returns false when the request is too long for this kernel: a CTA holds at
+// most share_max tokens and a call runs at most kMaxSplits splits.
+constexpr int kMaxSplits = 4096;
+
+static bool split_plan(int C, int share_max, bool fp16, int64_t units, int max_seq_len, int req, int sms, int P,
                        Plan *pl) {
     const int max_pages_needed = (max_seq_len + P - 1) / P;
     int S = req;
@@ -122,9 +126,10 @@ static void split_plan(int C, int share_max, bool fp16, int64_t units, int max_s
         // each CTA of a cluster holds at most share_max tokens
         const int64_t need = (static_cast<int64_t>(max_seq_len) + static_cast<int64_t>(C) * share_max - 1) /
                              (static_cast<int64_t>(C) * share_max);
+        if (need > kMaxSplits) return false;
         if (S < need) S = static_cast<int>(need);
     }
-    if (S > 4096) S = 4096;
+    if (S > kMaxSplits) S = kMaxSplits;
     if (max_pages_needed == 0) S = 1;
     // split length: page multiple; recompute S so no trailing split is empty
     int split_pages = (max_pages_needed + S - 1) / S;
@@ -135,6 +140,7 @@ static void split_plan(int C, int share_max, bool fp16, int64_t units, int max_s
     pl->cluster = C;
     pl->split_len = split_pages * P;
     pl->share = ((pl->split_len + C - 1) / C + P - 1) / P * P;
+    return true;
 }
 
 // Which PQ kernel: AQPQ_DECODE_KERNEL=1 or 2 in the environment forces one
@@ -168,7 +174,7 @@ static bool attend_plan(int M, int G, int64_t units, int max_seq_len, int req, i
             if (want > S) S = want;
         }
     }
-    if (S > 4096) S = 4096;
+    if (S > kMaxSplits) S = kMaxSplits;
     if (pages == 0) S = 1;
     int split_pages = (pages + S - 1) / S;
     if (split_pages < 1) split_pages = 1;
@@ -208,9 +214,11 @@ static aq_status make_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv, 
     Plan p1{}, p1x{};
     aq_status st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1, !e4m3);
     if (st != AQ_OK) return st;
-    st = share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1x, e4m3);
-    if (st != AQ_OK) return st;
-    if (p1x.workspace > p1.workspace) p1.workspace = p1x.workspace;
+    // the other format's plan only widens the workspace; a length it cannot
+    // take is refused when a call of that format asks for it
+    if (share_plan(cfg, batch, Hq, Hkv, max_seq_len, req, fp16, sms, smem_cap, &p1x, e4m3) == AQ_OK &&
+        p1x.workspace > p1.workspace)
+        p1.workspace = p1x.workspace;
     Plan p2{};
     const int64_t units = static_cast<int64_t>(batch) * Hkv;
     const int forced = forced_kernel();
@@ -261,16 +269,20 @@ static aq_status share_plan(const aq_pq_config *cfg, int batch, int Hq, int Hkv,
         // shares of several chunks (streamed in two passes) for clusters of 4 or 8
         auto share_max = [&](int c) { return stream && c >= 4 ? chunk * kMaxStreamChunks : chunk; };
         const int64_t clusters = units * nsub;         // per split
-        split_plan(C, share_max(C), false, clusters, max_seq_len, req, sms, P, pl);
+        if (!split_plan(C, share_max(C), false, clusters, max_seq_len, req, sms, P, pl))
+            return AQ_ERR_UNSUPPORTED;
         const int64_t ctas = clusters * pl->num_splits * C;
+        // a re-plan replaces the first one only where it exists
+        Plan alt = *pl;
         if (C == 4 && ctas >= static_cast<int64_t>(kManyWaves) * sms * 4 &&
-            pq_decode_smem_bytes(M, Gs, 2) <= smem_cap)
-            split_plan(2, share_max(2), false, clusters, max_seq_len, req, sms, P, pl);
-        else if (C == 4 && M == 8 && pl->num_splits >= 2 && pq_decode_smem_bytes(M, Gs, 8) > 0 &&
-                 pq_decode_smem_bytes(M, Gs, 8) <= smem_cap)
+            pq_decode_smem_bytes(M, Gs, 2) <= smem_cap) {
+            if (split_plan(2, share_max(2), false, clusters, max_seq_len, req, sms, P, &alt)) *pl = alt;
+        } else if (C == 4 && M == 8 && pl->num_splits >= 2 && pq_decode_smem_bytes(M, Gs, 8) > 0 &&
+                   pq_decode_smem_bytes(M, Gs, 8) <= smem_cap) {
             // a long request with 8 subspaces: clusters of 8, one subspace per
             // CTA, half the splits and so half the per-split fixed work
-            split_plan(8, share_max(8), false, clusters, max_seq_len, req, sms, P, pl);
+            if (split_plan(8, share_max(8), false, clusters, max_seq_len, req, sms, P, &alt)) *pl = alt;
+        }
         pl->head_split = nsub;
         pl->smem = pq_decode_smem_bytes(M, Gs, pl->cluster);
     }
@@ -726,15 +738,17 @@ static aq_status mixed_plans(const aq_pq_config *cfg, int32_t batch, int32_t Hq,
         // the workspace covers the plan of either codebook format (the size
         // query does not know the format) and the token-share plan that
         // replaces the head-split one when the codebooks get no TMA view
+        // (a length one of those cannot take is refused by the call that needs it)
         Plan other{}, share{};
-        st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
-                       &other, !e4m3);
-        if (st != AQ_OK) return st;
-        st = make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
-                       &share, true, false);
-        if (st != AQ_OK) return st;
-        int s = ppq->num_splits > other.num_splits ? ppq->num_splits : other.num_splits;
-        if (share.num_splits > s) s = share.num_splits;
+        int s = ppq->num_splits;
+        if (make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
+                      &other, !e4m3) == AQ_OK &&
+            other.num_splits > s)
+            s = other.num_splits;
+        if (make_plan(cfg, batch, (Hkv - n16) * G, Hkv - n16, max_seq_len, 0, false, kPlanSMs, kPlanSmemCap,
+                      &share, true, false) == AQ_OK &&
+            share.num_splits > s)
+            s = share.num_splits;
         *ws += part_bytes(batch, Hq, s);
     }
     return AQ_OK;

@@ -223,7 +223,14 @@ aq_status aq_encode_append(const aq_pq_config *cfg, int32_t num_tokens,
  * `fp16` selects the plan of aq_decode_attention_fp16.
  * Two PQ kernels exist: one whose cluster CTAs split the tokens and merge
  * their value bins, and one whose CTAs each score every token of their split
- * (used for GQA groups of 4 or more query heads per kv head).  The
+ * (used for GQA groups of 4 or more query heads per kv head).
+ * A call runs at most 4096 splits and a CTA holds a bounded share of tokens,
+ * so a PQ call has a longest request it can take: beyond it this function
+ * and the decode calls return AQ_ERR_UNSUPPORTED (before any CUDA call).
+ * With M = 4 and one query head per kv head that is 2^29 tokens with fp16
+ * codebooks and 2^25 with E4M3 codebooks (which are not streamed); larger
+ * groups hold fewer tokens per CTA.  The fp16 comparison call has no such
+ * bound.  The
  * environment variable AQPQ_DECODE_KERNEL=1 or =2 forces the first or, where
  * its split fits, the second (read at every call; results agree within
  * rounding).

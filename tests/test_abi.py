@@ -266,3 +266,35 @@ def test_wrappers_reject_tensors_on_another_device():
     assert api._same_device(a, x=torch.zeros(2), y=None) == -1
     with pytest.raises(ValueError, match="cuda:1"):
         api._same_device(a, codebooks=OnDevice1())
+
+
+def test_lengths_beyond_the_split_limit_are_unsupported(lib):
+    """A CTA holds a bounded share of tokens and a call runs at most 4096
+    splits, so the longest request a plan can take is bounded: the planner
+    reports AQ_ERR_UNSUPPORTED beyond it (never a plan the launch would refuse),
+    and the decode calls return the same before any CUDA call.  M = 4 with one
+    query head per kv head holds 2048 tokens per CTA, 16 chunks of them when
+    streamed (fp16 codebooks, clusters of 4): 2^29 tokens at most; E4M3
+    codebooks stream nothing: 2^25 tokens at most."""
+    UNS = 2
+    s, c, w = _plan(lib, 1, 1, 1, 1 << 28)
+    assert s <= 4096 and c == 4 and w >= s * 130 * 4
+    assert _plan(lib, 1, 1, 1, 1 << 29)[:2] == (4096, 4)
+    cfg = _cfg()
+    out = (ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t())
+    r = lib.aq_decode_plan(ctypes.byref(cfg), 1, 1, 1, 1 << 30, 0, 0, *(ctypes.byref(x) for x in out))
+    assert r == UNS
+    r = lib.aq_decode_plan(ctypes.byref(_cfg(M=8)), 1, 1, 1, 1 << 29, 0, 0, *(ctypes.byref(x) for x in out))
+    assert r == UNS
+    assert _plan(lib, 1, 1, 1, 1 << 30, fp16=1)[0] >= 1        # the fp16 comparison plan has no such bound
+    # the calls themselves: rejected on the host.  Their pointers are fake, so
+    # they run only where no GPU could be reached if a regression let them pass
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        return
+    L = (1 << 30)
+    assert _decode(lib, _cfg(), B=1, Hq=1, Hkv=1, max_pages=L // 16, max_seq_len=L) == UNS
+    L = (1 << 25) + 16
+    r = lib.aq_decode_step(ctypes.byref(cfg), 1, 1, 1, FAKE, FAKE, FAKE, 64, FAKE, 1, FAKE, FAKE, L // 16 + 1,
+                           FAKE, L, 0.1, 0, 2, FAKE, FAKE, 1 << 30, None, None)   # AQ_STEP_E4M3
+    assert r == UNS
